@@ -1,0 +1,317 @@
+/*
+ * CPU oracle for the MXFP4 Mixture-of-Experts expert layer (fp64, plain C).
+ *
+ * TEST INFRASTRUCTURE ONLY: loaded by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg; never by the CUDA library, with which it
+ * shares no code.
+ *
+ * Sources of the definitions:
+ *  - Only the MoE expert weights are FP4, in the MXFP4 format with a block
+ *    size of 32 and a shared scale: ai.appwright.xyz, tag page "投機的デコード",
+ *    section "第1層：FP4量子化"; techllm.github.io, "Xiaomi MiMo and TileRT ...
+ *    1000 tokens per second", section "세 층의 속도 최적화 / 1. MXFP4".
+ *  - The layer runs on T = sequences x 8 tokens because DFlash verifies a
+ *    masked block of up to 8 positions in one forward: techllm.github.io,
+ *    section "2. DFlash"; dothoosh.com, section "جزئیات پیاده‌سازی DFlash".
+ *  - The parts the pages leave open are fixed by the layer specification this
+ *    repository implements: E2M1 grid {0,.5,1,1.5,2,3,4,6} with sign, E8M0
+ *    scale 2^(c-127) chosen as 2^(floor(log2(amax)) - 2), round to nearest
+ *    even with saturation at +-6; top-k with the lower expert index winning
+ *    ties; softmax renormalised over the k selected logits; SwiGLU
+ *    silu(gate) * up; bf16 output; MXFP8-E4M3 activations.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <omp.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ formats */
+
+/* E2M1: bit 3 sign, bits 2..1 exponent (bias 1), bit 0 mantissa.
+ * exponent 0 is subnormal: m * 0.5; otherwise (1 + m/2) * 2^(exp-1). */
+double oracle_e2m1_value(int code) {
+  int s = (code >> 3) & 1, ex = (code >> 1) & 3, m = code & 1;
+  double mag = (ex == 0) ? 0.5 * m : (1.0 + 0.5 * m) * ldexp(1.0, ex - 1);
+  return s ? -mag : mag;
+}
+
+/* E8M0: unsigned exponent, value 2^(code-127); 0xFF is NaN */
+double oracle_e8m0_value(int code) {
+  if (code == 255) return NAN;
+  return ldexp(1.0, code - 127);
+}
+
+/* E4M3 (finite-only variant): bit 7 sign, bits 6..3 exponent (bias 7),
+ * bits 2..0 mantissa; exponent 0 subnormal m/8 * 2^-6; S.1111.111 is NaN. */
+double oracle_e4m3_value(int code) {
+  int s = (code >> 7) & 1, ex = (code >> 3) & 15, m = code & 7;
+  if (ex == 15 && m == 7) return NAN;
+  double mag = (ex == 0) ? (m / 8.0) * ldexp(1.0, -6) : (1.0 + m / 8.0) * ldexp(1.0, ex - 7);
+  return s ? -mag : mag;
+}
+
+/* bf16: the upper 16 bits of an IEEE binary32 */
+double oracle_bf16_value(uint16_t bits) {
+  uint32_t u = (uint32_t)bits << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+int oracle_floor_log2_f32(float a) {
+  uint32_t u;
+  memcpy(&u, &a, 4);
+  int ex = (int)((u >> 23) & 0xFF);
+  if (ex > 0) return ex - 127;
+  uint32_t m = u & 0x7FFFFF; /* subnormal: m * 2^-149 */
+  int p = 0;
+  while ((m >> (p + 1)) != 0) ++p;
+  return p - 149;
+}
+
+/* nearest of the non-negative codes [0, n) of a decoder; ties to the even code */
+static int nearest_code(double a, int n, double (*dec)(int)) {
+  int best = 0;
+  double bd = fabs(a - dec(0));
+  for (int c = 1; c < n; ++c) {
+    double d = fabs(a - dec(c));
+    if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
+      best = c;
+      bd = d;
+    }
+  }
+  return best;
+}
+
+/* sign copied from the input's sign bit, so -0 and small negatives give code 8 */
+int oracle_e2m1_encode(double q) {
+  int neg = signbit(q) ? 1 : 0;
+  double a = fabs(q);
+  if (a >= 6.0) return (neg << 3) | 7; /* saturate */
+  return (neg << 3) | nearest_code(a, 8, oracle_e2m1_value);
+}
+
+int oracle_e4m3_encode(double q) {
+  int neg = signbit(q) ? 1 : 0;
+  double a = fabs(q);
+  if (a >= 448.0) return (neg << 7) | 0x7E; /* satfinite */
+  return (neg << 7) | nearest_code(a, 0x7F, oracle_e4m3_value);
+}
+
+uint16_t oracle_bf16_from_double(double v) {
+  if (isnan(v)) return 0x7FC0;
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (a == 0.0) return sign;
+  int ex2;
+  frexp(a, &ex2);
+  int e = ex2 - 1; /* floor(log2(a)) */
+  if (e < -126) e = -126;
+  double ulp = ldexp(1.0, e - 7); /* 8 significant bits */
+  double n = a / ulp;             /* exact */
+  double r = floor(n);
+  double fr = n - r;
+  if (fr > 0.5 || (fr == 0.5 && fmod(r, 2.0) != 0.0)) r += 1.0;
+  double rv = r * ulp;
+  if (rv >= 0x1p128) return sign | 0x7F80;
+  float f = (float)rv; /* exact: rv has <= 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, 4);
+  return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------------ quantization */
+
+static int clamp_scale_code(int e) {
+  int c = e + 127;
+  return c < 0 ? 0 : (c > 254 ? 254 : c);
+}
+
+/* MXFP4: per block of 32 along K, scale code = clamp(floor(log2(amax)) - 2 + 127),
+ * elements q = w / 2^(code-127) rounded to the E2M1 grid.  amax == 0 gives
+ * scale code 0.  Element 2i sits in the low nibble of byte i. */
+void oracle_mxfp4_quantize(const float* w, int64_t R, int64_t K, uint8_t* out_fp4,
+                           uint8_t* out_e8m0) {
+  const int64_t nb = K / 32;
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* blk = w + r * K + b * 32;
+      float amax = 0.0f;
+      for (int i = 0; i < 32; ++i) {
+        float a = fabsf(blk[i]);
+        if (a > amax) amax = a;
+      }
+      int code = (amax == 0.0f) ? 0 : clamp_scale_code(oracle_floor_log2_f32(amax) - 2);
+      out_e8m0[r * nb + b] = (uint8_t)code;
+      double X = oracle_e8m0_value(code);
+      for (int i = 0; i < 32; i += 2) {
+        int lo = oracle_e2m1_encode((double)blk[i] / X);
+        int hi = oracle_e2m1_encode((double)blk[i + 1] / X);
+        out_fp4[(r * K + b * 32 + i) / 2] = (uint8_t)(lo | (hi << 4));
+      }
+    }
+  }
+}
+
+/* MXFP8-E4M3: per block of 32, scale code = clamp(floor(log2(amax)) - 8 + 127)
+ * (8 = exponent of the largest power of two in E4M3), elements rounded to
+ * nearest even E4M3 with saturation at +-448.  amax == 0 gives scale code 0. */
+void oracle_mxfp8_quantize_row(const double* v, int64_t K, uint8_t* codes, uint8_t* scales) {
+  for (int64_t b = 0; b < K / 32; ++b) {
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      double a = fabs(v[b * 32 + i]);
+      if (a > amax) amax = a;
+    }
+    int code = 0;
+    if (amax > 0.0) {
+      int ex2;
+      frexp(amax, &ex2);
+      code = clamp_scale_code((ex2 - 1) - 8);
+    }
+    scales[b] = (uint8_t)code;
+    double X = oracle_e8m0_value(code);
+    for (int i = 0; i < 32; ++i) codes[b * 32 + i] = (uint8_t)oracle_e4m3_encode(v[b * 32 + i] / X);
+  }
+}
+
+/* act step of the given mode applied in place to a row of K doubles */
+static void apply_act(double* v, int64_t K, int act_mode, uint8_t* tmp_codes, uint8_t* tmp_sc) {
+  if (act_mode == ORACLE_ACT_MXFP8) {
+    oracle_mxfp8_quantize_row(v, K, tmp_codes, tmp_sc);
+    for (int64_t i = 0; i < K; ++i)
+      v[i] = oracle_e4m3_value(tmp_codes[i]) * oracle_e8m0_value(tmp_sc[i / 32]);
+  } else if (act_mode == ORACLE_ACT_BF16) {
+    for (int64_t i = 0; i < K; ++i) v[i] = oracle_bf16_value(oracle_bf16_from_double(v[i]));
+  }
+}
+
+/* ------------------------------------------------------------------ routing */
+
+void oracle_route(const float* logits, int64_t T, int64_t E, int k, int32_t* idx,
+                  double* gate) {
+  char* taken = (char*)malloc((size_t)E);
+  for (int64_t t = 0; t < T; ++t) {
+    const float* l = logits + t * E;
+    memset(taken, 0, (size_t)E);
+    for (int j = 0; j < k; ++j) {
+      int64_t best = -1;
+      for (int64_t e = 0; e < E; ++e) {
+        if (taken[e]) continue;
+        if (best < 0 || l[e] > l[best]) best = e; /* strict: lower index keeps ties */
+      }
+      taken[best] = 1;
+      idx[t * k + j] = (int32_t)best;
+    }
+    double m = (double)l[idx[t * k]];
+    double s = 0.0;
+    for (int j = 0; j < k; ++j) s += exp((double)l[idx[t * k + j]] - m);
+    for (int j = 0; j < k; ++j) gate[t * k + j] = exp((double)l[idx[t * k + j]] - m) / s;
+  }
+  free(taken);
+}
+
+void oracle_route_arrays(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* cnt,
+                         int32_t* off, int32_t* perm, int32_t* pos) {
+  for (int64_t e = 0; e < E; ++e) cnt[e] = 0;
+  for (int64_t f = 0; f < T * k; ++f) cnt[idx[f]]++;
+  off[0] = 0;
+  for (int64_t e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+  int32_t* fill = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+  for (int64_t f = 0; f < T * k; ++f) { /* ascending flat index t*k + j */
+    int32_t e = idx[f];
+    int32_t p = off[e] + fill[e]++;
+    perm[p] = (int32_t)(f / k);
+    pos[f] = p;
+  }
+  free(fill);
+}
+
+/* ------------------------------------------------------------------ forward */
+
+static double g_e2m1[16];
+static double g_e8m0[256];
+static int g_tables_ready = 0;
+
+static void init_tables(void) {
+  if (g_tables_ready) return;
+  for (int c = 0; c < 16; ++c) g_e2m1[c] = oracle_e2m1_value(c);
+  for (int c = 0; c < 256; ++c) g_e8m0[c] = oracle_e8m0_value(c);
+  g_tables_ready = 1;
+}
+
+/* decoded weight element (row r, column c) of a packed matrix with K columns */
+static inline double wval(const uint8_t* fp4, const uint8_t* e8m0, int64_t K, int64_t r,
+                          int64_t c) {
+  uint8_t byte = fp4[(r * K + c) >> 1];
+  int nib = (c & 1) ? (byte >> 4) : (byte & 0xF);
+  return g_e2m1[nib] * g_e8m0[e8m0[r * (K / 32) + c / 32]];
+}
+
+static double silu(double z) { return z / (1.0 + exp(-z)); }
+
+int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
+                       const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                       const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int64_t T, int64_t H,
+                       int64_t I, int64_t E, int k, int act_mode, const int64_t* tokens,
+                       int64_t n_tokens, double* y_f64, uint16_t* y_bf16, double* h_out,
+                       int n_threads) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k < 1 || k > E || H % 32 || I % 32) return -1;
+  if (act_mode < 0 || act_mode > 2) return -1;
+  if (!tokens) n_tokens = T;
+  init_tables();
+
+#pragma omp parallel num_threads(n_threads > 0 ? n_threads : omp_get_max_threads())
+  {
+    double* a = (double*)malloc(sizeof(double) * (size_t)H);
+    double* hv = (double*)malloc(sizeof(double) * (size_t)I);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
+    uint8_t* tc = (uint8_t*)malloc((size_t)(H > I ? H : I));
+    uint8_t* ts = (uint8_t*)malloc((size_t)(H > I ? H : I) / 32);
+    int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
+    double* g = (double*)malloc(sizeof(double) * (size_t)k);
+
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t n = 0; n < n_tokens; ++n) {
+      int64_t t = tokens ? tokens[n] : n;
+      for (int64_t h = 0; h < H; ++h) a[h] = oracle_bf16_value(x_bf16[t * H + h]);
+      apply_act(a, H, act_mode == ORACLE_ACT_MXFP8 ? ORACLE_ACT_MXFP8 : ORACLE_ACT_EXACT, tc, ts);
+      oracle_route(router_logits + t * E, 1, E, k, idx, g);
+      for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
+      for (int j = 0; j < k; ++j) {
+        int64_t e = idx[j];
+        const int64_t r0 = e * 2 * I; /* first w13 row of expert e */
+        for (int64_t i = 0; i < I; ++i) {
+          double gate = 0.0, up = 0.0;
+          for (int64_t h = 0; h < H; ++h) {
+            gate += wval(w13_fp4, w13_e8m0, H, r0 + i, h) * a[h];
+            up += wval(w13_fp4, w13_e8m0, H, r0 + I + i, h) * a[h];
+          }
+          hv[i] = silu(gate) * up;
+        }
+        apply_act(hv, I, act_mode, tc, ts);
+        if (h_out)
+          for (int64_t i = 0; i < I; ++i) h_out[(n * k + j) * I + i] = hv[i];
+        for (int64_t o = 0; o < H; ++o) {
+          double d = 0.0;
+          for (int64_t i = 0; i < I; ++i) d += wval(w2_fp4, w2_e8m0, I, e * H + o, i) * hv[i];
+          acc[o] += g[j] * d;
+        }
+      }
+      for (int64_t h = 0; h < H; ++h) {
+        if (y_f64) y_f64[n * H + h] = acc[h];
+        if (y_bf16) y_bf16[n * H + h] = oracle_bf16_from_double(acc[h]);
+      }
+    }
+    free(a);
+    free(hv);
+    free(acc);
+    free(tc);
+    free(ts);
+    free(idx);
+    free(g);
+  }
+  return 0;
+}

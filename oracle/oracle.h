@@ -1,0 +1,85 @@
+/*
+ * CPU oracle for the MXFP4 Mixture-of-Experts expert layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Plain, slow, fp64 C that states the layer's
+ * definition directly.  Only the tests, the smoke check and the benchmark's
+ * CPU-baseline leg may load it; the CUDA library never does, and the two
+ * share no code, header, table or helper.
+ *
+ * What the layer computes (per token t, with W1 = rows [0,I) of w13 and
+ * W3 = rows [I,2I) of w13, every weight decoded exactly as
+ * e2m1(code) * 2^(scale - 127)):
+ *
+ *   (e_j, g_j)_{j<k} = top-k of router_logits[t] (ties: lower expert index
+ *                      first), g = softmax over the k selected logits
+ *   y[t] = bf16_RNE( sum_j g_j * W2_{e_j} act2( silu(W1_{e_j} act1(x_t))
+ *                                               * (W3_{e_j} act1(x_t)) ) )
+ *
+ * act1/act2 are the identity in exact mode, MXFP8 (E4M3 elements, E8M0 scale
+ * per 32 along the reduction dimension) in MXFP8-emulation mode, and bf16
+ * rounding of the intermediate in bf16-emulation mode.
+ *
+ * Parity pins: every function below is checked by the CPU test-suite against
+ * closed forms, format tables, library routines or brute force (see the
+ * tests named test_oracle_*).  No function here is unpinned.
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ORACLE_ACT_EXACT 0
+#define ORACLE_ACT_MXFP8 1
+#define ORACLE_ACT_BF16 2
+
+/* format decoders: exact values */
+double oracle_e2m1_value(int code);   /* code in [0,16) */
+double oracle_e8m0_value(int code);   /* code in [0,255): 2^(code-127); 255 -> NaN */
+double oracle_e4m3_value(int code);   /* code in [0,256); 0x7F/0xFF -> NaN */
+double oracle_bf16_value(uint16_t bits);
+
+/* exact floor(log2(a)) of a positive finite fp32, read from its bits */
+int oracle_floor_log2_f32(float a);
+
+/* encoders: round to nearest, ties to the even code, saturating */
+int oracle_e2m1_encode(double q);
+int oracle_e4m3_encode(double q);
+uint16_t oracle_bf16_from_double(double v);
+
+/* MXFP4 packing of fp32 rows [R, K] (K % 32 == 0) */
+void oracle_mxfp4_quantize(const float* w, int64_t R, int64_t K, uint8_t* out_fp4,
+                           uint8_t* out_e8m0);
+
+/* MXFP8 (E4M3) quantization of one row of K doubles (K % 32 == 0) */
+void oracle_mxfp8_quantize_row(const double* v, int64_t K, uint8_t* codes, uint8_t* scales);
+
+/* routing: top-k + renormalised softmax; idx [T,k] int32, gate [T,k] fp64 */
+void oracle_route(const float* logits, int64_t T, int64_t E, int k, int32_t* idx,
+                  double* gate);
+
+/* stable counting sort of the (t, j) assignments by expert:
+ * cnt[E], off[E+1], perm[T*k] (slot -> token), pos[T*k] (t*k+j -> slot) */
+void oracle_route_arrays(const int32_t* idx, int64_t T, int k, int64_t E, int32_t* cnt,
+                         int32_t* off, int32_t* perm, int32_t* pos);
+
+/* The layer.  tokens (n_tokens entries) selects which rows of y to compute;
+ * NULL means all T rows in order.  y_f64 [n_tokens, H] (before the final
+ * bf16 rounding), y_bf16 [n_tokens, H], h_out [n_tokens, k, I] (act2 output)
+ * may each be NULL.  n_threads <= 0 uses the OpenMP default.
+ * Returns 0, or -1 on invalid arguments. */
+int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
+                       const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                       const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int64_t T, int64_t H,
+                       int64_t I, int64_t E, int k, int act_mode, const int64_t* tokens,
+                       int64_t n_tokens, double* y_f64, uint16_t* y_bf16, double* h_out,
+                       int n_threads);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

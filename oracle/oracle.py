@@ -1,0 +1,134 @@
+"""ctypes binding of the fp64 CPU oracle (``liboracle.so``).
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py``.  The CUDA library never imports it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB = os.path.join(_HERE, "liboracle.so")
+
+ACT_EXACT, ACT_MXFP8, ACT_BF16 = 0, 1, 2
+
+
+def build() -> None:
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-ffp-contract=off", "-fopenmp",
+                           "-shared", "-fPIC", "-o", LIB, os.path.join(_HERE, "oracle.c"), "-lm"])
+
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            build()
+        L = ctypes.CDLL(LIB)
+        vp, i64, i32, d = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+        for name in ("oracle_e2m1_value", "oracle_e8m0_value", "oracle_e4m3_value"):
+            getattr(L, name).restype = d
+            getattr(L, name).argtypes = [i32]
+        L.oracle_bf16_value.restype = d
+        L.oracle_bf16_value.argtypes = [ctypes.c_uint16]
+        L.oracle_floor_log2_f32.restype = i32
+        L.oracle_floor_log2_f32.argtypes = [ctypes.c_float]
+        L.oracle_e2m1_encode.restype = i32
+        L.oracle_e2m1_encode.argtypes = [d]
+        L.oracle_e4m3_encode.restype = i32
+        L.oracle_e4m3_encode.argtypes = [d]
+        L.oracle_bf16_from_double.restype = ctypes.c_uint16
+        L.oracle_bf16_from_double.argtypes = [d]
+        L.oracle_mxfp4_quantize.restype = None
+        L.oracle_mxfp4_quantize.argtypes = [vp, i64, i64, vp, vp]
+        L.oracle_mxfp8_quantize_row.restype = None
+        L.oracle_mxfp8_quantize_row.argtypes = [vp, i64, vp, vp]
+        L.oracle_route.restype = None
+        L.oracle_route.argtypes = [vp, i64, i64, i32, vp, vp]
+        L.oracle_route_arrays.restype = None
+        L.oracle_route_arrays.argtypes = [vp, i64, i32, i64, vp, vp, vp, vp]
+        L.oracle_moe_forward.restype = i32
+        L.oracle_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
+                                         vp, i64, vp, vp, vp, i32]
+        _lib = L
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def e2m1_value(c): return lib().oracle_e2m1_value(int(c))
+def e8m0_value(c): return lib().oracle_e8m0_value(int(c))
+def e4m3_value(c): return lib().oracle_e4m3_value(int(c))
+def bf16_value(b): return lib().oracle_bf16_value(int(b))
+def floor_log2_f32(a): return lib().oracle_floor_log2_f32(float(a))
+def e2m1_encode(q): return lib().oracle_e2m1_encode(float(q))
+def e4m3_encode(q): return lib().oracle_e4m3_encode(float(q))
+def bf16_from_double(v): return lib().oracle_bf16_from_double(float(v))
+
+
+def mxfp4_quantize(w: np.ndarray):
+    """fp32 [R, K] -> (packed E2M1 [R, K/2] uint8, E8M0 [R, K/32] uint8)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    R = w.size // K
+    fp4 = np.empty(w.shape[:-1] + (K // 2,), dtype=np.uint8)
+    sc = np.empty(w.shape[:-1] + (K // 32,), dtype=np.uint8)
+    lib().oracle_mxfp4_quantize(_p(w), R, K, _p(fp4), _p(sc))
+    return fp4, sc
+
+
+def mxfp8_quantize_row(v: np.ndarray):
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    codes = np.empty(v.shape[0], dtype=np.uint8)
+    sc = np.empty(v.shape[0] // 32, dtype=np.uint8)
+    lib().oracle_mxfp8_quantize_row(_p(v), v.shape[0], _p(codes), _p(sc))
+    return codes, sc
+
+
+def route(logits: np.ndarray, k: int):
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    idx = np.empty((T, k), dtype=np.int32)
+    gate = np.empty((T, k), dtype=np.float64)
+    lib().oracle_route(_p(logits), T, E, k, _p(idx), _p(gate))
+    return idx, gate
+
+
+def route_arrays(idx: np.ndarray, E: int):
+    idx = np.ascontiguousarray(idx, dtype=np.int32)
+    T, k = idx.shape
+    cnt = np.empty(E, dtype=np.int32)
+    off = np.empty(E + 1, dtype=np.int32)
+    perm = np.empty(T * k, dtype=np.int32)
+    pos = np.empty(T * k, dtype=np.int32)
+    lib().oracle_route_arrays(_p(idx), T, k, E, _p(cnt), _p(off), _p(perm), _p(pos))
+    return cnt, off, perm, pos
+
+
+def moe_forward(x_bf16, logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, k, act_mode=ACT_EXACT,
+                tokens=None, want_h=False, n_threads=0):
+    """Returns (y_bf16 uint16 [n, H], y_f64 [n, H], h [n, k, I] or None)."""
+    x_bf16 = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, H = x_bf16.shape
+    E = logits.shape[1]
+    I = w2_fp4.shape[-1] * 2
+    tok = None if tokens is None else np.ascontiguousarray(tokens, dtype=np.int64)
+    n = T if tok is None else tok.shape[0]
+    y16 = np.empty((n, H), dtype=np.uint16)
+    y64 = np.empty((n, H), dtype=np.float64)
+    h = np.empty((n, k, I), dtype=np.float64) if want_h else None
+    arrs = [np.ascontiguousarray(a, dtype=np.uint8) for a in (w13_fp4, w13_e8m0, w2_fp4, w2_e8m0)]
+    rc = lib().oracle_moe_forward(_p(x_bf16), _p(logits), *(_p(a) for a in arrs), T, H, I, E, k,
+                                  act_mode, _p(tok), n, _p(y64), _p(y16), _p(h), n_threads)
+    if rc != 0:
+        raise ValueError(f"oracle_moe_forward rejected the arguments ({rc})")
+    return y16, y64, h

@@ -1,0 +1,140 @@
+"""Seeded synthetic inputs for the MXFP4 MoE layer (test and benchmark infrastructure).
+
+The generator is counter-based and integer-only (definitions in ``synth_core.h``), so the
+host library (``libsynth.so``) and the device library (``libsynth_dev.so``) produce the same
+bits.  It holds none of the layer's arithmetic; packing the fp32 weights to MXFP4 is done by
+whichever side (the oracle or the CUDA library) is under test.
+
+Workload recipe (shapes and value distributions of the layers this repository measures):
+  x       [T, H]  bf16 RNE of a unit-variance draw           (tensor id 0)
+  logits  [T, E]  fp32 unit-variance draw, optional Zipf bias (tensor id 1)
+  w13     [E, 2I, H] fp32 draw with sigma 0.02 before packing (tensor id 2)
+  w2      [E, H, I]  fp32 draw with sigma 0.02 before packing (tensor id 3)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+HOST_LIB = os.path.join(_HERE, "libsynth.so")
+DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
+
+ID_X, ID_LOGITS, ID_W13, ID_W2 = 0, 1, 2, 3
+W_SIGMA = 0.02
+
+
+def build(device: bool = True) -> None:
+    """Compile the host generator (gcc) and, if ``device``, its CUDA twin (nvcc, sm_103a)."""
+    src = os.path.join(_HERE, "synth.c")
+    subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fopenmp", "-shared",
+                           "-fPIC", "-o", HOST_LIB, src, "-lm"])
+    if device:
+        subprocess.check_call(["nvcc", "-O3", "-std=c++17", "-gencode",
+                               "arch=compute_103a,code=sm_103a", "-lineinfo", "-shared",
+                               "-Xcompiler", "-fPIC", "-cudart", "shared", "-o", DEV_LIB,
+                               os.path.join(_HERE, "synth_dev.cu")])
+
+
+_host = None
+_dev = None
+
+
+def _host_lib():
+    global _host
+    if _host is None:
+        if not os.path.exists(HOST_LIB):
+            build(device=False)
+        lib = ctypes.CDLL(HOST_LIB)
+        u64, u32, i64 = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int64
+        lib.synth_splitmix_out.restype = u64
+        lib.synth_splitmix_out.argtypes = [u64, u64]
+        lib.synth_z_numerator.restype = ctypes.c_int32
+        lib.synth_z_numerator.argtypes = [u64, u32, u64]
+        lib.synth_fill_normal_f32.restype = None
+        lib.synth_fill_normal_f32.argtypes = [u64, u32, u64, u64, ctypes.c_float, ctypes.c_void_p]
+        lib.synth_fill_x_bf16.restype = None
+        lib.synth_fill_x_bf16.argtypes = [u64, i64, i64, ctypes.c_void_p]
+        lib.synth_fill_logits.restype = None
+        lib.synth_fill_logits.argtypes = [u64, i64, i64, ctypes.c_int, ctypes.c_void_p]
+        _host = lib
+    return _host
+
+
+def _dev_lib():
+    global _dev
+    if _dev is None:
+        if not os.path.exists(DEV_LIB):
+            raise RuntimeError(f"{DEV_LIB} is not built; run __graft_entry__.build()")
+        lib = ctypes.CDLL(DEV_LIB)
+        lib.synth_dev_fill_normal_f32.restype = ctypes.c_int
+        lib.synth_dev_fill_normal_f32.argtypes = [ctypes.c_uint64, ctypes.c_uint32,
+                                                  ctypes.c_uint64, ctypes.c_uint64,
+                                                  ctypes.c_float, ctypes.c_void_p,
+                                                  ctypes.c_void_p]
+        _dev = lib
+    return _dev
+
+
+def splitmix_out(seed: int, n: int) -> int:
+    """n-th output (n >= 1) of SplitMix64 seeded with ``seed``."""
+    return int(_host_lib().synth_splitmix_out(seed, n))
+
+
+def z_numerator(seed: int, tensor_id: int, i: int) -> int:
+    return int(_host_lib().synth_z_numerator(seed, tensor_id, i))
+
+
+def normal_f32(seed: int, tensor_id: int, start: int, n: int, sigma: float) -> np.ndarray:
+    out = np.empty(n, dtype=np.float32)
+    if n:
+        _host_lib().synth_fill_normal_f32(seed, tensor_id, start, n, sigma,
+                                          out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def x_bf16(seed: int, T: int, H: int) -> np.ndarray:
+    """[T, H] bf16 bit patterns (uint16)."""
+    out = np.empty((T, H), dtype=np.uint16)
+    if T * H:
+        _host_lib().synth_fill_x_bf16(seed, T, H, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def logits(seed: int, T: int, E: int, zipf: bool = False) -> np.ndarray:
+    out = np.empty((T, E), dtype=np.float32)
+    if T * E:
+        _host_lib().synth_fill_logits(seed, T, E, int(zipf), out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def w13_f32(seed: int, E: int, I: int, H: int, experts=None) -> np.ndarray:
+    """fp32 gate/up weights [E, 2I, H] (only ``experts`` filled if given, rest zero)."""
+    out = np.zeros((E, 2 * I, H), dtype=np.float32)
+    for e in (range(E) if experts is None else experts):
+        n = 2 * I * H
+        _host_lib().synth_fill_normal_f32(seed, ID_W13, e * n, n, W_SIGMA,
+                                          out[e].ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def w2_f32(seed: int, E: int, H: int, I: int, experts=None) -> np.ndarray:
+    """fp32 down weights [E, H, I] (only ``experts`` filled if given, rest zero)."""
+    out = np.zeros((E, H, I), dtype=np.float32)
+    for e in (range(E) if experts is None else experts):
+        n = H * I
+        _host_lib().synth_fill_normal_f32(seed, ID_W2, e * n, n, W_SIGMA,
+                                          out[e].ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def dev_fill_normal_f32(seed: int, tensor_id: int, start: int, n: int, sigma: float,
+                        dev_ptr: int, stream: int = 0) -> None:
+    """Device twin of ``normal_f32``: writes n fp32 values to device memory at ``dev_ptr``."""
+    rc = _dev_lib().synth_dev_fill_normal_f32(seed, tensor_id, start, n, sigma,
+                                              ctypes.c_void_p(dev_ptr), ctypes.c_void_p(stream))
+    if rc != 0:
+        raise RuntimeError(f"synth_dev_fill_normal_f32 failed ({rc})")

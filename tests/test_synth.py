@@ -1,0 +1,47 @@
+"""The seeded input generator: published SplitMix64 outputs, moments, determinism, shapes."""
+import math
+
+import numpy as np
+
+from conftest import read_golden
+
+
+def test_splitmix64_published_outputs(synth_mod):
+    for n, hexv in read_golden("splitmix64_seed0.txt"):
+        assert synth_mod.splitmix_out(0, int(n)) == int(hexv, 16)
+
+
+def test_normal_moments_and_support(synth_mod):
+    z = synth_mod.normal_f32(5, 2, 0, 400000, 1.0).astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.var() - 1.0) < 0.01
+    assert np.abs(z).max() <= 6.0
+    # exact multiples of 2^-16
+    assert (z * 65536 == np.round(z * 65536)).all()
+    k = ((z ** 4).mean()) / z.var() ** 2
+    assert 2.8 < k < 3.0          # Irwin-Hall(12) kurtosis 2.9
+
+
+def test_streams_are_counter_based(synth_mod):
+    a = synth_mod.normal_f32(3, 2, 1000, 50, 0.02)
+    b = synth_mod.normal_f32(3, 2, 0, 1050, 0.02)[1000:]
+    assert (a == b).all()
+    assert not (synth_mod.normal_f32(3, 3, 1000, 50, 0.02) == a).all()
+    assert not (synth_mod.normal_f32(4, 2, 1000, 50, 0.02) == a).all()
+    num = synth_mod.z_numerator(3, 2, 1000)
+    assert a[0] == np.float32(np.float32(num / 65536.0) * np.float32(0.02))
+
+
+def test_x_is_bf16_of_unit_draw(synth_mod):
+    x = synth_mod.x_bf16(1, 4, 64)
+    z = synth_mod.normal_f32(1, 0, 0, 256, 1.0).reshape(4, 64)
+    back = (x.astype(np.uint32) << 16).view(np.float32)
+    assert np.all(np.abs(back - z) <= np.abs(z) * 2.0 ** -8 + 1e-30)
+
+
+def test_zipf_bias(synth_mod):
+    E = 384
+    a = synth_mod.logits(4, 8, E, zipf=False)
+    b = synth_mod.logits(4, 8, E, zipf=True)
+    bias = np.array([3.0 * math.log(1.0 / (e + 1)) for e in range(E)])
+    assert np.allclose(b - a, bias[None, :], atol=1e-5)
+    assert b[:, 0].mean() > b[:, -1].mean()

@@ -1,0 +1,386 @@
+#!/usr/bin/env python3
+"""Benchmark of the MXFP4 MoE expert layer at DFlash verification token counts.
+
+Metric: MoE-layer tokens/s at T = 256 (32 sequences x a DFlash block of 8) on the full-shape
+layer (H=6144, I=2048, E=384, top-8), plus achieved HBM GB/s as a fraction of the measured
+B300 peak.  One JSON line on stdout (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--layer NAME]
+
+ours       K forward calls through the C ABI with all inputs resident in HBM (the 7.7 GB of
+           packed weights exceed L2, so no L2 flush is needed), timed with CUDA events on the
+           launching stream; then K end-to-end calls with host buffers (pinned x and logits
+           copied in, y copied out, inside the timed region); then the CPU oracle on a bounded
+           sample (rank 0, N = 1).
+reference  the fp64 CPU oracle on the host cores, each step a bounded sample of the workload.
+N > 1      one process per GPU (torchrun); each rank runs an independent replica of the layer
+           (the layer needs no exchange on one GPU), value = all ranks' tokens / max time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at T=256; achieved HBM GB/s as fraction of B300 peak"
+UNIT = "tokens/s"
+PEAK_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f)
+                  for f in sorted(os.listdir(os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300",
+                                                          "csrc")))
+                  if f.endswith((".cu", ".cuh"))]
+STEP_NAMES = ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(PEAK_FALLBACK), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def layer_bytes(L, cnt):
+    """Algorithmic bytes: touched experts' packed weights + scales, x, logits and y."""
+    touched = int((cnt > 0).sum())
+    w13 = 2 * L.I * L.H // 2 + 2 * L.I * L.H // 32
+    w2 = L.H * L.I // 2 + L.H * L.I // 32
+    act = L.T * L.H * 2 + L.T * L.E * 4 + L.T * L.H * 2
+    return touched, touched * w13, touched * w2, touched * (w13 + w2) + act
+
+
+# ------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
+                stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------- events
+
+class Events:
+    """Raw cudaEvent_t handles (the library records step markers into them)."""
+
+    def __init__(self):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+
+    def create(self, n):
+        arr = (ctypes.c_void_p * n)()
+        for i in range(n):
+            h = ctypes.c_void_p()
+            assert self.rt.cudaEventCreate(ctypes.byref(h)) == 0
+            arr[i] = h
+        return arr
+
+    def elapsed_ms(self, a, b) -> float:
+        ms = ctypes.c_float()
+        assert self.rt.cudaEventElapsedTime(ctypes.byref(ms), a, b) == 0
+        return float(ms.value)
+
+    def destroy(self, arr):
+        for h in arr:
+            self.rt.cudaEventDestroy(h)
+
+
+# ------------------------------------------------------------------------- oracle leg
+
+def oracle_sample(L, n_tokens: int):
+    """Prepare the oracle's inputs for the first n_tokens tokens (packing excluded from any
+    timing): returns a closure that runs the oracle on a list of token indices."""
+    from oracle import oracle as O
+    from synth import layers as LY
+    x, lg = LY.host_x(L), LY.host_logits(L)
+    toks = np.arange(min(n_tokens, L.T))
+    ridx, _ = O.route(lg[toks], L.k)
+    w = LY.host_packed_weights(L, O.mxfp4_quantize, np.unique(ridx))
+
+    def run(tokens):
+        O.moe_forward(x, lg, *w, L.k, O.ACT_MXFP8, tokens=np.asarray(tokens, dtype=np.int64))
+    return run, int(np.unique(ridx).size)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, L, rank):
+    if rank != 0:
+        return
+    n_tok = 8
+    log(f"[reference] preparing oracle inputs for {n_tok} tokens of {L.name}")
+    run, n_exp = oracle_sample(L, n_tok)
+    for i in range(args.warmup):
+        run([i % n_tok])
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run([i % n_tok])
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cores = cpu_cores()
+    sample = (f"one token per step (cycling through the first {n_tok} tokens of the layer, "
+              f"{n_exp} experts), fp64 oracle in MXFP8-emulation mode; MXFP4 packing excluded")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{L.name}: {L.desc}", "parallelism": "host threads"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+# ------------------------------------------------------------------------- our path
+
+def run_ours(args, L, rank, world, local_rank):
+    import torch
+    import mxfp4_expert_layer_dflash_b300 as moe
+    from synth import layers as LY
+
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    log(f"[rank {rank}] building {L.name} on cuda:{local_rank}")
+    x_h, lg_h = LY.host_x(L), LY.host_logits(L)
+    x = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).cuda()
+    lg = torch.from_numpy(lg_h).cuda()
+    w13, s13, w2, s2 = LY.device_packed_weights(L, moe.mxfp4_quantize)
+    y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    # routing counts for the byte model (the library's own routing)
+    cnt = torch.empty(L.E, dtype=torch.int32, device="cuda")
+    tk = [torch.empty(L.T * L.k, dtype=dt, device="cuda")
+          for dt in (torch.int32, torch.float32)]
+    aux = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (L.E + 1, L.T * L.k,
+                                                                       L.T * L.k)]
+    moe.moe_mxfp4_route(lg, L.T, L.E, L.k, tk[0], tk[1], cnt, *aux)
+    touched, b_gemm1, b_gemm2, b_layer = layer_bytes(L, cnt.cpu().numpy())
+
+    ev = Events()
+    nsteps = len(STEP_NAMES) + 1
+    marks = [ev.create(nsteps) for _ in range(args.steps)]
+
+    def fwd(step_events=None):
+        moe.moe_mxfp4_forward_ex(x, lg, w13, s13, w2, s2, L.T, L.H, L.I, L.E, L.k, y, stream,
+                                 step_events=step_events)
+
+    for _ in range(args.warmup):
+        fwd()
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = moe.moe_mxfp4_launch_count()
+    with ClockSampler(local_rank) as clk:
+        start.record(stream)
+        for i in range(args.steps):
+            fwd(marks[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    launches = moe.moe_mxfp4_launch_count() - launches0
+    if dist:
+        dist.barrier()
+    ms = start.elapsed_time(stop) / args.steps
+    status = moe.moe_mxfp4_get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+
+    per_step = {n: [] for n in STEP_NAMES}
+    for m in marks:
+        for j, n in enumerate(STEP_NAMES):
+            per_step[n].append(ev.elapsed_ms(m[j], m[j + 1]))
+    step_ms = {n: statistics.mean(v) for n, v in per_step.items()}
+    for m in marks:
+        ev.destroy(m)
+
+    # end-to-end through the public API with host buffers
+    x_pin = torch.from_numpy(x_h.view(np.int16)).view(torch.bfloat16).pin_memory()
+    lg_pin = torch.from_numpy(lg_h).pin_memory()
+    y_pin = torch.empty((L.T, L.H), dtype=torch.bfloat16).pin_memory()
+    h2d = x_pin.numel() * 2 + lg_pin.numel() * 4
+    d2h = y_pin.numel() * 2
+    for _ in range(args.warmup):
+        x.copy_(x_pin, non_blocking=True)
+        lg.copy_(lg_pin, non_blocking=True)
+        fwd()
+        y_pin.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e_start, e_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_pin, non_blocking=True)
+        lg.copy_(lg_pin, non_blocking=True)
+        fwd()
+        y_pin.copy_(y, non_blocking=True)
+    e_stop.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_stop) / args.steps
+
+    # max over ranks
+    if dist:
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = t.tolist()
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return
+
+    pk, pk_src = peaks()
+    hbm = float(pk["hbm_gbs"])
+    dominant = max(("gemm1", "gemm2"), key=lambda n: step_ms[n])
+    dom_bytes = b_gemm1 if dominant == "gemm1" else b_gemm2
+    achieved = dom_bytes / (step_ms[dominant] * 1e-3) / 1e9
+    traffic = None
+    if os.path.exists(TRAFFIC_FILE):
+        tf = json.load(open(TRAFFIC_FILE))
+        ent = tf.get(dominant)
+        if ent and tf.get("source_sha") == kernel_source_sha() and tf.get("layer") == L.name:
+            traffic = ent.get("dram_bytes_per_launch")
+    layer_gbs = b_layer / (ms * 1e-3) / 1e9
+
+    out = {
+        "metric": METRIC, "value": world * L.T / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e2m1xe4m3->f32", "data": "synthetic",
+        "config": {"workload": f"{L.name}: {L.desc}", "global_batch": world * L.T,
+                   "seq_len": 8, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (packed weights %.2f GB)" % (b_layer / 1e9),
+                   "touched_experts": touched, "act_mode": "mxfp8"},
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
+                     "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
+                     "peak_source": f"{pk_src} hbm_gbs", "algorithmic_bytes": dom_bytes},
+        "layer_roofline": {"achieved": layer_gbs, "peak": hbm, "unit": "GB/s",
+                           "frac": layer_gbs / hbm, "algorithmic_bytes": b_layer,
+                           "us_per_layer": ms * 1e3},
+        "step_ms": step_ms,
+        "gpu_launches": int(launches),
+        "e2e": {"value": world * L.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        log("[rank 0] timing the CPU oracle on a bounded sample")
+        n_tok = args.cpu_tokens
+        run, n_exp = oracle_sample(L, n_tok)
+        t0 = time.perf_counter()
+        run(list(range(min(n_tok, L.T))))
+        dt = time.perf_counter() - t0
+        out["cpu_baseline"] = {
+            "value": min(n_tok, L.T) / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {min(n_tok, L.T)} of {L.T} tokens ({n_exp} experts), fp64 oracle "
+                      f"in MXFP8-emulation mode, {dt:.2f} s; MXFP4 packing excluded"}
+    print(json.dumps(out), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--layer", default="full_t256")
+    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from synth import layers as LY
+    L = LY.LAYERS[args.layer]
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    if args.impl == "reference":
+        run_reference(args, L, rank)
+    else:
+        run_ours(args, L, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,194 @@
+/*
+ * moe_mxfp4.h — C ABI of libmoe_mxfp4.so: the MXFP4-weight Mixture-of-Experts
+ * expert layer, run at DFlash verification token counts, on one B300
+ * (sm_103a).
+ *
+ * What the layer is (sources):
+ *  - MoE expert weights in MXFP4 (FP4 elements, block size 32, shared
+ *    scale); everything outside the experts stays at higher precision:
+ *    ai.appwright.xyz, tag page "投機的デコード", section "第1層：FP4量子化";
+ *    techllm.github.io, "Xiaomi MiMo and TileRT push a 1-trillion-parameter
+ *    model past 1000 tokens per second", section "1. MXFP4 — MoE에만 걸린
+ *    양자화"; dothoosh.com, section "موتور فنی: کوانتیزاسیون و DFlash".
+ *  - Token count: DFlash fills a masked block of up to 8 positions in one
+ *    forward and the main model verifies the block, so each MoE layer sees
+ *    T = sequences x 8 tokens: techllm.github.io, section "2. DFlash";
+ *    dothoosh.com, section "جزئیات پیاده‌سازی DFlash" (block size capped at 8).
+ *  - Decode is bound by weight bandwidth: ai.appwright.xyz, "第1層".
+ *  - The layer definition the pages leave open (E2M1 grid, E8M0 scale rule,
+ *    routing rule, SwiGLU, output type) is the layer specification this
+ *    library implements, restated at each entry point below.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are caller-owned, row-major, contiguous device memory unless
+ *    stated.  The library never frees caller memory and writes only the
+ *    outputs named below.
+ *  - Calls are stream-ordered and asynchronous; none synchronizes except
+ *    moe_mxfp4_get_status.
+ *  - Argument errors are detected on the host and returned before anything
+ *    is launched.  Device-side faults (a bounded wait that expired, an index
+ *    out of range) never trap: they set a device status word that
+ *    moe_mxfp4_get_status returns.
+ *  - Inputs must be finite; NaN/Inf give unspecified values (never a hang).
+ *  - The library requires a device of compute capability 10.3 (B300).
+ */
+#ifndef MOE_MXFP4_H
+#define MOE_MXFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* the CUDA runtime's stream and event handles (identical typedefs to driver_types.h) */
+typedef struct CUstream_st* cudaStream_t;
+typedef struct CUevent_st* cudaEvent_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1,      /* null pointer, negative size, k out of range */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 128, E or k too large */
+  MOE_ERR_ALIGNMENT = -3,        /* a pointer is not aligned as documented */
+  MOE_ERR_CUDA = -4,             /* a CUDA runtime call failed (launch, alloc, ...) */
+  MOE_ERR_NO_MEMORY = -5,        /* workspace could not be allocated / is too small */
+  MOE_ERR_DEVICE_TIMEOUT = -6,   /* a bounded device-side wait expired */
+  MOE_ERR_DEVICE_FAULT = -7,     /* a device-side bounds/consistency check failed */
+  MOE_ERR_NO_DEVICE = -8         /* no device of compute capability 10.3 is current */
+} moe_status;
+
+#define MOE_MAX_K 16     /* largest top-k */
+#define MOE_MAX_E 1024   /* largest expert count */
+
+/* activation modes of moe_opts.act_mode */
+#define MOE_ACT_MXFP8 0  /* x and h quantized to MXFP8-E4M3 (blocks of 32) */
+#define MOE_ACT_BF16 1   /* x used as bf16, h rounded to bf16 */
+
+/* execution paths of moe_opts.path */
+#define MOE_PATH_AUTO 0
+#define MOE_PATH_MULTI 1      /* routing kernels, GEMM1, GEMM2, combine */
+#define MOE_PATH_PERSISTENT 2 /* routing kernels, then one persistent kernel */
+
+/*
+ * moe_mxfp4_forward — the MoE expert layer.
+ *
+ *   y[t] = bf16_RNE( sum_{j<k} g[t,j] * W2_{e_j} act2( silu(W1_{e_j} act1(x[t]))
+ *                                                   * (W3_{e_j} act1(x[t])) ) )
+ *
+ * Routing: (e_j) are the k largest router_logits[t] in descending order, the
+ * lower expert index first among equal logits; g[t,:] is the softmax of the
+ * k selected logits.  W1 = rows [0, I) and W3 = rows [I, 2I) of the expert's
+ * w13; each weight is e2m1(code) * 2^(scale - 127).  act1/act2 quantize to
+ * MXFP8-E4M3 along the reduction dimension (the default) — see
+ * moe_mxfp4_forward_ex for the bf16 mode.  silu(z) = z / (1 + e^-z).  The
+ * gate-weighted sum is accumulated in fp32 in slot order j = 0..k-1 (the
+ * result is deterministic run to run).
+ *
+ * Arguments (all device pointers):
+ *  x_bf16         [T, H]       bf16 activations
+ *  router_logits  [T, E]       fp32
+ *  w13_fp4        [E, 2I, H/2] packed E2M1, element 2i in the low nibble of
+ *                              byte i; 32-byte aligned
+ *  w13_e8m0       [E, 2I, H/32] one E8M0 scale per 32 elements along H
+ *  w2_fp4         [E, H, I/2]  packed E2M1; 32-byte aligned
+ *  w2_e8m0        [E, H, I/32]
+ *  T >= 0 (T = 0 returns MOE_OK and launches nothing), H and I multiples of
+ *  128, 1 <= E <= MOE_MAX_E, 1 <= k <= min(E, MOE_MAX_K)
+ *  y_bf16         [T, H]       bf16 output, overwritten
+ *  stream         CUDA stream the work is ordered on (0 = legacy default)
+ * Other pointers must be 16-byte aligned.  Scratch space comes from a
+ * library-owned per-device cache that grows on first use of a larger shape
+ * (a cudaMalloc outside any stream capture).
+ * Returns MOE_OK or an moe_status error (host-detected errors launch nothing).
+ */
+int moe_mxfp4_forward(const void* x_bf16, const float* router_logits, const uint8_t* w13_fp4,
+                      const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
+                      int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream);
+
+typedef struct {
+  int act_mode;           /* MOE_ACT_MXFP8 (0) or MOE_ACT_BF16 (1) */
+  int path;               /* MOE_PATH_* */
+  void* workspace;        /* optional caller scratch (device, 256-byte aligned) */
+  size_t workspace_bytes; /* >= moe_mxfp4_workspace_size(...) when workspace != NULL */
+  uint32_t debug_flags;   /* 0 in normal use; see MOE_DEBUG_* */
+  /* optional step markers: caller-created events; the library records
+   * step_events[i] on `stream` just before the i-th kernel of the call and one
+   * more after the last (i < n_step_events).  Kernel order: multi path —
+   * route_topk, route_permute, act_quant, gemm1, gemm2, combine; persistent
+   * path — route_topk, route_permute, act_quant, moe_persistent. */
+  cudaEvent_t* step_events;
+  int n_step_events;
+} moe_opts;
+
+/* debug_flags: cap every bounded device wait at ~1 ms instead of ~2 s; used
+ * to exercise the timeout path without faulting anything */
+#define MOE_DEBUG_SHORT_TIMEOUT 1u
+
+/*
+ * moe_mxfp4_forward_ex — moe_mxfp4_forward with options (NULL opts = defaults).
+ * With a caller workspace the call allocates nothing.
+ */
+int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const uint8_t* w13_fp4,
+                         const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
+                         int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream,
+                         const moe_opts* opts);
+
+/* bytes of scratch a forward of this shape needs (0 on invalid arguments) */
+size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode);
+
+/*
+ * mxfp4_quantize — pack fp32 weights to MXFP4 with the layer's rule (offline).
+ *  w        [rows, K] fp32 device, K a multiple of 32, 16-byte aligned
+ *  out_fp4  [rows, K/2] packed E2M1 (element 2i in the low nibble of byte i)
+ *  out_e8m0 [rows, K/32] E8M0 scale codes
+ * Per block of 32 along K: amax = max |w|; scale code c = clamp(floor(log2(amax))
+ * - 2 + 127, 0, 254) with floor(log2) read exactly from the fp32 bits (c = 0
+ * when amax = 0); each element is q = w / 2^(c-127) rounded to the nearest of
+ * {0, .5, 1, 1.5, 2, 3, 4, 6} (ties to the even code), saturated at 6, sign
+ * from the input's sign bit.  Block size 32: ai.appwright.xyz, "第1層：FP4量子化".
+ */
+int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4,
+                   uint8_t* out_e8m0, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_route — the routing steps alone (top-k + softmax, per-expert
+ * histogram, prefix scan, stable permutation), for bit-exact checks.
+ *  router_logits [T, E] fp32 device;  outputs (device):
+ *  topk_idx [T, k] int32, topk_w [T, k] fp32, cnt [E] int32, off [E+1] int32,
+ *  perm [T*k] int32 (slot -> token), pos [T*k] int32 ((t*k + j) -> slot).
+ * Slots are expert-major; within an expert, ascending t*k + j.
+ */
+int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* topk_idx,
+                    float* topk_w, int32_t* cnt, int32_t* off, int32_t* perm, int32_t* pos,
+                    cudaStream_t stream);
+
+/*
+ * moe_mxfp8_quantize_rows — the MXFP8-E4M3 activation quantizer alone.
+ *  x_bf16 [rows, K] device (K a multiple of 32) -> codes [rows, K] E4M3,
+ *  scales [rows, K/32] E8M0.  Per block of 32: c = clamp(floor(log2(amax)) - 8
+ *  + 127, 0, 254) (c = 0 when amax = 0); elements round to nearest even E4M3 of
+ *  x / 2^(c-127), saturating at +-448.
+ */
+int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_get_status — synchronizes `stream`, returns the first device-side
+ * error recorded since the last call (MOE_OK if none) and clears it.  A CUDA
+ * error seen while synchronizing returns MOE_ERR_CUDA.
+ */
+int moe_mxfp4_get_status(cudaStream_t stream);
+
+/* number of kernels this library has launched in this process (all devices,
+ * all entry points); a diagnostic for counting launches in a timed region */
+uint64_t moe_mxfp4_launch_count(void);
+
+/* human-readable name of an moe_status value (static string) */
+const char* moe_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

@@ -1,0 +1,53 @@
+// Shared definitions of the MXFP4 MoE layer library: status word, workspace
+// layout, small device helpers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_mxfp4.h"
+
+namespace moe {
+
+// Assignments of one expert are processed in chunks of at most this many
+// slots (tokens); a chunk is the N dimension of one GEMM work item.
+constexpr int kChunkMax = 96;
+constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
+constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
+
+// Per-call device scratch.  Offsets are computed on the host by
+// workspace_layout(); every sub-buffer starts on a 256-byte boundary.
+struct Work {
+  int32_t* topk_idx;  // [T*k]
+  float* topk_w;      // [T*k]
+  int32_t* cnt;       // [E]
+  int32_t* off;       // [E+1]
+  int32_t* perm;      // [T*k] slot -> token
+  int32_t* pos;       // [T*k] (t*k+j) -> slot
+  int4* chunks;       // [max_chunks] {expert, first slot, n slots, 0}
+  int32_t* meta;      // [0] chunk count, [1] touched experts, [2..] step counters
+  uint8_t* xq;        // [T*k, H] E4M3 (MXFP8) or [T*k, H] bf16 (bf16 mode)
+  uint8_t* xs;        // [T*k, H/32] E8M0
+  uint8_t* hq;        // [T*k, I] E4M3 or bf16
+  uint8_t* hs;        // [T*k, I/32]
+  float* yp;          // [T*k, H] per-slot expert outputs (fp32)
+  int max_chunks;
+};
+
+__device__ __forceinline__ void set_status(int* status, int code) {
+  atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+}  // namespace moe

@@ -1,0 +1,369 @@
+// libmoe_mxfp4.so — C ABI entry points (declared in include/moe_mxfp4.h).
+//
+// One translation unit: the kernels live in the headers included below.  The
+// host code validates arguments before any CUDA call, lays out the per-call
+// scratch, and enqueues the steps of the layer on the caller's stream:
+//   route_topk -> route_permute -> act quant/gather -> GEMM1 -> GEMM2 -> combine
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstring>
+#include <mutex>
+
+#include "combine.cuh"
+#include "common.cuh"
+#include "fmt.cuh"
+#include "gemm_simt.cuh"
+#include "quant.cuh"
+#include "route.cuh"
+
+namespace moe {
+
+__device__ int g_status;  // first device-side error since the last get_status
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;
+  int sms = 0;
+  int* status = nullptr;
+  void* ws = nullptr;  // library-owned scratch cache
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+std::atomic<uint64_t> g_launches{0};
+
+// records the step markers of moe_opts around the kernels of one call
+struct Steps {
+  const moe_opts* o;
+  cudaStream_t s;
+  int i = 0;
+  void mark() {
+    if (o && o->step_events && i < o->n_step_events) cudaEventRecord(o->step_events[i], s);
+    ++i;
+  }
+  void launched(int n = 1) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+};
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// current device; checks compute capability 10.3 and caches per-device data
+int device_state(DeviceState** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_NO_DEVICE;
+  if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_NO_DEVICE;
+    if (major != 10 || minor != 3) return MOE_ERR_NO_DEVICE;
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_status) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
+    if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             permute_smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    d.ready = true;
+  }
+  *out = &d;
+  return MOE_OK;
+}
+
+struct Layout {
+  size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, meta, xq, xs, hq, hs, yp, total;
+  int max_chunks;
+};
+
+Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act_mode) {
+  Layout L{};
+  const int64_t TK = T * k;
+  const int64_t act_bytes = act_mode == MOE_ACT_BF16 ? 2 : 1;
+  L.max_chunks = (int)(std::min<int64_t>(E, TK) + TK / kChunkMax + 1);
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  L.topk_idx = take(TK * 4);
+  L.topk_w = take(TK * 4);
+  L.cnt = take(E * 4);
+  L.off = take((E + 1) * 4);
+  L.perm = take(TK * 4);
+  L.pos = take(TK * 4);
+  L.chunks = take((size_t)L.max_chunks * 16);
+  L.meta = take(64 * 4);
+  L.xq = take(TK * H * act_bytes);
+  L.xs = take(TK * (H / 32));
+  L.hq = take(TK * I * act_bytes);
+  L.hs = take(TK * (I / 32));
+  L.yp = take(TK * H * 4);
+  L.total = o;
+  return L;
+}
+
+Work carve(void* base, const Layout& L) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  Work w;
+  w.topk_idx = reinterpret_cast<int32_t*>(b + L.topk_idx);
+  w.topk_w = reinterpret_cast<float*>(b + L.topk_w);
+  w.cnt = reinterpret_cast<int32_t*>(b + L.cnt);
+  w.off = reinterpret_cast<int32_t*>(b + L.off);
+  w.perm = reinterpret_cast<int32_t*>(b + L.perm);
+  w.pos = reinterpret_cast<int32_t*>(b + L.pos);
+  w.chunks = reinterpret_cast<int4*>(b + L.chunks);
+  w.meta = reinterpret_cast<int32_t*>(b + L.meta);
+  w.xq = b + L.xq;
+  w.xs = b + L.xs;
+  w.hq = b + L.hq;
+  w.hs = b + L.hs;
+  w.yp = reinterpret_cast<float*>(b + L.yp);
+  w.max_chunks = L.max_chunks;
+  return w;
+}
+
+// library-owned scratch of at least `bytes` on this device
+int cached_workspace(DeviceState* d, size_t bytes, void** out) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (d->ws_bytes < bytes) {
+    if (d->ws) cudaFree(d->ws);  // synchronizes: no call still uses it
+    d->ws = nullptr;
+    d->ws_bytes = 0;
+    if (cudaMalloc(&d->ws, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return MOE_ERR_NO_MEMORY;
+    }
+    d->ws_bytes = bytes;
+  }
+  *out = d->ws;
+  return MOE_OK;
+}
+
+int validate_shape(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+  if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
+  if (k > E) return MOE_ERR_INVALID_ARG;
+  if (k > MOE_MAX_K || E > MOE_MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 128 || I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (T * k > (int64_t)1 << 30 || T * k * H > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+int launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int grid_for(int64_t work, int per_block, int cap) {
+  int64_t g = (work + per_block - 1) / per_block;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(g, cap));
+}
+
+// routing steps (1)-(4) into w
+int enqueue_route(const float* logits, int T, int E, int k, const Work& w, DeviceState* d,
+                  cudaStream_t s, Steps& st) {
+  const int grid = grid_for((int64_t)T * 32, 256, 1 << 30);
+  st.mark();
+  if (E <= 128)
+    route_topk_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
+  else if (E <= 384)
+    route_topk_kernel<12><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
+  else
+    route_topk_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
+  st.launched();
+  st.mark();
+  const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
+  route_permute_kernel<<<1, 1024, smem, s>>>(w.topk_idx, T, k, E, w.cnt, w.off, w.perm, w.pos,
+                                             w.chunks, w.max_chunks, w.meta, d->status);
+  st.launched();
+  return launch_status();
+}
+
+int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
+                 const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
+                 void* y, cudaStream_t stream, const moe_opts* opts) {
+  if (!x_bf16 || !logits || !w13 || !w13s || !w2 || !w2s || !y) return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
+  const int path = opts ? opts->path : MOE_PATH_AUTO;
+  if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w13, 32) || !aligned(w2, 32)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
+      !aligned(y, 16))
+    return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_for(T, H, I, E, k, act);
+  if (opts && opts->workspace) {
+    if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
+    if (opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
+  }
+  if (T == 0) return MOE_OK;
+
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  void* ws = opts ? opts->workspace : nullptr;
+  if (!ws && (rc = cached_workspace(d, L.total, &ws))) return rc;
+  const Work w = carve(ws, L);
+  const int TK = T * k;
+
+  Steps st{opts, stream};
+  if ((rc = enqueue_route(logits, T, E, k, w, d, stream, st))) return rc;
+  const int cap = d->sms * 8;
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  st.mark();
+  if (act == MOE_ACT_MXFP8)
+    mxfp8_rows_kernel<<<grid_for(TK, 8, cap), 256, 0, stream>>>(x, w.perm, TK, H, T, w.xq, w.xs,
+                                                               d->status);
+  else
+    gather_bf16_rows_kernel<<<grid_for(TK, 8, cap), 256, 0, stream>>>(
+        x, w.perm, TK, H, T, reinterpret_cast<uint16_t*>(w.xq), d->status);
+  st.launched();
+  const int ggrid = d->sms * 4;
+  st.mark();
+  if (act == MOE_ACT_MXFP8)
+    gemm1_simt_kernel<MOE_ACT_MXFP8><<<ggrid, 128, 0, stream>>>(w13, w13s, w.xq, w.xs, w.chunks,
+                                                               w.meta, H, I, w.hq, w.hs);
+  else
+    gemm1_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w13, w13s, w.xq, w.xs, w.chunks,
+                                                              w.meta, H, I, w.hq, w.hs);
+  st.launched();
+  st.mark();
+  if (act == MOE_ACT_MXFP8)
+    gemm2_simt_kernel<MOE_ACT_MXFP8><<<ggrid, 128, 0, stream>>>(w2, w2s, w.hq, w.hs, w.chunks,
+                                                               w.meta, H, I, w.yp);
+  else
+    gemm2_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w2, w2s, w.hq, w.hs, w.chunks,
+                                                              w.meta, H, I, w.yp);
+  st.launched();
+  st.mark();
+  combine_kernel<<<grid_for((int64_t)T * H / 8, 256, cap), 256, 0, stream>>>(
+      w.yp, w.pos, w.topk_w, T, H, k, static_cast<uint16_t*>(y));
+  st.launched();
+  st.mark();
+  return launch_status();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_mxfp4_forward(const void* x_bf16, const float* router_logits, const uint8_t* w13_fp4,
+                      const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
+                      int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream) {
+  return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I, E, k,
+                      y_bf16, stream, nullptr);
+}
+
+int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const uint8_t* w13_fp4,
+                         const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
+                         int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream,
+                         const moe_opts* opts) {
+  return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I, E, k,
+                      y_bf16, stream, opts);
+}
+
+size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode) {
+  if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
+  return layout_for(T, H, I, E, k, act_mode).total;
+}
+
+int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4, uint8_t* out_e8m0,
+                   cudaStream_t stream) {
+  if (!w || !out_fp4 || !out_e8m0 || rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(out_fp4, 16)) return MOE_ERR_ALIGNMENT;
+  if (rows == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  const int64_t nblocks = rows * (K / 32);
+  mxfp4_quantize_kernel<<<grid_for(nblocks, 256, d->sms * 16), 256, 0, stream>>>(
+      w, nblocks, out_fp4, out_e8m0);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return launch_status();
+}
+
+int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* topk_idx,
+                    float* topk_w, int32_t* cnt, int32_t* off, int32_t* perm, int32_t* pos,
+                    cudaStream_t stream) {
+  if (!router_logits || !topk_idx || !topk_w || !cnt || !off || !perm || !pos)
+    return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, 128, 128, E, k);
+  if (rc) return rc;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  const Layout L = layout_for(T, 128, 128, E, k, MOE_ACT_MXFP8);
+  void* ws = nullptr;
+  if ((rc = cached_workspace(d, L.total, &ws))) return rc;
+  Work w = carve(ws, L);
+  w.topk_idx = topk_idx;
+  w.topk_w = topk_w;
+  w.cnt = cnt;
+  w.off = off;
+  w.perm = perm;
+  w.pos = pos;
+  Steps st{nullptr, stream};
+  return enqueue_route(router_logits, T, E, k, w, d, stream, st);
+}
+
+int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t* codes,
+                            uint8_t* scales, cudaStream_t stream) {
+  if (!x_bf16 || !codes || !scales || rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x_bf16, 16) || !aligned(codes, 16)) return MOE_ERR_ALIGNMENT;
+  if (rows == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  mxfp8_rows_kernel<<<grid_for(rows, 8, d->sms * 8), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(x_bf16), nullptr, rows, K, rows, codes, scales, d->status);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return launch_status();
+}
+
+int moe_mxfp4_get_status(cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  const int zero = 0;
+  if (v != 0 && cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return v;
+}
+
+uint64_t moe_mxfp4_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+    case MOE_ERR_ALIGNMENT: return "MOE_ERR_ALIGNMENT";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_NO_MEMORY: return "MOE_ERR_NO_MEMORY";
+    case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+    case MOE_ERR_DEVICE_FAULT: return "MOE_ERR_DEVICE_FAULT";
+    case MOE_ERR_NO_DEVICE: return "MOE_ERR_NO_DEVICE";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

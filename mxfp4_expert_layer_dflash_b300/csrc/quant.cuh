@@ -1,0 +1,124 @@
+// Quantization kernels:
+//  - MXFP4 packing of fp32 weights (offline): per block of 32, scale code
+//    clamp(floor(log2(amax)) - 2 + 127, 0, 254), elements on the E2M1 grid
+//    (block size 32: ai.appwright.xyz, "投機的デコード", "第1層：FP4量子化");
+//  - the activation step a4: gather x rows into expert-major slot order and
+//    quantize them to MXFP8-E4M3 (blocks of 32 along H), or copy them as bf16.
+#pragma once
+
+#include "common.cuh"
+#include "fmt.cuh"
+
+namespace moe {
+
+// one thread per block of 32 fp32 elements; blocks are contiguous in memory
+__global__ void __launch_bounds__(256) mxfp4_quantize_kernel(const float* __restrict__ w,
+                                                             int64_t nblocks,
+                                                             uint8_t* __restrict__ fp4,
+                                                             uint8_t* __restrict__ e8m0) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
+    const float4* src = reinterpret_cast<const float4*>(w + b * 32);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float4 q = __ldcs(src + i);  // streamed once
+      v[4 * i] = q.x;
+      v[4 * i + 1] = q.y;
+      v[4 * i + 2] = q.z;
+      v[4 * i + 3] = q.w;
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    const int code = block_scale_code(amax, 2);
+    const float inv = exp2_exact(127 - code);  // exact power of two
+    uint32_t words[4];
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x |= e2m1_encode(v[wd * 8 + i] * inv) << (4 * i);
+      words[wd] = x;
+    }
+    *reinterpret_cast<uint4*>(fp4 + b * 16) = make_uint4(words[0], words[1], words[2], words[3]);
+    e8m0[b] = (uint8_t)code;
+  }
+}
+
+// load 32 bf16 (64 bytes, 16-byte aligned) as floats
+__device__ __forceinline__ void load_bf16x32(const uint16_t* p, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 q = s[i];
+    uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[8 * i + 2 * j] = __uint_as_float(w[j] << 16);
+      v[8 * i + 2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+    }
+  }
+}
+
+__device__ __forceinline__ void store_u8x32(uint8_t* p, const uint8_t* c) {
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    w[i] = (uint32_t)c[4 * i] | ((uint32_t)c[4 * i + 1] << 8) | ((uint32_t)c[4 * i + 2] << 16) |
+           ((uint32_t)c[4 * i + 3] << 24);
+  reinterpret_cast<uint4*>(p)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// MXFP8 rows: one warp per row, lane-strided blocks of 32.  src_row(r) selects
+// the source row (identity, or the permutation slot -> token).
+__global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ row_map,
+                                                         int64_t rows, int64_t K, int64_t src_rows,
+                                                         uint8_t* __restrict__ q,
+                                                         uint8_t* __restrict__ s, int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nb = K / 32;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    int64_t src = row_map ? row_map[r] : r;
+    if (src < 0 || src >= src_rows) {
+      if (lane == 0) set_status(status, kStatusFault);
+      src = 0;
+    }
+    for (int64_t b = lane; b < nb; b += 32) {
+      float v[32];
+      uint8_t c[32];
+      load_bf16x32(x + src * K + b * 32, v);
+      const int code = mxfp8_block(v, c);
+      store_u8x32(q + r * K + b * 32, c);
+      s[r * nb + b] = (uint8_t)code;
+    }
+  }
+}
+
+// bf16 mode of a4: gather rows unchanged
+__global__ void __launch_bounds__(256) gather_bf16_rows_kernel(const uint16_t* __restrict__ x,
+                                                               const int32_t* __restrict__ row_map,
+                                                               int64_t rows, int64_t K,
+                                                               int64_t src_rows,
+                                                               uint16_t* __restrict__ out,
+                                                               int* status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    int64_t src = row_map[r];
+    if (src < 0 || src >= src_rows) {
+      if (lane == 0) set_status(status, kStatusFault);
+      src = 0;
+    }
+    const uint4* a = reinterpret_cast<const uint4*>(x + src * K);
+    uint4* o = reinterpret_cast<uint4*>(out + r * K);
+    for (int64_t i = lane; i < K / 8; i += 32) o[i] = a[i];
+  }
+}
+
+}  // namespace moe

@@ -71,12 +71,13 @@ int oracle_floor_log2_f32(float a) {
   return p - 149;
 }
 
-/* nearest of the non-negative codes [0, n) of a decoder; ties to the even code */
-static int nearest_code(double a, int n, double (*dec)(int)) {
+/* nearest of the non-negative codes [0, n) whose decoded magnitudes are mag[];
+ * ties to the even code */
+static int nearest_code(double a, int n, const double* mag) {
   int best = 0;
-  double bd = fabs(a - dec(0));
+  double bd = fabs(a - mag[0]);
   for (int c = 1; c < n; ++c) {
-    double d = fabs(a - dec(c));
+    double d = fabs(a - mag[c]);
     if (d < bd || (d == bd && (c & 1) == 0 && (best & 1) == 1)) {
       best = c;
       bd = d;
@@ -85,19 +86,35 @@ static int nearest_code(double a, int n, double (*dec)(int)) {
   return best;
 }
 
+/* decoded non-negative magnitudes, memoized once (same values as the decoders) */
+static double g_e2m1_mag[8], g_e4m3_mag[0x7F];
+static void init_mags(void) {
+  static int ready = 0;
+  if (ready) return;
+#pragma omp critical(oracle_init_mags)
+  if (!ready) {
+    for (int c = 0; c < 8; ++c) g_e2m1_mag[c] = oracle_e2m1_value(c);
+    for (int c = 0; c < 0x7F; ++c) g_e4m3_mag[c] = oracle_e4m3_value(c);
+#pragma omp flush
+    ready = 1;
+  }
+}
+
 /* sign copied from the input's sign bit, so -0 and small negatives give code 8 */
 int oracle_e2m1_encode(double q) {
+  init_mags();
   int neg = signbit(q) ? 1 : 0;
   double a = fabs(q);
   if (a >= 6.0) return (neg << 3) | 7; /* saturate */
-  return (neg << 3) | nearest_code(a, 8, oracle_e2m1_value);
+  return (neg << 3) | nearest_code(a, 8, g_e2m1_mag);
 }
 
 int oracle_e4m3_encode(double q) {
+  init_mags();
   int neg = signbit(q) ? 1 : 0;
   double a = fabs(q);
   if (a >= 448.0) return (neg << 7) | 0x7E; /* satfinite */
-  return (neg << 7) | nearest_code(a, 0x7F, oracle_e4m3_value);
+  return (neg << 7) | nearest_code(a, 0x7F, g_e4m3_mag);
 }
 
 uint16_t oracle_bf16_from_double(double v) {
@@ -135,6 +152,8 @@ static int clamp_scale_code(int e) {
 void oracle_mxfp4_quantize(const float* w, int64_t R, int64_t K, uint8_t* out_fp4,
                            uint8_t* out_e8m0) {
   const int64_t nb = K / 32;
+  init_mags();
+#pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < R; ++r) {
     for (int64_t b = 0; b < nb; ++b) {
       const float* blk = w + r * K + b * 32;
@@ -262,56 +281,73 @@ int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
   if (act_mode < 0 || act_mode > 2) return -1;
   if (!tokens) n_tokens = T;
   init_tables();
+  init_mags();
+  const int nt = n_threads > 0 ? n_threads : omp_get_max_threads();
 
-#pragma omp parallel num_threads(n_threads > 0 ? n_threads : omp_get_max_threads())
-  {
-    double* a = (double*)malloc(sizeof(double) * (size_t)H);
-    double* hv = (double*)malloc(sizeof(double) * (size_t)I);
-    double* acc = (double*)malloc(sizeof(double) * (size_t)H);
-    uint8_t* tc = (uint8_t*)malloc((size_t)(H > I ? H : I));
-    uint8_t* ts = (uint8_t*)malloc((size_t)(H > I ? H : I) / 32);
-    int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)k);
-    double* g = (double*)malloc(sizeof(double) * (size_t)k);
+  /* per token: act1(x) and the routing decision */
+  double* a = (double*)malloc(sizeof(double) * (size_t)(n_tokens * H));
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_tokens * k));
+  double* g = (double*)malloc(sizeof(double) * (size_t)(n_tokens * k));
+  /* per (token, slot): the expert's output W2 act2(h) */
+  double* d = (double*)malloc(sizeof(double) * (size_t)(n_tokens * k * H));
 
-#pragma omp for schedule(dynamic, 1)
-    for (int64_t n = 0; n < n_tokens; ++n) {
-      int64_t t = tokens ? tokens[n] : n;
-      for (int64_t h = 0; h < H; ++h) a[h] = oracle_bf16_value(x_bf16[t * H + h]);
-      apply_act(a, H, act_mode == ORACLE_ACT_MXFP8 ? ORACLE_ACT_MXFP8 : ORACLE_ACT_EXACT, tc, ts);
-      oracle_route(router_logits + t * E, 1, E, k, idx, g);
-      for (int64_t h = 0; h < H; ++h) acc[h] = 0.0;
-      for (int j = 0; j < k; ++j) {
-        int64_t e = idx[j];
-        const int64_t r0 = e * 2 * I; /* first w13 row of expert e */
-        for (int64_t i = 0; i < I; ++i) {
-          double gate = 0.0, up = 0.0;
-          for (int64_t h = 0; h < H; ++h) {
-            gate += wval(w13_fp4, w13_e8m0, H, r0 + i, h) * a[h];
-            up += wval(w13_fp4, w13_e8m0, H, r0 + I + i, h) * a[h];
-          }
-          hv[i] = silu(gate) * up;
-        }
-        apply_act(hv, I, act_mode, tc, ts);
-        if (h_out)
-          for (int64_t i = 0; i < I; ++i) h_out[(n * k + j) * I + i] = hv[i];
-        for (int64_t o = 0; o < H; ++o) {
-          double d = 0.0;
-          for (int64_t i = 0; i < I; ++i) d += wval(w2_fp4, w2_e8m0, I, e * H + o, i) * hv[i];
-          acc[o] += g[j] * d;
-        }
-      }
-      for (int64_t h = 0; h < H; ++h) {
-        if (y_f64) y_f64[n * H + h] = acc[h];
-        if (y_bf16) y_bf16[n * H + h] = oracle_bf16_from_double(acc[h]);
-      }
-    }
-    free(a);
-    free(hv);
-    free(acc);
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int64_t n = 0; n < n_tokens; ++n) {
+    int64_t t = tokens ? tokens[n] : n;
+    uint8_t* tc = (uint8_t*)malloc((size_t)H);
+    uint8_t* ts = (uint8_t*)malloc((size_t)H / 32);
+    double* an = a + n * H;
+    for (int64_t h = 0; h < H; ++h) an[h] = oracle_bf16_value(x_bf16[t * H + h]);
+    apply_act(an, H, act_mode == ORACLE_ACT_MXFP8 ? ORACLE_ACT_MXFP8 : ORACLE_ACT_EXACT, tc, ts);
+    oracle_route(router_logits + t * E, 1, E, k, idx + n * k, g + n * k);
     free(tc);
     free(ts);
-    free(idx);
-    free(g);
   }
+
+#pragma omp parallel for schedule(dynamic, 1) num_threads(nt)
+  for (int64_t task = 0; task < n_tokens * k; ++task) {
+    const int64_t n = task / k;
+    const int j = (int)(task % k);
+    const int64_t e = idx[n * k + j];
+    const double* an = a + n * H;
+    double* hv = (double*)malloc(sizeof(double) * (size_t)I);
+    uint8_t* tc = (uint8_t*)malloc((size_t)I);
+    uint8_t* ts = (uint8_t*)malloc((size_t)I / 32);
+    const int64_t r0 = e * 2 * I; /* first w13 row of expert e */
+    for (int64_t i = 0; i < I; ++i) {
+      double gate = 0.0, up = 0.0;
+      for (int64_t h = 0; h < H; ++h) {
+        gate += wval(w13_fp4, w13_e8m0, H, r0 + i, h) * an[h];
+        up += wval(w13_fp4, w13_e8m0, H, r0 + I + i, h) * an[h];
+      }
+      hv[i] = silu(gate) * up;
+    }
+    apply_act(hv, I, act_mode, tc, ts);
+    if (h_out)
+      for (int64_t i = 0; i < I; ++i) h_out[(n * k + j) * I + i] = hv[i];
+    double* dn = d + task * H;
+    for (int64_t o = 0; o < H; ++o) {
+      double acc = 0.0;
+      for (int64_t i = 0; i < I; ++i) acc += wval(w2_fp4, w2_e8m0, I, e * H + o, i) * hv[i];
+      dn[o] = acc;
+    }
+    free(hv);
+    free(tc);
+    free(ts);
+  }
+
+  /* gate-weighted sum in slot order j = 0..k-1, then bf16 rounding */
+  for (int64_t n = 0; n < n_tokens; ++n) {
+    for (int64_t h = 0; h < H; ++h) {
+      double acc = 0.0;
+      for (int j = 0; j < k; ++j) acc += g[n * k + j] * d[(n * k + j) * H + h];
+      if (y_f64) y_f64[n * H + h] = acc;
+      if (y_bf16) y_bf16[n * H + h] = oracle_bf16_from_double(acc);
+    }
+  }
+  free(a);
+  free(idx);
+  free(g);
+  free(d);
   return 0;
 }

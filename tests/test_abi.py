@@ -1,0 +1,100 @@
+"""The C-ABI library loads and exports every function include/*.h declares; host-side argument
+validation returns its error codes before any CUDA call (no GPU needed)."""
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(",
+                             src, flags=re.M):
+            if not m.group(0).lstrip().startswith(("typedef", "#", "return")):
+                names.add(m.group(1))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import mxfp4_expert_layer_dflash_b300 as m
+    if not os.path.exists(m.LIB_PATH):
+        from mxfp4_expert_layer_dflash_b300 import build
+        build.build()
+    m.lib()
+    return m
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for must in ("moe_mxfp4_forward", "moe_mxfp4_forward_ex", "mxfp4_quantize",
+                 "moe_mxfp4_workspace_size", "moe_mxfp4_get_status", "moe_mxfp4_route",
+                 "moe_mxfp8_quantize_rows", "moe_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(moe):
+    for name in _declared_functions():
+        assert hasattr(moe.lib(), name), name
+
+
+def test_status_strings(moe):
+    for code, name in moe.STATUS.items():
+        assert moe.moe_status_string(code) == name
+
+
+def test_workspace_size(moe):
+    small = moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 2)
+    big = moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8)
+    assert 0 < small < big
+    assert moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8, 1) > big
+    assert moe.moe_mxfp4_workspace_size(16, 250, 128, 8, 2) == 0       # H % 128
+    assert moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 9) == 0       # k > E
+    assert moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 2, 7) == 0    # bad act mode
+
+
+def _fwd(moe, **kw):
+    a = dict(x=256, lg=512, w13=1024, s13=2048, w2=4096, s2=8192, T=4, H=256, I=128, E=8, k=2,
+             y=16384)
+    a.update(kw)
+    return moe.lib().moe_mxfp4_forward(a["x"], a["lg"], a["w13"], a["s13"], a["w2"], a["s2"],
+                                       a["T"], a["H"], a["I"], a["E"], a["k"], a["y"], None)
+
+
+def test_host_validation_rejects_before_launch(moe):
+    # fake, never-dereferenced addresses: every case fails validation on the host
+    assert _fwd(moe, x=None) == -1
+    assert _fwd(moe, T=-1) == -1
+    assert _fwd(moe, k=0) == -1
+    assert _fwd(moe, k=9) == -1
+    assert _fwd(moe, k=17, E=32) == -2
+    assert _fwd(moe, E=2000, k=2) == -2
+    assert _fwd(moe, H=200) == -2
+    assert _fwd(moe, I=96) == -2
+    assert _fwd(moe, w13=1040) == -3        # fp4 weights need 32-byte alignment
+    assert _fwd(moe, x=258) == -3
+    assert _fwd(moe, T=0) == 0               # no-op, nothing launched
+    L = moe.lib()
+    assert L.mxfp4_quantize(None, 4, 64, 256, 512, None) == -1
+    assert L.mxfp4_quantize(256, 4, 48, 256, 512, None) == -2
+    assert L.mxfp4_quantize(260, 4, 64, 256, 512, None) == -3
+    assert L.mxfp4_quantize(256, 0, 64, 256, 512, None) == 0
+    assert L.moe_mxfp8_quantize_rows(256, 3, 40, 512, 1024, None) == -2
+
+
+def test_forward_ex_rejects_small_workspace(moe):
+    o = moe.moe_opts(0, 0, 256 * 1024, 16, 0, None, 0)
+    import ctypes
+    rc = moe.lib().moe_mxfp4_forward_ex(256, 512, 1024, 2048, 4096, 8192, 4, 256, 128, 8, 2,
+                                        16384, None, ctypes.byref(o))
+    assert rc == -5
+    o = moe.moe_opts(3, 0, None, 0, 0, None, 0)
+    rc = moe.lib().moe_mxfp4_forward_ex(256, 512, 1024, 2048, 4096, 8192, 4, 256, 128, 8, 2,
+                                        16384, None, ctypes.byref(o))
+    assert rc == -1

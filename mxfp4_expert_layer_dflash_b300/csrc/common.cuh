@@ -11,7 +11,7 @@ namespace moe {
 
 // Assignments of one expert are processed in chunks of at most this many
 // slots (tokens); a chunk is the N dimension of one GEMM work item.
-constexpr int kChunkMax = 96;
+constexpr int kChunkMax = 64;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 

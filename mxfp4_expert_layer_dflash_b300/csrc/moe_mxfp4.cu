@@ -4,7 +4,11 @@
 // host code validates arguments before any CUDA call, lays out the per-call
 // scratch, and enqueues the steps of the layer on the caller's stream:
 //   route_topk -> route_permute -> act quant/gather -> GEMM1 -> GEMM2 -> combine
+// MXFP8 mode runs the GEMMs on tcgen05 block-scaled MMA fed by TMA; bf16 mode
+// runs them on CUDA cores.
+#include <cuda.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <atomic>
@@ -15,6 +19,7 @@
 #include "common.cuh"
 #include "fmt.cuh"
 #include "gemm_simt.cuh"
+#include "gemm_tc.cuh"
 #include "quant.cuh"
 #include "route.cuh"
 
@@ -73,12 +78,48 @@ int device_state(DeviceState** out) {
       return MOE_ERR_CUDA;
     const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
     if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             permute_smem) != cudaSuccess)
+                             permute_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<true>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<false>::kSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
     d.ready = true;
   }
   *out = &d;
   return MOE_OK;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against libcuda)
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2D row-major map: `inner` elements per row, `rows` rows, `stride` bytes
+// between rows, box of box_inner x box_rows, 128-byte swizzle
+int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+             uint64_t rows, uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return MOE_ERR_CUDA;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {stride};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
 struct Layout {
@@ -227,23 +268,61 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     gather_bf16_rows_kernel<<<grid_for(TK, 8, cap), 256, 0, stream>>>(
         x, w.perm, TK, H, T, reinterpret_cast<uint16_t*>(w.xq), d->status);
   st.launched();
-  const int ggrid = d->sms * 4;
-  st.mark();
-  if (act == MOE_ACT_MXFP8)
-    gemm1_simt_kernel<MOE_ACT_MXFP8><<<ggrid, 128, 0, stream>>>(w13, w13s, w.xq, w.xs, w.chunks,
-                                                               w.meta, H, I, w.hq, w.hs);
-  else
+  if (act == MOE_ACT_MXFP8) {
+    const unsigned long long timeout_ns =
+        (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
+    TcParams p1{};
+    if ((rc = make_map(&p1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
+                       H / 2, 128, 128)) ||
+        (rc = make_map(&p1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)))
+      return rc;
+    p1.w_sf = w13s;
+    p1.x_sf = w.xs;
+    p1.chunks = w.chunks;
+    p1.meta = w.meta;
+    p1.hq = w.hq;
+    p1.hs = w.hs;
+    p1.K = H;
+    p1.R = 2 * I;
+    p1.m_tiles = I / 128;
+    p1.half = I;
+    p1.out_dim = I;
+    p1.status = d->status;
+    p1.timeout_ns = timeout_ns;
+    TcParams p2{};
+    if ((rc = make_map(&p2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
+                       I / 2, 128, 128)) ||
+        (rc = make_map(&p2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
+      return rc;
+    p2.w_sf = w2s;
+    p2.x_sf = w.hs;
+    p2.chunks = w.chunks;
+    p2.meta = w.meta;
+    p2.yp = w.yp;
+    p2.K = I;
+    p2.R = H;
+    p2.m_tiles = H / 128;
+    p2.half = 0;
+    p2.out_dim = H;
+    p2.status = d->status;
+    p2.timeout_ns = timeout_ns;
+    st.mark();
+    gemm_tc_kernel<true><<<d->sms, kTcThreads, TcCfg<true>::kSmem, stream>>>(p1);
+    st.launched();
+    st.mark();
+    gemm_tc_kernel<false><<<d->sms, kTcThreads, TcCfg<false>::kSmem, stream>>>(p2);
+    st.launched();
+  } else {
+    const int ggrid = d->sms * 4;
+    st.mark();
     gemm1_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w13, w13s, w.xq, w.xs, w.chunks,
                                                               w.meta, H, I, w.hq, w.hs);
-  st.launched();
-  st.mark();
-  if (act == MOE_ACT_MXFP8)
-    gemm2_simt_kernel<MOE_ACT_MXFP8><<<ggrid, 128, 0, stream>>>(w2, w2s, w.hq, w.hs, w.chunks,
-                                                               w.meta, H, I, w.yp);
-  else
+    st.launched();
+    st.mark();
     gemm2_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w2, w2s, w.hq, w.hs, w.chunks,
                                                               w.meta, H, I, w.yp);
-  st.launched();
+    st.launched();
+  }
   st.mark();
   combine_kernel<<<grid_for((int64_t)T * H / 8, 256, cap), 256, 0, stream>>>(
       w.yp, w.pos, w.topk_w, T, H, k, static_cast<uint16_t*>(y));

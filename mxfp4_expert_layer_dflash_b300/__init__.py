@@ -11,7 +11,9 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_mxfp4.so")
+# MOE_MXFP4_LIB selects another build of the same library (e.g. one compiled with different
+# tuning knobs); by default the in-tree build is loaded
+LIB_PATH = os.environ.get("MOE_MXFP4_LIB") or os.path.join(_HERE, "libmoe_mxfp4.so")
 
 MOE_OK = 0
 MOE_ACT_MXFP8, MOE_ACT_BF16 = 0, 1

@@ -15,12 +15,13 @@ NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a",
               "-I", os.path.join(ROOT, "include")]
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    cmd = ["nvcc", *NVCC_FLAGS, "-o", LIB, SRC]
+def build(verbose_ptxas: bool = False, out: str = LIB, defines=()) -> str:
+    """Compile the library to ``out``; ``defines`` are extra -D tuning knobs."""
+    cmd = ["nvcc", *NVCC_FLAGS, *[f"-D{d}" for d in defines], "-o", out, SRC]
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     subprocess.check_call(cmd)
-    return LIB
+    return out
 
 
 if __name__ == "__main__":

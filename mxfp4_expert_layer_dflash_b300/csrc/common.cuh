@@ -11,7 +11,11 @@ namespace moe {
 
 // Assignments of one expert are processed in chunks of at most this many
 // slots (tokens); a chunk is the N dimension of one GEMM work item.
-constexpr int kChunkMax = 64;
+// MOE_TC_NMAX (32 or 64) is a compile-time tuning knob.
+#ifndef MOE_TC_NMAX
+#define MOE_TC_NMAX 64
+#endif
+constexpr int kChunkMax = MOE_TC_NMAX;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 

@@ -5,23 +5,35 @@
 // the tiny decode-time token count never pads the weight side.  A is FP4
 // (E2M1) straight from HBM: TMA's 16U4_ALIGN16B mode expands each 16-element
 // group into the 16-byte-aligned form the MMA reads, so no thread touches the
-// weights.  B is the MXFP8-E4M3 activation tile.  Both E8M0 scale sets go
-// to TMEM through tcgen05.cp and the MMA applies them per 32 elements
-// (kind::mxf8f6f4, block_scale).  Decode is bound by weight bandwidth
-// (ai.appwright.xyz, "第1層"); the pipeline keeps several weight tiles in
-// flight per SM while the tensor cores work on the previous ones (the
+// weights.  B is the MXFP8-E4M3 activation tile.  The E8M0 scales of both
+// operands are written into TMEM by a scale warpgroup and applied by the MMA
+// per 32 elements (kind::mxf8f6f4, block_scale).  Decode is bound by weight
+// bandwidth (ai.appwright.xyz, "第1層"); the pipeline keeps several weight
+// tiles in flight per SM while the tensor cores work on earlier ones (the
 // load/compute overlap of dothoosh.com, "TileRT", done here per kernel).
 //
-// Warp roles (256 threads, one CTA per SM, persistent over work items):
-//   warp 0     TMA producer (weights + activations), one lane
-//   warp 1     scale producer: cp.async of the E8M0 words into the layout
-//              tcgen05.cp expects, generic->async proxy fence, mbarrier arrive
-//   warp 2     TMEM owner and MMA issuer, one lane
-//   warps 4-7  epilogue: TMEM -> registers -> SwiGLU + MXFP8 requant (GEMM1)
-//              or fp32 rows of yp (GEMM2); warp w reads TMEM lanes 32*(w%4)..
-// Work item = (chunk of one expert's slots, 128-row tile of the output).
-// GEMM1 tiles pair gate rows [r, r+128) with up rows [I+r, I+r+128), so the
-// epilogue has both operands of silu(gate)*up for the same (row, token).
+// Both GEMMs load two 128-row weight tiles per stage that share one
+// activation tile: GEMM1 pairs gate rows [r, r+128) with up rows
+// [I+r, I+r+128) (so the epilogue has both operands of silu(gate)*up for the
+// same row and token); GEMM2 pairs output rows [r, r+128) with [r+128, r+256).
+// Two weight boxes per pipeline round keep the fixed cost of a round small
+// against the bytes it moves.
+//
+// Warp roles (384 threads, one CTA per SM, persistent over work items):
+//   warp 0      TMA producer (weight tiles + activation tile), one lane
+//   warp 2      TMEM owner and MMA issuer, one lane
+//   warps 4-7   scale stagers: warp w owns TMEM lanes 32*(w%4).. and writes the
+//               E8M0 words of each stage there with tcgen05.st, loading them
+//               from global memory a few stages ahead into a register ring
+//   warps 8-11  epilogue: TMEM -> registers -> SwiGLU + MXFP8 requant (GEMM1)
+//               or fp32 rows of yp (GEMM2)
+// Work item = (chunk of one expert's slots, one pair of weight tiles).
+//
+// Scale placement in TMEM (checked on the device by a layout probe): the MMA
+// reads the A scale of row m from lane m, column sfa + m/32, and the B scale
+// of token n from lane 32q + n%32 of every lane quarter q, column sfb + n/32;
+// the byte inside the 32-bit word is the instruction descriptor's scale id
+// (one per 32-element block of the 128-element stage).
 #pragma once
 
 #include <cuda.h>
@@ -32,11 +44,21 @@
 
 namespace moe {
 
-constexpr int kTcThreads = 256;
-constexpr int kBlockK = 128;  // K elements per stage: one TMA box of FP4
-constexpr int kBoxRowsB = 16; // activation rows per TMA box
+constexpr int kTcThreads = 384;
+constexpr int kBlockK = 128;   // K elements per stage: one TMA box of FP4
+constexpr int kBoxRowsB = 16;  // activation rows per TMA box
 constexpr int kNMax = kChunkMax;
-constexpr int kSfLag = 2;     // stages the scale producer runs ahead of its arrivals
+constexpr int kSfRing = 4;     // stages of scale words a stager keeps in registers
+
+// Tuning knobs (compile-time):
+//  MOE_TC_PF_W    L2 prefetch distance of weight tiles, in pipeline fills (0 = off)
+//  MOE_TC_PF_SF   L2 prefetch distance of scale sectors, in fills (0 = off)
+#ifndef MOE_TC_PF_W
+#define MOE_TC_PF_W 0
+#endif
+#ifndef MOE_TC_PF_SF
+#define MOE_TC_PF_SF 0
+#endif
 
 struct TcParams {
   CUtensorMap map_w;  // FP4 weights [E*R rows, K], 16U4_ALIGN16B, box {128, 128}, SW128
@@ -48,42 +70,71 @@ struct TcParams {
   uint8_t* hq;  // GEMM1 out: [T*k, I] E4M3
   uint8_t* hs;  // GEMM1 out: [T*k, I/32]
   float* yp;    // GEMM2 out: [T*k, H]
-  int K;        // reduction length
-  int R;        // weight rows per expert (2I or H)
-  int m_tiles;  // 128-row output tiles per expert (I/128 or H/128)
-  int half;     // GEMM1: row offset of the up half (I)
-  int out_dim;  // row length of the output (I or H)
+  int K;         // reduction length
+  int R;         // weight rows per expert (2I or H)
+  int m_tiles;   // tile pairs per expert (I/128 for GEMM1, H/256 for GEMM2)
+  int m_stride;  // weight rows between consecutive tile pairs (128 or 256)
+  int half;      // row offset of the second tile of a pair (I or 128)
+  int out_dim;   // row length of the output (I or H)
+  int rows_total;  // E * R: weight rows in the tensor (guards the odd last tile pair)
   int* status;
   unsigned long long timeout_ns;
 };
 
 template <bool kGated>
 struct TcCfg {
-  static constexpr int kA = kGated ? 2 : 1;           // A tiles per stage
-  static constexpr int kATile = 128 * 128;            // unpacked FP4 tile bytes
+  static constexpr int kA = 2;                 // A tiles per stage
+  static constexpr int kATile = 128 * 128;     // unpacked FP4 tile bytes
   static constexpr int kBTile = kNMax * 128;
-  static constexpr int kSf = 512;                     // one scale set: 32 rows x 16 B
-  static constexpr int kStageBytes = ((kA * kATile + kBTile + (kA + 1) * kSf) + 1023) / 1024 * 1024;
-  static constexpr int kStages = kGated ? 5 : 8;
-  static constexpr int kAccCols = kA * kNMax;         // one accumulator buffer
-  static constexpr int kSfBase = 2 * kAccCols;        // TMEM column of stage 0's scales
-  static constexpr int kSfStride = 16;                // TMEM columns per stage of scales
-  static constexpr int kTmemCols = kGated ? 512 : 256;
-  static constexpr uint32_t kTxA = 128 * 64;          // packed bytes of one weight box
+  static constexpr int kStageBytes = kA * kATile + kBTile;  // multiple of 1024
+  static constexpr int kStages = (232448 - 1024 - 256) / kStageBytes;
+  static constexpr int kAccCols = kA * kNMax;  // one accumulator buffer
+  static constexpr int kSfBase = 2 * kAccCols; // TMEM column of stage 0's scales
+  static constexpr int kSfStride = 16;         // TMEM columns per stage of scales
+  static constexpr int kSfbCol = 4 * kA;       // B scales after the A scale columns
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kTxA = 128 * 64;   // packed bytes of one weight box
+  static constexpr int kWords = kA + kNMax / 32;  // scale words per lane per stage
   static constexpr int kBarBytes = 256;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kNMax == 32 || kNMax == 64, "B-scale columns per stage");
   static_assert(kSfBase + kStages * kSfStride <= kTmemCols, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
+// Walks the (work item, k-stage) sequence of one CTA.
+struct FillCursor {
+  int item, ks, n_items, ksteps, m_tiles, step;
+  int4 ch;
+  int mt;
+  __device__ __forceinline__ void start(int first, int n, int kst, int mtl, int stp,
+                                        const int4* chunks) {
+    item = first;
+    ks = 0;
+    n_items = n;
+    ksteps = kst;
+    m_tiles = mtl;
+    step = stp;
+    ch = make_int4(0, 0, 0, 0);
+    mt = 0;
+    load(chunks);
+  }
+  __device__ __forceinline__ bool valid() const { return item < n_items; }
+  __device__ __forceinline__ void load(const int4* chunks) {
+    if (item < n_items) {
+      ch = chunks[item / m_tiles];
+      mt = item % m_tiles;
+    }
+  }
+  __device__ __forceinline__ void next(const int4* chunks) {
+    if (++ks == ksteps) {
+      ks = 0;
+      item += step;
+      load(chunks);
+    }
+  }
+};
 
 template <bool kGated>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
@@ -102,8 +153,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
-      ptx::mbar_init(&full[s], 1 + 32);  // TMA arrive.expect_tx + 32 scale-producer lanes
-      ptx::mbar_init(&empty[s], 1);      // MMA commit
+      ptx::mbar_init(&full[s], 1 + 4);  // TMA arrive.expect_tx + one arrival per scale warp
+      ptx::mbar_init(&empty[s], 1);     // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&acc_full[b], 1);   // MMA commit
@@ -139,85 +190,38 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
-      uint32_t fill = 0;
-      bool ok = true;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-        const int4 ch = p.chunks[item / p.m_tiles];
-        const int mt = item % p.m_tiles;
-        const int nrows = (ch.z + 15) & ~15;
-        const int row0 = ch.x * p.R + mt * 128;
-        const uint32_t tx = C::kA * C::kTxA + (uint32_t)(nrows / kBoxRowsB) * (kBoxRowsB * 128);
-        for (int ks = 0; ks < ksteps; ++ks, ++fill) {
-          const int s = (int)(fill % C::kStages);
-          const uint32_t use = fill / C::kStages;
-          if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
-            fail(kStatusTimeout);
-            ok = false;
-            break;
-          }
-          uint8_t* st = smem + s * C::kStageBytes;
-          ptx::mbar_arrive_expect_tx(&full[s], tx);
-          ptx::tma_load_2d(st, &p.map_w, &full[s], ks * kBlockK, row0, pol_w);
-          if (kGated)
-            ptx::tma_load_2d(st + C::kATile, &p.map_w, &full[s], ks * kBlockK, row0 + p.half,
-                             pol_w);
-          for (int r = 0; r < nrows; r += kBoxRowsB)
-            ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &p.map_x, &full[s], ks * kBlockK,
-                             ch.y + r, pol_x);
+      FillCursor pf;  // lookahead: weight tiles prefetched into L2 MOE_TC_PF_W fills ahead
+      pf.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
+      auto pf_step = [&]() {
+        if (pf.valid() && (pf.ks & 3) == 0) {  // 256-byte L2 fetches cover 4 boxes per row
+          const int prow = pf.ch.x * p.R + pf.mt * p.m_stride;
+          ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow);
+          ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow + p.half);
         }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ scale producer
-    // Stage layout of one scale set: 32 rows x 16 B; row L, word q holds the
-    // four E8M0 bytes (one per 32-element block of this stage) of operand row
-    // 32q + L.  tcgen05.cp 32x128b.warpx4 then puts operand row m at TMEM lane m
-    // of column m/32, which is where the block-scaled MMA reads it.
-    uint32_t fill = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x) {
-      const int4 ch = p.chunks[item / p.m_tiles];
-      const int mt = item % p.m_tiles;
-      const int row0 = ch.x * p.R + mt * 128;
-      for (int ks = 0; ks < ksteps; ++ks, ++fill) {
+        pf.next(p.chunks);
+      };
+      for (int i = 0; i < MOE_TC_PF_W; ++i) pf_step();
+      FillCursor c;
+      c.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
+      for (uint32_t fill = 0; c.valid(); ++fill, c.next(p.chunks)) {
         const int s = (int)(fill % C::kStages);
         const uint32_t use = fill / C::kStages;
         if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
-          if (lane == 0) fail(kStatusTimeout);
-          ok = false;
+          fail(kStatusTimeout);
           break;
         }
-        uint8_t* sf = smem + s * C::kStageBytes + C::kA * C::kATile + C::kBTile;
-#pragma unroll
-        for (int a = 0; a < C::kA; ++a) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int64_t row = (int64_t)row0 + a * p.half + q * 32 + lane;
-            ptx::cp_async_4(sf + a * C::kSf + lane * 16 + q * 4,
-                            p.w_sf + row * sf_row + ks * 4, 4);
-          }
-        }
-        uint8_t* sfb = sf + C::kA * C::kSf;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int n = q * 32 + lane;
-          const bool valid = n < ch.z;
-          const uint8_t* src = valid ? p.x_sf + (int64_t)(ch.y + n) * sf_row + ks * 4 : p.x_sf;
-          ptx::cp_async_4(sfb + lane * 16 + q * 4, src, valid ? 4u : 0u);
-        }
-        cp_async_commit();
-        if (fill >= (uint32_t)kSfLag) {
-          cp_async_wait_group<kSfLag>();
-          ptx::fence_proxy_async_smem();
-          ptx::mbar_arrive(&full[(fill - kSfLag) % C::kStages]);
-        }
+        const int nrows = (c.ch.z + 15) & ~15;
+        const int row0 = c.ch.x * p.R + c.mt * p.m_stride;
+        const uint32_t tx = C::kA * C::kTxA + (uint32_t)nrows * 128;
+        uint8_t* st = smem + s * C::kStageBytes;
+        ptx::mbar_arrive_expect_tx(&full[s], tx);
+        ptx::tma_load_2d(st, &p.map_w, &full[s], c.ks * kBlockK, row0, pol_w);
+        ptx::tma_load_2d(st + C::kATile, &p.map_w, &full[s], c.ks * kBlockK, row0 + p.half, pol_w);
+        for (int r = 0; r < nrows; r += kBoxRowsB)
+          ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &p.map_x, &full[s], c.ks * kBlockK,
+                           c.ch.y + r, pol_x);
+        if (MOE_TC_PF_W > 0) pf_step();
       }
-    }
-    cp_async_wait_group<0>();
-    ptx::fence_proxy_async_smem();
-    if (ok) {
-      const uint32_t first = fill > (uint32_t)kSfLag ? fill - kSfLag : 0;
-      for (uint32_t f = first; f < fill; ++f) ptx::mbar_arrive(&full[f % C::kStages]);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
@@ -248,24 +252,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           ptx::tc_fence_after();
           const uint32_t st = ptx::smem_u32(smem + s * C::kStageBytes);
           const uint32_t sa0 = st, sa1 = st + C::kATile, sb = st + C::kA * C::kATile;
-          const uint32_t ssf = sb + C::kBTile;
           const uint32_t tsf = tbase + C::kSfBase + s * C::kSfStride;
-#pragma unroll
-          for (int a = 0; a <= C::kA; ++a)
-            ptx::tmem_cp_32x128b_warpx4(tsf + 4 * a, ptx::smem_desc(ssf + a * C::kSf, 0, 128, 0));
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint32_t idesc = ptx::idesc_mxf8f6f4(N, kk, kk);
             const uint32_t accum = (ks | kk) ? 1u : 0u;
             ptx::mma_mxf8f6f4(acc0, ptx::desc_kmajor_sw128(sa0 + 32 * kk),
-                              ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf, tsf + 4 * C::kA,
+                              ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf, tsf + C::kSfbCol,
                               accum);
-            if (kGated)
-              ptx::mma_mxf8f6f4(acc1, ptx::desc_kmajor_sw128(sa1 + 32 * kk),
-                                ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf + 4,
-                                tsf + 4 * C::kA, accum);
+            ptx::mma_mxf8f6f4(acc1, ptx::desc_kmajor_sw128(sa1 + 32 * kk),
+                              ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf + 4,
+                              tsf + C::kSfbCol, accum);
           }
-          ptx::mma_commit(&empty[s]);  // frees the smem stage once these MMAs finish
+          ptx::mma_commit(&empty[s]);  // frees the smem stage and its scale columns
         }
         if (!ok) break;
         ptx::mma_commit(&acc_full[b]);
@@ -273,7 +272,83 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ptx::mma_commit(drain);
       if (!ptx::mbar_wait(drain, 0, deadline(), abort_flag)) fail(kStatusTimeout);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ scale stagers
+    const int q = warp & 3;
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    FillCursor ld, stc, pf;
+    ld.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
+    stc = ld;
+    pf = ld;
+    uint32_t ring[kSfRing][C::kWords];
+    // words of one fill for this lane: A scales of rows 32q+lane (+ up half),
+    // then B scales of tokens 32j+lane; unused B words are 0
+    auto load_words = [&](uint32_t (&w)[C::kWords], const FillCursor& c) {
+#pragma unroll
+      for (int i = 0; i < C::kWords; ++i) w[i] = 0;
+      if (!c.valid()) return;
+      const int64_t row = (int64_t)c.ch.x * p.R + c.mt * p.m_stride + q * 32 + lane;
+#pragma unroll
+      for (int a = 0; a < C::kA; ++a)
+        if (row + a * p.half < p.rows_total)
+          w[a] = __ldg(reinterpret_cast<const uint32_t*>(p.w_sf + (row + a * p.half) * sf_row +
+                                                         c.ks * 4));
+#pragma unroll
+      for (int jb = 0; jb < kNMax / 32; ++jb) {
+        const int n = jb * 32 + lane;
+        if (n < c.ch.z)
+          w[C::kA + jb] = __ldg(reinterpret_cast<const uint32_t*>(
+              p.x_sf + (int64_t)(c.ch.y + n) * sf_row + c.ks * 4));
+      }
+    };
+    auto pf_step = [&]() {  // scale sectors (8 stages each) of the lookahead fill into L2
+      if (pf.valid() && (pf.ks & 7) == 0) {
+        const int64_t row = (int64_t)pf.ch.x * p.R + pf.mt * p.m_stride + q * 32 + lane;
+#pragma unroll
+        for (int a = 0; a < C::kA; ++a)
+          if (row + a * p.half < p.rows_total)
+            ptx::prefetch_l2(p.w_sf + (row + a * p.half) * sf_row + pf.ks * 4);
+      }
+      pf.next(p.chunks);
+    };
+    for (int i = 0; i < MOE_TC_PF_SF; ++i) pf_step();
+#pragma unroll
+    for (int r = 0; r < kSfRing; ++r) {
+      load_words(ring[r], ld);
+      ld.next(p.chunks);
+    }
+    bool ok = true;
+    for (uint32_t f0 = 0; ok && stc.valid(); f0 += kSfRing) {
+#pragma unroll
+      for (int r = 0; r < kSfRing; ++r) {
+        if (!stc.valid()) break;
+        const uint32_t fill = f0 + r;
+        const int s = (int)(fill % C::kStages);
+        const uint32_t use = fill / C::kStages;
+        if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
+          if (lane == 0) fail(kStatusTimeout);
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t tsf = tbase + lane_off + C::kSfBase + s * C::kSfStride;
+#pragma unroll
+        for (int a = 0; a < C::kA; ++a) ptx::tmem_st_x1(tsf + 4 * a + q, ring[r][a]);
+        if (kNMax == 64)
+          ptx::tmem_st_x2(tsf + C::kSfbCol, ring[r][C::kA], ring[r][C::kWords - 1]);
+        else
+          ptx::tmem_st_x1(tsf + C::kSfbCol, ring[r][C::kA]);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&full[s]);
+        load_words(ring[r], ld);  // refill with the fill kSfRing ahead
+        ld.next(p.chunks);
+        if (MOE_TC_PF_SF > 0) pf_step();
+        stc.next(p.chunks);
+      }
+    }
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -289,11 +364,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
       ptx::tc_fence_after();
       const uint32_t acc0 = tbase + lane_off + b * C::kAccCols;
-      const int row = mt * 128 + q * 32 + lane;  // output row within the expert
+      const int row = mt * p.m_stride + q * 32 + lane;  // output row within the expert
       for (int n0 = 0; n0 < ch.z; n0 += 8) {
         uint32_t v0[8], v1[8];
         ptx::tmem_ld_x8(acc0 + n0, v0);
-        if (kGated) ptx::tmem_ld_x8(acc0 + kNMax + n0, v1);
+        ptx::tmem_ld_x8(acc0 + kNMax + n0, v1);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int t = 0; t < 8; ++t) {
@@ -307,6 +382,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
               if (lane == 0) p.hs[slot * (p.out_dim / 32) + row / 32] = (uint8_t)code;
             } else {
               p.yp[slot * p.out_dim + row] = __uint_as_float(v0[t]);
+              if (row + 128 < p.out_dim) p.yp[slot * p.out_dim + row + 128] = __uint_as_float(v1[t]);
             }
           }
         }

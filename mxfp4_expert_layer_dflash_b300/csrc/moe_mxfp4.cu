@@ -285,8 +285,10 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     p1.K = H;
     p1.R = 2 * I;
     p1.m_tiles = I / 128;
+    p1.m_stride = 128;
     p1.half = I;
     p1.out_dim = I;
+    p1.rows_total = E * 2 * I;
     p1.status = d->status;
     p1.timeout_ns = timeout_ns;
     TcParams p2{};
@@ -301,9 +303,11 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     p2.yp = w.yp;
     p2.K = I;
     p2.R = H;
-    p2.m_tiles = H / 128;
-    p2.half = 0;
+    p2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
+    p2.m_stride = 256;
+    p2.half = 128;
     p2.out_dim = H;
+    p2.rows_total = E * H;
     p2.status = d->status;
     p2.timeout_ns = timeout_ns;
     st.mark();

@@ -40,6 +40,9 @@ LAYERS = {
     "full_t8": Layer("full_t8", 6144, 2048, 384, 8, 8, 2),
     "full_t256": Layer("full_t256", 6144, 2048, 384, 8, 256, 3),
     "full_t1024_zipf": Layer("full_t1024_zipf", 6144, 2048, 384, 8, 1024, 4, zipf=True),
+    # full per-expert shape with 32 experts (0.64 GB of packed weights, larger than L2):
+    # the case detailed ncu captures run on
+    "full_e32_t64": Layer("full_e32_t64", 6144, 2048, 32, 8, 64, 5),
 }
 
 

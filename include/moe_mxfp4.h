@@ -174,6 +174,42 @@ int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t
                             uint8_t* scales, cudaStream_t stream);
 
 /*
+ * moe_mxfp4_forward_noalloc — moe_mxfp4_forward (same arguments, same result,
+ * MXFP8 activations) for callers that cannot allocate device memory.  The
+ * pages describe no such entry point; it exists for deployments where the
+ * code that runs the layer is not allowed to call cudaMalloc and has no
+ * workspace to hand over: plugin interfaces that give an operator only its
+ * input and output buffers and plan all memory up front, runtimes whose
+ * memory belongs to another allocator (a caching pool that direct cudaMalloc
+ * calls would fragment or bypass), and real-time services that allocate
+ * everything at start-up and forbid allocation on the serving path.
+ *
+ * Scratch: a file-scope device array of MOE_NOALLOC_SCRATCH_BYTES (80 MiB)
+ * inside this library.  Every device that loads the library holds that array
+ * until the process exits, whether or not this entry point is used.  The
+ * first call on each device looks up the array's device address (and does the
+ * library's other one-time set-up); make that first call before any stream
+ * capture.  The call allocates nothing: no cudaMalloc, cudaFree or allocating
+ * library routine.
+ *
+ * Limits and sharing:
+ *  - Shapes whose scratch (moe_mxfp4_workspace_size(T, H, I, E, k, 0)) exceeds
+ *    MOE_NOALLOC_SCRATCH_BYTES return MOE_ERR_NO_MEMORY before anything is
+ *    launched; at H = 6144, I = 2048, E = 384, k = 8 the largest T is 317.
+ *  - All calls share the one array and it keeps the last call's contents;
+ *    nothing in it needs to start at zero (every scratch byte a call reads is
+ *    written earlier in the same call).  Calls that overlap on the GPU (on
+ *    different streams, or from different threads, without ordering between
+ *    them) race on the array and give wrong results: order them.
+ * Other arguments, alignment rules and errors: as moe_mxfp4_forward.
+ */
+#define MOE_NOALLOC_SCRATCH_BYTES (80u * 1024u * 1024u)
+int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
+                              const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                              const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int T, int H, int I,
+                              int E, int k, void* y_bf16, cudaStream_t stream);
+
+/*
  * moe_mxfp4_get_status — synchronizes `stream`, returns the first device-side
  * error recorded since the last call (MOE_OK if none) and clears it.  A CUDA
  * error seen while synchronizing returns MOE_ERR_CUDA.

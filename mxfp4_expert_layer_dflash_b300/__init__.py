@@ -20,6 +20,7 @@ MOE_ACT_MXFP8, MOE_ACT_BF16 = 0, 1
 MOE_PATH_AUTO, MOE_PATH_MULTI, MOE_PATH_PERSISTENT = 0, 1, 2
 MOE_DEBUG_SHORT_TIMEOUT = 1
 MOE_MAX_K, MOE_MAX_E = 16, 1024
+MOE_NOALLOC_SCRATCH_BYTES = 80 * 1024 * 1024
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE",
           -3: "MOE_ERR_ALIGNMENT", -4: "MOE_ERR_CUDA", -5: "MOE_ERR_NO_MEMORY",
@@ -57,6 +58,8 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_forward.restype = i
         L.moe_mxfp4_forward_ex.argtypes = fwd + [ctypes.POINTER(moe_opts)]
         L.moe_mxfp4_forward_ex.restype = i
+        L.moe_mxfp4_forward_noalloc.argtypes = fwd
+        L.moe_mxfp4_forward_noalloc.restype = i
         L.moe_mxfp4_workspace_size.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_workspace_size.restype = sz
         L.mxfp4_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
@@ -116,6 +119,15 @@ def moe_mxfp4_forward_ex(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8
                                              _ptr(w13_e8m0), _ptr(w2_fp4), _ptr(w2_e8m0), T, H, I,
                                              E, k, _ptr(y_bf16), _stream(stream),
                                              ctypes.byref(o)), "moe_mxfp4_forward_ex")
+
+
+def moe_mxfp4_forward_noalloc(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,
+                              I, E, k, y_bf16, stream=None):
+    """moe_mxfp4_forward for callers that cannot allocate: scratch lives in a fixed-size
+    device array inside the library (MOE_NOALLOC_SCRATCH_BYTES)."""
+    return _check(lib().moe_mxfp4_forward_noalloc(
+        _ptr(x_bf16), _ptr(router_logits), _ptr(w13_fp4), _ptr(w13_e8m0), _ptr(w2_fp4),
+        _ptr(w2_e8m0), T, H, I, E, k, _ptr(y_bf16), _stream(stream)), "moe_mxfp4_forward_noalloc")
 
 
 def moe_mxfp4_workspace_size(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:

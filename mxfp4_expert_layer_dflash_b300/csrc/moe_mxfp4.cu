@@ -434,6 +434,63 @@ int moe_mxfp4_get_status(cudaStream_t stream) {
 
 uint64_t moe_mxfp4_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+// ---------------------------------------------------------------- no-alloc entry point
+//
+// Scratch for moe_mxfp4_forward_noalloc: a fixed-size array in the module's
+// global memory, created on every device that loads the library and kept
+// until the process exits.  Host code must not pass g_noalloc_scratch itself
+// to a kernel (in host code the name is a host-side stand-in, not a device
+// address); the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+namespace moe {
+namespace {
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices];
+
+// device address of g_noalloc_scratch on the current device (looked up once
+// per device, with that device current)
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_NO_DEVICE;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MOE_OK;
+}
+}  // namespace
+}  // namespace moe
+
+int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
+                              const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                              const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int T, int H, int I,
+                              int E, int k, void* y_bf16, cudaStream_t stream) {
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  if (layout_for(T, H, I, E, k, MOE_ACT_MXFP8).total > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
+    return MOE_ERR_NO_MEMORY;  // needs more scratch than the static array holds
+  if (T == 0) return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,
+                                  I, E, k, y_bf16, stream, nullptr);
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  void* scratch = nullptr;
+  if ((rc = noalloc_scratch(&scratch))) return rc;
+  moe_opts o{};
+  o.act_mode = MOE_ACT_MXFP8;
+  o.path = MOE_PATH_AUTO;
+  o.workspace = scratch;
+  o.workspace_bytes = MOE_NOALLOC_SCRATCH_BYTES;
+  return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I, E, k,
+                      y_bf16, stream, &o);
+}
+
 const char* moe_status_string(int status) {
   switch (status) {
     case MOE_OK: return "MOE_OK";

@@ -36,7 +36,7 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s at T=256; achieved HBM GB/s as fraction of B300 peak"
 UNIT = "tokens/s"
 PEAK_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.txt")
 KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f)
                   for f in sorted(os.listdir(os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300",
                                                           "csrc")))
@@ -61,6 +61,23 @@ def kernel_source_sha() -> str:
     for f in KERNEL_SOURCES:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
+
+
+def read_traffic(kernel: str, layer: str):
+    """DRAM bytes per launch of `kernel` on `layer` from the committed ncu summary, or None
+    when there is none or the kernel sources changed since it was captured."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE):
+        line = line.split("#", 1)[0].strip()
+        if ":" in line:
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha") != kernel_source_sha() or kv.get("layer") != layer:
+        return None
+    v = kv.get(f"{kernel}_dram_bytes_per_launch")
+    return float(v) if v else None
 
 
 def layer_bytes(L, cnt):
@@ -314,12 +331,7 @@ def run_ours(args, L, rank, world, local_rank):
     dominant = max(("gemm1", "gemm2"), key=lambda n: step_ms[n])
     dom_bytes = b_gemm1 if dominant == "gemm1" else b_gemm2
     achieved = dom_bytes / (step_ms[dominant] * 1e-3) / 1e9
-    traffic = None
-    if os.path.exists(TRAFFIC_FILE):
-        tf = json.load(open(TRAFFIC_FILE))
-        ent = tf.get(dominant)
-        if ent and tf.get("source_sha") == kernel_source_sha() and tf.get("layer") == L.name:
-            traffic = ent.get("dram_bytes_per_launch")
+    traffic = read_traffic(dominant, L.name)
     layer_gbs = b_layer / (ms * 1e-3) / 1e9
 
     out = {
@@ -366,7 +378,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layer", default="full_t256")
-    ap.add_argument("--cpu-tokens", type=int, default=8)
+    ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -48,7 +48,10 @@ constexpr int kTcThreads = 384;
 constexpr int kBlockK = 128;   // K elements per stage: one TMA box of FP4
 constexpr int kBoxRowsB = 16;  // activation rows per TMA box
 constexpr int kNMax = kChunkMax;
-constexpr int kSfRing = 4;     // stages of scale words a stager keeps in registers
+#ifndef MOE_TC_SF_RING
+#define MOE_TC_SF_RING 4
+#endif
+constexpr int kSfRing = MOE_TC_SF_RING;  // stages of scale words a stager keeps in registers
 
 // Tuning knobs (compile-time):
 //  MOE_TC_PF_W    L2 prefetch distance of weight tiles, in pipeline fills (0 = off)

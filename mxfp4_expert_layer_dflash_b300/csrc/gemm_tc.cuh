@@ -24,7 +24,7 @@
 //   warp 2      TMEM owner and MMA issuer, one lane
 //   warps 4-7   scale stagers: warp w owns TMEM lanes 32*(w%4).. and writes the
 //               E8M0 words of each stage there with tcgen05.st, loading them
-//               from global memory a few stages ahead into a register ring
+//               from global memory four to eight stages ahead into registers
 //   warps 8-11  epilogue: TMEM -> registers -> SwiGLU + MXFP8 requant (GEMM1)
 //               or fp32 rows of yp (GEMM2)
 // Work item = (chunk of one expert's slots, one pair of weight tiles).
@@ -48,19 +48,12 @@ constexpr int kTcThreads = 384;
 constexpr int kBlockK = 128;   // K elements per stage: one TMA box of FP4
 constexpr int kBoxRowsB = 16;  // activation rows per TMA box
 constexpr int kNMax = kChunkMax;
-#ifndef MOE_TC_SF_RING
-#define MOE_TC_SF_RING 4
-#endif
-constexpr int kSfRing = MOE_TC_SF_RING;  // stages of scale words a stager keeps in registers
+constexpr int kSfGroup = 4;    // fills per scale load group (16 bytes of scales per row)
 
-// Tuning knobs (compile-time):
-//  MOE_TC_PF_W    L2 prefetch distance of weight tiles, in pipeline fills (0 = off)
-//  MOE_TC_PF_SF   L2 prefetch distance of scale sectors, in fills (0 = off)
+// Tuning knob (compile-time): MOE_TC_PF_W = L2 prefetch distance of weight
+// tiles in pipeline fills (0 = off)
 #ifndef MOE_TC_PF_W
 #define MOE_TC_PF_W 0
-#endif
-#ifndef MOE_TC_PF_SF
-#define MOE_TC_PF_SF 0
 #endif
 
 struct TcParams {
@@ -277,78 +270,109 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ scale stagers
+    // Scale words are loaded a group of kSfGroup fills at a time, one group
+    // ahead of the group being written into TMEM.  When the scale rows allow it
+    // (K a multiple of 512), one 16-byte load per row covers the whole group,
+    // which keeps the scale traffic to a quarter of the L2 requests.
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    FillCursor ld, stc, pf;
+    const bool vec = (sf_row % 16) == 0 && (ksteps % kSfGroup) == 0;
+    FillCursor ld, stc;
     ld.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
     stc = ld;
-    pf = ld;
-    uint32_t ring[kSfRing][C::kWords];
-    // words of one fill for this lane: A scales of rows 32q+lane (+ up half),
-    // then B scales of tokens 32j+lane; unused B words are 0
-    auto load_words = [&](uint32_t (&w)[C::kWords], const FillCursor& c) {
+    // words of one fill for this lane: A scales of rows 32q+lane (+ second
+    // tile), then B scales of tokens 32j+lane; absent words are 0
+    uint32_t grp[2][kSfGroup][C::kWords];
+    auto load_group = [&](uint32_t (&g)[kSfGroup][C::kWords]) {
 #pragma unroll
-      for (int i = 0; i < C::kWords; ++i) w[i] = 0;
-      if (!c.valid()) return;
-      const int64_t row = (int64_t)c.ch.x * p.R + c.mt * p.m_stride + q * 32 + lane;
+      for (int i = 0; i < kSfGroup; ++i)
 #pragma unroll
-      for (int a = 0; a < C::kA; ++a)
-        if (row + a * p.half < p.rows_total)
-          w[a] = __ldg(reinterpret_cast<const uint32_t*>(p.w_sf + (row + a * p.half) * sf_row +
-                                                         c.ks * 4));
+        for (int w = 0; w < C::kWords; ++w) g[i][w] = 0;
+      if (vec) {  // the group's fills are ks .. ks+3 of one work item
+        if (ld.valid()) {
+          const int64_t row = (int64_t)ld.ch.x * p.R + ld.mt * p.m_stride + q * 32 + lane;
 #pragma unroll
-      for (int jb = 0; jb < kNMax / 32; ++jb) {
-        const int n = jb * 32 + lane;
-        if (n < c.ch.z)
-          w[C::kA + jb] = __ldg(reinterpret_cast<const uint32_t*>(
-              p.x_sf + (int64_t)(c.ch.y + n) * sf_row + c.ks * 4));
-      }
-    };
-    auto pf_step = [&]() {  // scale sectors (8 stages each) of the lookahead fill into L2
-      if (pf.valid() && (pf.ks & 7) == 0) {
-        const int64_t row = (int64_t)pf.ch.x * p.R + pf.mt * p.m_stride + q * 32 + lane;
+          for (int a = 0; a < C::kA; ++a) {
+            if (row + a * p.half < p.rows_total) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                  p.w_sf + (row + a * p.half) * sf_row + ld.ks * 4));
+              g[0][a] = v.x;
+              g[1][a] = v.y;
+              g[2][a] = v.z;
+              g[3][a] = v.w;
+            }
+          }
 #pragma unroll
-        for (int a = 0; a < C::kA; ++a)
-          if (row + a * p.half < p.rows_total)
-            ptx::prefetch_l2(p.w_sf + (row + a * p.half) * sf_row + pf.ks * 4);
-      }
-      pf.next(p.chunks);
-    };
-    for (int i = 0; i < MOE_TC_PF_SF; ++i) pf_step();
-#pragma unroll
-    for (int r = 0; r < kSfRing; ++r) {
-      load_words(ring[r], ld);
-      ld.next(p.chunks);
-    }
-    bool ok = true;
-    for (uint32_t f0 = 0; ok && stc.valid(); f0 += kSfRing) {
-#pragma unroll
-      for (int r = 0; r < kSfRing; ++r) {
-        if (!stc.valid()) break;
-        const uint32_t fill = f0 + r;
-        const int s = (int)(fill % C::kStages);
-        const uint32_t use = fill / C::kStages;
-        if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
-          if (lane == 0) fail(kStatusTimeout);
-          ok = false;
-          break;
+          for (int jb = 0; jb < kNMax / 32; ++jb) {
+            const int n = jb * 32 + lane;
+            if (n < ld.ch.z) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+                  p.x_sf + (int64_t)(ld.ch.y + n) * sf_row + ld.ks * 4));
+              g[0][C::kA + jb] = v.x;
+              g[1][C::kA + jb] = v.y;
+              g[2][C::kA + jb] = v.z;
+              g[3][C::kA + jb] = v.w;
+            }
+          }
         }
-        ptx::tc_fence_after();
-        const uint32_t tsf = tbase + lane_off + C::kSfBase + s * C::kSfStride;
 #pragma unroll
-        for (int a = 0; a < C::kA; ++a) ptx::tmem_st_x1(tsf + 4 * a + q, ring[r][a]);
-        if (kNMax == 64)
-          ptx::tmem_st_x2(tsf + C::kSfbCol, ring[r][C::kA], ring[r][C::kWords - 1]);
-        else
-          ptx::tmem_st_x1(tsf + C::kSfbCol, ring[r][C::kA]);
-        ptx::tmem_st_wait();
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&full[s]);
-        load_words(ring[r], ld);  // refill with the fill kSfRing ahead
-        ld.next(p.chunks);
-        if (MOE_TC_PF_SF > 0) pf_step();
-        stc.next(p.chunks);
+        for (int i = 0; i < kSfGroup; ++i) ld.next(p.chunks);
+      } else {
+#pragma unroll
+        for (int i = 0; i < kSfGroup; ++i) {
+          if (ld.valid()) {
+            const int64_t row = (int64_t)ld.ch.x * p.R + ld.mt * p.m_stride + q * 32 + lane;
+#pragma unroll
+            for (int a = 0; a < C::kA; ++a)
+              if (row + a * p.half < p.rows_total)
+                g[i][a] = __ldg(reinterpret_cast<const uint32_t*>(
+                    p.w_sf + (row + a * p.half) * sf_row + ld.ks * 4));
+#pragma unroll
+            for (int jb = 0; jb < kNMax / 32; ++jb) {
+              const int n = jb * 32 + lane;
+              if (n < ld.ch.z)
+                g[i][C::kA + jb] = __ldg(reinterpret_cast<const uint32_t*>(
+                    p.x_sf + (int64_t)(ld.ch.y + n) * sf_row + ld.ks * 4));
+            }
+          }
+          ld.next(p.chunks);
+        }
+      }
+    };
+    load_group(grp[0]);
+    load_group(grp[1]);
+    bool ok = true;
+    uint32_t fill = 0;
+    while (ok && stc.valid()) {
+#pragma unroll
+      for (int gi = 0; gi < 2; ++gi) {
+#pragma unroll
+        for (int i = 0; i < kSfGroup; ++i) {
+          if (ok && stc.valid()) {
+            const int s = (int)(fill % C::kStages);
+            const uint32_t use = fill / C::kStages;
+            if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
+              if (lane == 0) fail(kStatusTimeout);
+              ok = false;
+            } else {
+              ptx::tc_fence_after();
+              const uint32_t tsf = tbase + lane_off + C::kSfBase + s * C::kSfStride;
+#pragma unroll
+              for (int a = 0; a < C::kA; ++a) ptx::tmem_st_x1(tsf + 4 * a + q, grp[gi][i][a]);
+              if (kNMax == 64)
+                ptx::tmem_st_x2(tsf + C::kSfbCol, grp[gi][i][C::kA], grp[gi][i][C::kWords - 1]);
+              else
+                ptx::tmem_st_x1(tsf + C::kSfbCol, grp[gi][i][C::kA]);
+              ptx::tmem_st_wait();
+              ptx::tc_fence_before();
+              __syncwarp();
+              if (lane == 0) ptx::mbar_arrive(&full[s]);
+              ++fill;
+              stc.next(p.chunks);
+            }
+          }
+        }
+        if (ok && stc.valid()) load_group(grp[gi]);  // the group two ahead
       }
     }
   } else if (warp >= 8) {

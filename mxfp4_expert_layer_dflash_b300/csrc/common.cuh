@@ -10,12 +10,19 @@
 namespace moe {
 
 // Assignments of one expert are processed in chunks of at most this many
-// slots (tokens); a chunk is the N dimension of one GEMM work item.
-// MOE_TC_NMAX (32 or 64) is a compile-time tuning knob.
-#ifndef MOE_TC_NMAX
-#define MOE_TC_NMAX 64
+// slots (tokens); a chunk is the N dimension of one GEMM work item.  Narrow
+// chunks keep the GEMM pipeline deep (small activation tiles); wide chunks
+// halve the MMA instructions per token when experts receive many tokens.
+constexpr int kChunkNarrow = 64;
+#ifndef MOE_CHUNK_WIDE
+#define MOE_CHUNK_WIDE 96
 #endif
-constexpr int kChunkMax = MOE_TC_NMAX;
+constexpr int kChunkWide = MOE_CHUNK_WIDE;
+// layers with at least this many tokens use wide chunks (MXFP8 mode)
+#ifndef MOE_WIDE_MIN_TOKENS
+#define MOE_WIDE_MIN_TOKENS 512
+#endif
+constexpr int kWideMinTokens = MOE_WIDE_MIN_TOKENS;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128) gemm1_simt_kernel(
     const uint8_t* __restrict__ xq, const uint8_t* __restrict__ xs, const int4* __restrict__ chunks,
     const int32_t* __restrict__ meta, int H, int I, uint8_t* __restrict__ hq,
     uint8_t* __restrict__ hs) {
-  __shared__ float hbuf[kSimtRows][kChunkMax];
+  __shared__ float hbuf[kSimtRows][kChunkNarrow];  // bf16 mode always uses narrow chunks
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int iblocks = I / kSimtRows;
   const int64_t items = (int64_t)meta[0] * iblocks;

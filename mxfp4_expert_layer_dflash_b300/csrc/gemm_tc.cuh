@@ -47,7 +47,6 @@ namespace moe {
 constexpr int kTcThreads = 384;
 constexpr int kBlockK = 128;   // K elements per stage: one TMA box of FP4
 constexpr int kBoxRowsB = 16;  // activation rows per TMA box
-constexpr int kNMax = kChunkMax;
 constexpr int kSfGroup = 4;    // fills per scale load group (16 bytes of scales per row)
 
 // Tuning knob (compile-time): MOE_TC_PF_W = L2 prefetch distance of weight
@@ -55,10 +54,19 @@ constexpr int kSfGroup = 4;    // fills per scale load group (16 bytes of scales
 #ifndef MOE_TC_PF_W
 #define MOE_TC_PF_W 0
 #endif
+#ifndef MOE_TC_PF_EVERY
+#define MOE_TC_PF_EVERY 1  // prefetch every k-stage's boxes (or every n-th)
+#endif
+// MOE_TC_PF_LSU = distance in fills at which warp 1 prefetches weight rows into
+// L2 with plain prefetch instructions (which bypass the TMA engine); 0 = off
+#ifndef MOE_TC_PF_LSU
+#define MOE_TC_PF_LSU 0
+#endif
 
 struct TcParams {
   CUtensorMap map_w;  // FP4 weights [E*R rows, K], 16U4_ALIGN16B, box {128, 128}, SW128
   CUtensorMap map_x;  // E4M3 activations [T*k rows, K], u8, box {128, 16}, SW128
+  const uint8_t* w_packed;  // [E*R, K/2] the packed weights map_w describes
   const uint8_t* w_sf;  // [E*R, K/32]
   const uint8_t* x_sf;  // [T*k, K/32]
   const int4* chunks;
@@ -77,16 +85,18 @@ struct TcParams {
   unsigned long long timeout_ns;
 };
 
-template <bool kGated>
+template <bool kGated, int kNMax>
 struct TcCfg {
   static constexpr int kA = 2;                 // A tiles per stage
   static constexpr int kATile = 128 * 128;     // unpacked FP4 tile bytes
   static constexpr int kBTile = kNMax * 128;
   static constexpr int kStageBytes = kA * kATile + kBTile;  // multiple of 1024
   static constexpr int kStages = (232448 - 1024 - 256) / kStageBytes;
-  static constexpr int kAccCols = kA * kNMax;  // one accumulator buffer
-  static constexpr int kSfBase = 2 * kAccCols; // TMEM column of stage 0's scales
+  static constexpr int kAccCols = kA * kNMax;  // one accumulator buffer (gate|up or lo|hi)
   static constexpr int kSfStride = 16;         // TMEM columns per stage of scales
+  // accumulators are double-buffered when TMEM has room for two
+  static constexpr int kAccBufs = 2 * kAccCols + kStages * kSfStride <= 512 ? 2 : 1;
+  static constexpr int kSfBase = kAccBufs * kAccCols;   // TMEM column of stage 0's scales
   static constexpr int kSfbCol = 4 * kA;       // B scales after the A scale columns
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kTxA = 128 * 64;   // packed bytes of one weight box
@@ -94,7 +104,7 @@ struct TcCfg {
   static constexpr int kBarBytes = 256;
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + kBarBytes;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
-  static_assert(kNMax == 32 || kNMax == 64, "B-scale columns per stage");
+  static_assert(kNMax % 32 == 0 && kNMax <= 128, "B-scale columns per stage");
   static_assert(kSfBase + kStages * kSfStride <= kTmemCols, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -132,9 +142,9 @@ struct FillCursor {
   }
 };
 
-template <bool kGated>
+template <bool kGated, int kNMax>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<kGated>;
+  using C = TcCfg<kGated, kNMax>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -145,6 +155,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile uint32_t* prod_fill = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -155,9 +166,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     for (int b = 0; b < 2; ++b) {
       ptx::mbar_init(&acc_full[b], 1);   // MMA commit
       ptx::mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
-    }
+    }  // (only C::kAccBufs of the two are used)
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
+    *prod_fill = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       FillCursor pf;  // lookahead: weight tiles prefetched into L2 MOE_TC_PF_W fills ahead
       pf.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
       auto pf_step = [&]() {
-        if (pf.valid() && (pf.ks & 3) == 0) {  // 256-byte L2 fetches cover 4 boxes per row
+        if (pf.valid() && (pf.ks % MOE_TC_PF_EVERY) == 0) {
           const int prow = pf.ch.x * p.R + pf.mt * p.m_stride;
           ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow);
           ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow + p.half);
@@ -217,6 +229,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &p.map_x, &full[s], c.ks * kBlockK,
                            c.ch.y + r, pol_x);
         if (MOE_TC_PF_W > 0) pf_step();
+        if (MOE_TC_PF_LSU > 0) *prod_fill = fill + 1;
+      }
+    }
+  } else if (warp == 1 && MOE_TC_PF_LSU > 0) {
+    // ------------------------------------------------------------ L2 prefetcher
+    // Keeps the weight rows of the fills MOE_TC_PF_LSU ahead of the TMA
+    // producer in L2; one 128-byte line per row covers two k-stages.
+    FillCursor pf;
+    pf.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
+    const uint8_t* wbase = reinterpret_cast<const uint8_t*>(p.w_packed);
+    const int64_t row_bytes = p.K / 2;
+    uint32_t pfill = 0;
+    uint64_t idle_since = ptx::globaltimer();
+    while (pf.valid() && !*abort_flag) {
+      if (pfill < *prod_fill + MOE_TC_PF_LSU) {
+        if ((pf.ks & 1) == 0) {
+          const int64_t row0 = (int64_t)pf.ch.x * p.R + pf.mt * p.m_stride;
+#pragma unroll
+          for (int a = 0; a < 2; ++a)
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+              const int64_t row = row0 + a * p.half + qq * 32 + lane;
+              if (row < p.rows_total) ptx::prefetch_l2(wbase + row * row_bytes + pf.ks * 64);
+            }
+        }
+        ++pfill;
+        pf.next(p.chunks);
+        idle_since = ptx::globaltimer();
+      } else if (ptx::globaltimer() - idle_since > p.timeout_ns) {
+        break;  // the producer stopped advancing; nothing to report, just stop prefetching
       }
     }
   } else if (warp == 2) {
@@ -228,8 +270,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++j) {
         const int4 ch = p.chunks[item / p.m_tiles];
         const uint32_t N = (uint32_t)((ch.z + 15) & ~15);
-        const int b = j & 1;
-        const uint32_t u = (uint32_t)(j >> 1);
+        const int b = j % C::kAccBufs;
+        const uint32_t u = (uint32_t)(j / C::kAccBufs);
         if (!ptx::mbar_wait(&acc_empty[b], (u & 1) ^ 1, deadline(), abort_flag)) {
           fail(kStatusTimeout);
           break;
@@ -359,10 +401,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
               const uint32_t tsf = tbase + lane_off + C::kSfBase + s * C::kSfStride;
 #pragma unroll
               for (int a = 0; a < C::kA; ++a) ptx::tmem_st_x1(tsf + 4 * a + q, grp[gi][i][a]);
-              if (kNMax == 64)
-                ptx::tmem_st_x2(tsf + C::kSfbCol, grp[gi][i][C::kA], grp[gi][i][C::kWords - 1]);
-              else
-                ptx::tmem_st_x1(tsf + C::kSfbCol, grp[gi][i][C::kA]);
+#pragma unroll
+              for (int jb = 0; jb < kNMax / 32; ++jb)
+                ptx::tmem_st_x1(tsf + C::kSfbCol + jb, grp[gi][i][C::kA + jb]);
               ptx::tmem_st_wait();
               ptx::tc_fence_before();
               __syncwarp();
@@ -383,8 +424,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
       const int4 ch = p.chunks[item / p.m_tiles];
       const int mt = item % p.m_tiles;
-      const int b = j & 1;
-      const uint32_t u = (uint32_t)(j >> 1);
+      const int b = j % C::kAccBufs;
+      const uint32_t u = (uint32_t)(j / C::kAccBufs);
       if (!ptx::mbar_wait(&acc_full[b], u & 1, deadline(), abort_flag)) {
         if (lane == 0) fail(kStatusTimeout);
         break;

@@ -79,10 +79,18 @@ int device_state(DeviceState** out) {
     const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
     if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              permute_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<true>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<false>::kSmem) != cudaSuccess)
+        cudaFuncSetAttribute(gemm_tc_kernel<true, kChunkNarrow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<true, kChunkNarrow>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_kernel<false, kChunkNarrow>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<false, kChunkNarrow>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_kernel<true, kChunkWide>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<true, kChunkWide>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_tc_kernel<false, kChunkWide>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)TcCfg<false, kChunkWide>::kSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
     d.ready = true;
   }
@@ -131,7 +139,7 @@ Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act
   Layout L{};
   const int64_t TK = T * k;
   const int64_t act_bytes = act_mode == MOE_ACT_BF16 ? 2 : 1;
-  L.max_chunks = (int)(std::min<int64_t>(E, TK) + TK / kChunkMax + 1);
+  L.max_chunks = (int)(std::min<int64_t>(E, TK) + TK / kChunkNarrow + 1);
   size_t o = 0;
   auto take = [&](size_t bytes) {
     size_t at = o;
@@ -209,8 +217,8 @@ int grid_for(int64_t work, int per_block, int cap) {
 }
 
 // routing steps (1)-(4) into w
-int enqueue_route(const float* logits, int T, int E, int k, const Work& w, DeviceState* d,
-                  cudaStream_t s, Steps& st) {
+int enqueue_route(const float* logits, int T, int E, int k, int chunk_max, const Work& w,
+                  DeviceState* d, cudaStream_t s, Steps& st) {
   const int grid = grid_for((int64_t)T * 32, 256, 1 << 30);
   st.mark();
   if (E <= 128)
@@ -223,7 +231,8 @@ int enqueue_route(const float* logits, int T, int E, int k, const Work& w, Devic
   st.mark();
   const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
   route_permute_kernel<<<1, 1024, smem, s>>>(w.topk_idx, T, k, E, w.cnt, w.off, w.perm, w.pos,
-                                             w.chunks, w.max_chunks, w.meta, d->status);
+                                             w.chunks, w.max_chunks, chunk_max, w.meta,
+                                             d->status);
   st.launched();
   return launch_status();
 }
@@ -256,8 +265,12 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   const Work w = carve(ws, L);
   const int TK = T * k;
 
+  // Wide token chunks halve the MMA instructions per token when experts get
+  // many tokens (large T); narrow chunks keep the weight pipeline deepest.
+  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
   Steps st{opts, stream};
-  if ((rc = enqueue_route(logits, T, E, k, w, d, stream, st))) return rc;
+  if ((rc = enqueue_route(logits, T, E, k, wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
+    return rc;
   const int cap = d->sms * 8;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   st.mark();
@@ -276,6 +289,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
                        H / 2, 128, 128)) ||
         (rc = make_map(&p1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)))
       return rc;
+    p1.w_packed = w13;
     p1.w_sf = w13s;
     p1.x_sf = w.xs;
     p1.chunks = w.chunks;
@@ -296,6 +310,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
                        I / 2, 128, 128)) ||
         (rc = make_map(&p2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
       return rc;
+    p2.w_packed = w2;
     p2.w_sf = w2s;
     p2.x_sf = w.hs;
     p2.chunks = w.chunks;
@@ -311,10 +326,20 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     p2.status = d->status;
     p2.timeout_ns = timeout_ns;
     st.mark();
-    gemm_tc_kernel<true><<<d->sms, kTcThreads, TcCfg<true>::kSmem, stream>>>(p1);
+    if (wide)
+      gemm_tc_kernel<true, kChunkWide>
+          <<<d->sms, kTcThreads, TcCfg<true, kChunkWide>::kSmem, stream>>>(p1);
+    else
+      gemm_tc_kernel<true, kChunkNarrow>
+          <<<d->sms, kTcThreads, TcCfg<true, kChunkNarrow>::kSmem, stream>>>(p1);
     st.launched();
     st.mark();
-    gemm_tc_kernel<false><<<d->sms, kTcThreads, TcCfg<false>::kSmem, stream>>>(p2);
+    if (wide)
+      gemm_tc_kernel<false, kChunkWide>
+          <<<d->sms, kTcThreads, TcCfg<false, kChunkWide>::kSmem, stream>>>(p2);
+    else
+      gemm_tc_kernel<false, kChunkNarrow>
+          <<<d->sms, kTcThreads, TcCfg<false, kChunkNarrow>::kSmem, stream>>>(p2);
     st.launched();
   } else {
     const int ggrid = d->sms * 4;
@@ -400,7 +425,7 @@ int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* to
   w.perm = perm;
   w.pos = pos;
   Steps st{nullptr, stream};
-  return enqueue_route(router_logits, T, E, k, w, d, stream, st);
+  return enqueue_route(router_logits, T, E, k, kChunkNarrow, w, d, stream, st);
 }
 
 int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t* codes,

@@ -105,7 +105,8 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 __global__ void __launch_bounds__(1024) route_permute_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ cnt_out,
     int32_t* __restrict__ off_out, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
-    int4* __restrict__ chunks, int max_chunks, int32_t* __restrict__ meta, int* status) {
+    int4* __restrict__ chunks, int max_chunks, int chunk_max, int32_t* __restrict__ meta,
+    int* status) {
   extern __shared__ int smem[];
   int* s_cnt = smem;          // E
   int* s_off = s_cnt + E;     // E + 1
@@ -175,8 +176,8 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
   }
 
   // chunk list: touched experts in ascending order, each split into
-  // ceil(n / kChunkMax) chunks of near-equal size
-  const int nch = c > 0 ? (c + kChunkMax - 1) / kChunkMax : 0;
+  // ceil(n / chunk_max) chunks of near-equal size
+  const int nch = c > 0 ? (c + chunk_max - 1) / chunk_max : 0;
   const int cbase = block_exclusive_scan_1024(nch, s_warp, &s_tot[0]);
   const int touched = block_exclusive_scan_1024(c > 0 ? 1 : 0, s_warp, &s_tot[1]);
   (void)touched;

@@ -191,7 +191,9 @@ def _layer_inputs(O, T, H, I, E, k, seed, logits=None):
 @pytest.mark.parametrize("T,H,I,E,k,ties", [(1, 256, 128, 8, 2, False), (13, 128, 256, 5, 5, False),
                                             (200, 128, 128, 2, 1, False),
                                             (150, 256, 128, 4, 2, True), (7, 384, 384, 1, 1, False),
-                                            (33, 512, 128, 16, 16, False)])
+                                            (33, 512, 128, 16, 16, False),
+                                            (600, 256, 128, 4, 2, False),
+                                            (520, 128, 256, 3, 1, True)])
 @pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
 def test_forward_edge_shapes(O, T, H, I, E, k, ties, act):
     lg = np.zeros((T, E), np.float32) if ties else None   # ties: all tokens on experts 0..k-1

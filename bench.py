@@ -41,7 +41,10 @@ KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f
                   for f in sorted(os.listdir(os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300",
                                                           "csrc")))
                   if f.endswith((".cu", ".cuh"))]
-STEP_NAMES = ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"]
+# kernels of one forward in launch order, per execution path
+STEP_NAMES = {1: ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"],
+              2: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2", "combine"]}
+PATHS = {"auto": 0, "multi": 1, "persistent": 2}
 
 
 def log(*a):
@@ -253,13 +256,15 @@ def run_ours(args, L, rank, world, local_rank):
     moe.moe_mxfp4_route(lg, L.T, L.E, L.k, tk[0], tk[1], cnt, *aux)
     touched, b_gemm1, b_gemm2, b_layer = layer_bytes(L, cnt.cpu().numpy())
 
+    path = PATHS[args.path] or moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E, L.k)
+    names = STEP_NAMES[path]
     ev = Events()
-    nsteps = len(STEP_NAMES) + 1
+    nsteps = len(names) + 1
     marks = [ev.create(nsteps) for _ in range(args.steps)]
 
     def fwd(step_events=None):
         moe.moe_mxfp4_forward_ex(x, lg, w13, s13, w2, s2, L.T, L.H, L.I, L.E, L.k, y, stream,
-                                 step_events=step_events)
+                                 path=path, step_events=step_events)
 
     for _ in range(args.warmup):
         fwd()
@@ -285,9 +290,9 @@ def run_ours(args, L, rank, world, local_rank):
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
 
-    per_step = {n: [] for n in STEP_NAMES}
+    per_step = {n: [] for n in names}
     for m in marks:
-        for j, n in enumerate(STEP_NAMES):
+        for j, n in enumerate(names):
             per_step[n].append(ev.elapsed_ms(m[j], m[j + 1]))
     step_ms = {n: statistics.mean(v) for n, v in per_step.items()}
     for m in marks:
@@ -328,8 +333,9 @@ def run_ours(args, L, rank, world, local_rank):
 
     pk, pk_src = peaks()
     hbm = float(pk["hbm_gbs"])
-    dominant = max(("gemm1", "gemm2"), key=lambda n: step_ms[n])
-    dom_bytes = b_gemm1 if dominant == "gemm1" else b_gemm2
+    gemm_bytes = {"gemm1": b_gemm1, "gemm2": b_gemm2, "gemm1+gemm2": b_gemm1 + b_gemm2}
+    dominant = max((n for n in names if n in gemm_bytes), key=lambda n: step_ms[n])
+    dom_bytes = gemm_bytes[dominant]
     achieved = dom_bytes / (step_ms[dominant] * 1e-3) / 1e9
     traffic = read_traffic(dominant, L.name)
     layer_gbs = b_layer / (ms * 1e-3) / 1e9
@@ -342,7 +348,8 @@ def run_ours(args, L, rank, world, local_rank):
         "config": {"workload": f"{L.name}: {L.desc}", "global_batch": world * L.T,
                    "seq_len": 8, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (packed weights %.2f GB)" % (b_layer / 1e9),
-                   "touched_experts": touched, "act_mode": "mxfp8"},
+                   "touched_experts": touched, "act_mode": "mxfp8",
+                   "path": {1: "multi", 2: "persistent"}[path]},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{pk_src} hbm_gbs", "algorithmic_bytes": dom_bytes},
@@ -357,15 +364,19 @@ def run_ours(args, L, rank, world, local_rank):
     }
     if world == 1 and not args.no_cpu_baseline:
         log("[rank 0] timing the CPU oracle on a bounded sample")
-        n_tok = args.cpu_tokens
+        n_tok = min(args.cpu_tokens, L.T)
         run, n_exp = oracle_sample(L, n_tok)
-        t0 = time.perf_counter()
-        run(list(range(min(n_tok, L.T))))
-        dt = time.perf_counter() - t0
+        reps, t0 = 0, time.perf_counter()
+        while True:               # repeat the sample until at least --cpu-seconds of work
+            run(list(range(n_tok)))
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= args.cpu_seconds:
+                break
         out["cpu_baseline"] = {
-            "value": min(n_tok, L.T) / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"first {min(n_tok, L.T)} of {L.T} tokens ({n_exp} experts), fp64 oracle "
-                      f"in MXFP8-emulation mode, {dt:.2f} s; MXFP4 packing excluded"}
+            "value": reps * n_tok / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"first {n_tok} of {L.T} tokens ({n_exp} experts) x {reps} repeats, fp64 "
+                      f"oracle in MXFP8-emulation mode, {dt:.1f} s; MXFP4 packing excluded"}
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -378,7 +389,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layer", default="full_t256")
+    ap.add_argument("--path", choices=sorted(PATHS), default="auto")
     ap.add_argument("--cpu-tokens", type=int, default=32)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -65,10 +65,10 @@ typedef enum {
 #define MOE_ACT_MXFP8 0  /* x and h quantized to MXFP8-E4M3 (blocks of 32) */
 #define MOE_ACT_BF16 1   /* x used as bf16, h rounded to bf16 */
 
-/* execution paths of moe_opts.path */
-#define MOE_PATH_AUTO 0
+/* execution paths of moe_opts.path (the bf16 mode always runs the multi path) */
+#define MOE_PATH_AUTO 0       /* moe_mxfp4_select_path decides */
 #define MOE_PATH_MULTI 1      /* routing kernels, GEMM1, GEMM2, combine */
-#define MOE_PATH_PERSISTENT 2 /* routing kernels, then one persistent kernel */
+#define MOE_PATH_PERSISTENT 2 /* routing kernels, one kernel for both GEMMs, combine */
 
 /*
  * moe_mxfp4_forward — the MoE expert layer.
@@ -116,7 +116,7 @@ typedef struct {
    * step_events[i] on `stream` just before the i-th kernel of the call and one
    * more after the last (i < n_step_events).  Kernel order: multi path —
    * route_topk, route_permute, act_quant, gemm1, gemm2, combine; persistent
-   * path — route_topk, route_permute, act_quant, moe_persistent. */
+   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine. */
   cudaEvent_t* step_events;
   int n_step_events;
 } moe_opts;
@@ -133,6 +133,18 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
                          const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
                          int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream,
                          const moe_opts* opts);
+
+/*
+ * moe_mxfp4_select_path — the path MOE_PATH_AUTO takes for this shape on the
+ * current device: MOE_PATH_PERSISTENT when a bound on the GEMM work items
+ * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is at most 24 per SM,
+ * else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  The single
+ * launch saves the gap and tail between the GEMMs on layers with few work
+ * items per SM; two launches stream weights faster on large ones.  The paths
+ * give bitwise equal results.  Returns a negative moe_status on invalid
+ * arguments.  No counterpart in the papers: a support call.
+ */
+int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode);
 
 /* bytes of scratch a forward of this shape needs (0 on invalid arguments) */
 size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode);

@@ -60,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_forward_ex.restype = i
         L.moe_mxfp4_forward_noalloc.argtypes = fwd
         L.moe_mxfp4_forward_noalloc.restype = i
+        L.moe_mxfp4_select_path.argtypes = [i, i, i, i, i, i]
+        L.moe_mxfp4_select_path.restype = i
         L.moe_mxfp4_workspace_size.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_workspace_size.restype = sz
         L.mxfp4_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
@@ -132,6 +134,15 @@ def moe_mxfp4_forward_noalloc(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, 
 
 def moe_mxfp4_workspace_size(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
     return int(lib().moe_mxfp4_workspace_size(T, H, I, E, k, act_mode))
+
+
+def moe_mxfp4_select_path(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
+    """The path MOE_PATH_AUTO takes on the current device (MOE_PATH_MULTI or
+    MOE_PATH_PERSISTENT)."""
+    rc = int(lib().moe_mxfp4_select_path(T, H, I, E, k, act_mode))
+    if rc < 0:
+        raise MoeError(rc, "moe_mxfp4_select_path")
+    return rc
 
 
 def mxfp4_quantize(w, rows, K, out_fp4, out_e8m0, stream=None):

@@ -23,6 +23,12 @@ constexpr int kChunkWide = MOE_CHUNK_WIDE;
 #define MOE_WIDE_MIN_TOKENS 512
 #endif
 constexpr int kWideMinTokens = MOE_WIDE_MIN_TOKENS;
+// automatic path choice: one persistent launch for both GEMMs when the bound
+// on GEMM work items is at most this many per SM
+#ifndef MOE_PERSISTENT_ITEMS_PER_SM
+#define MOE_PERSISTENT_ITEMS_PER_SM 24
+#endif
+constexpr int kPersistentItemsPerSm = MOE_PERSISTENT_ITEMS_PER_SM;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 
@@ -36,6 +42,7 @@ struct Work {
   int32_t* perm;      // [T*k] slot -> token
   int32_t* pos;       // [T*k] (t*k+j) -> slot
   int4* chunks;       // [max_chunks] {expert, first slot, n slots, 0}
+  int32_t* done;      // [max_chunks] GEMM1 publications per chunk (persistent path)
   int32_t* meta;      // [0] chunk count, [1] touched experts, [2..] step counters
   uint8_t* xq;        // [T*k, H] E4M3 (MXFP8) or [T*k, H] bf16 (bf16 mode)
   uint8_t* xs;        // [T*k, H/32] E8M0

@@ -1,21 +1,29 @@
 // Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05), MXFP8 mode.
 //
 // Swap-AB: the expert's weight rows fill the 128-row MMA dimension (A) and the
-// expert's tokens (a chunk of at most kChunkMax slots, padded to 16) are N, so
-// the tiny decode-time token count never pads the weight side.  A is FP4
-// (E2M1) straight from HBM: TMA's 16U4_ALIGN16B mode expands each 16-element
-// group into the 16-byte-aligned form the MMA reads, so no thread touches the
+// expert's tokens (a chunk of slots, padded to 16) are N, so the tiny
+// decode-time token count never pads the weight side.  A is FP4 (E2M1)
+// straight from HBM: TMA's 16U4_ALIGN16B mode expands each 16-element group
+// into the 16-byte-aligned form the MMA reads, so no thread touches the
 // weights.  B is the MXFP8-E4M3 activation tile.  The E8M0 scales of both
 // operands are written into TMEM by a scale warpgroup and applied by the MMA
 // per 32 elements (kind::mxf8f6f4, block_scale).  Decode is bound by weight
 // bandwidth (ai.appwright.xyz, "第1層"); the pipeline keeps several weight
 // tiles in flight per SM while the tensor cores work on earlier ones (the
-// load/compute overlap of dothoosh.com, "TileRT", done here per kernel).
+// load/compute overlap of dothoosh.com, "TileRT").
 //
-// Both GEMMs load two 128-row weight tiles per stage that share one
-// activation tile: GEMM1 pairs gate rows [r, r+128) with up rows
-// [I+r, I+r+128) (so the epilogue has both operands of silu(gate)*up for the
-// same row and token); GEMM2 pairs output rows [r, r+128) with [r+128, r+256).
+// One kernel body runs one or two phases:
+//   phase GEMM1: z = W13_e x, h = silu(gate) * up, MXFP8-requantised into
+//                hq/hs (gate rows [r, r+128) paired with up rows [I+r, I+r+128),
+//                so the epilogue has both operands for the same row and token);
+//   phase GEMM2: yp = W2_e h (fp32), output rows [r, r+128) paired with
+//                [r+128, r+256).
+// The multi-kernel path launches it once per phase; the persistent path runs
+// both phases in one launch (the single resident engine kernel of dothoosh.com,
+// "TileRT", for this layer): every CTA walks its GEMM1 items, then its GEMM2
+// items, and a GEMM2 item waits (bounded) until all GEMM1 items of its token
+// chunk have published h.  Each CTA finishes its GEMM1 items before any GEMM2
+// item and all CTAs are resident, so every wait is on work that is running.
 // Two weight boxes per pipeline round keep the fixed cost of a round small
 // against the bytes it moves.
 //
@@ -25,8 +33,7 @@
 //   warps 4-7   scale stagers: warp w owns TMEM lanes 32*(w%4).. and writes the
 //               E8M0 words of each stage there with tcgen05.st, loading them
 //               from global memory four to eight stages ahead into registers
-//   warps 8-11  epilogue: TMEM -> registers -> SwiGLU + MXFP8 requant (GEMM1)
-//               or fp32 rows of yp (GEMM2)
+//   warps 8-11  epilogue: TMEM -> registers -> SwiGLU + MXFP8 requant, or fp32
 // Work item = (chunk of one expert's slots, one pair of weight tiles).
 //
 // Scale placement in TMEM (checked on the device by a layout probe): the MMA
@@ -49,43 +56,35 @@ constexpr int kBlockK = 128;   // K elements per stage: one TMA box of FP4
 constexpr int kBoxRowsB = 16;  // activation rows per TMA box
 constexpr int kSfGroup = 4;    // fills per scale load group (16 bytes of scales per row)
 
-// Tuning knob (compile-time): MOE_TC_PF_W = L2 prefetch distance of weight
-// tiles in pipeline fills (0 = off)
-#ifndef MOE_TC_PF_W
-#define MOE_TC_PF_W 0
-#endif
-#ifndef MOE_TC_PF_EVERY
-#define MOE_TC_PF_EVERY 1  // prefetch every k-stage's boxes (or every n-th)
-#endif
-// MOE_TC_PF_LSU = distance in fills at which warp 1 prefetches weight rows into
-// L2 with plain prefetch instructions (which bypass the TMA engine); 0 = off
-#ifndef MOE_TC_PF_LSU
-#define MOE_TC_PF_LSU 0
-#endif
-
-struct TcParams {
+struct TcPhase {
   CUtensorMap map_w;  // FP4 weights [E*R rows, K], 16U4_ALIGN16B, box {128, 128}, SW128
   CUtensorMap map_x;  // E4M3 activations [T*k rows, K], u8, box {128, 16}, SW128
-  const uint8_t* w_packed;  // [E*R, K/2] the packed weights map_w describes
   const uint8_t* w_sf;  // [E*R, K/32]
   const uint8_t* x_sf;  // [T*k, K/32]
+  int K;           // reduction length
+  int R;           // weight rows per expert (2I or H)
+  int m_tiles;     // tile pairs per expert (I/128 for GEMM1, ceil(H/256) for GEMM2)
+  int m_stride;    // weight rows between consecutive tile pairs (128 or 256)
+  int half;        // row offset of the second tile of a pair (I or 128)
+  int out_dim;     // row length of the output (I or H)
+  int rows_total;  // E * R: weight rows in the tensor (guards an odd last tile pair)
+  int dep_target;  // (GEMM2 of a persistent launch) GEMM1 publications per chunk to wait
+                   // for: 4 epilogue warps x tile pairs
+};
+
+struct TcParams {
+  TcPhase ph[2];  // [0] = the launch's (first) GEMM, [1] = GEMM2 of a persistent launch
   const int4* chunks;
-  const int32_t* meta;
-  uint8_t* hq;  // GEMM1 out: [T*k, I] E4M3
-  uint8_t* hs;  // GEMM1 out: [T*k, I/32]
-  float* yp;    // GEMM2 out: [T*k, H]
-  int K;         // reduction length
-  int R;         // weight rows per expert (2I or H)
-  int m_tiles;   // tile pairs per expert (I/128 for GEMM1, H/256 for GEMM2)
-  int m_stride;  // weight rows between consecutive tile pairs (128 or 256)
-  int half;      // row offset of the second tile of a pair (I or 128)
-  int out_dim;   // row length of the output (I or H)
-  int rows_total;  // E * R: weight rows in the tensor (guards the odd last tile pair)
+  const int32_t* meta;  // meta[0] = chunk count
+  uint8_t* hq;          // [T*k, I] E4M3
+  uint8_t* hs;          // [T*k, I/32]
+  float* yp;            // [T*k, H]
+  int* gemm1_done;      // [chunks] GEMM1 epilogue-warp publications per chunk (persistent path)
   int* status;
   unsigned long long timeout_ns;
 };
 
-template <bool kGated, int kNMax>
+template <int kNMax>
 struct TcCfg {
   static constexpr int kA = 2;                 // A tiles per stage
   static constexpr int kATile = 128 * 128;     // unpacked FP4 tile bytes
@@ -109,42 +108,95 @@ struct TcCfg {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-// Walks the (work item, k-stage) sequence of one CTA.
+// Kernel modes: one GEMM per launch, or both GEMMs in one persistent launch.
+constexpr int kModeGemm1 = 0, kModeGemm2 = 1, kModeBoth = 2;
+
+// Walks the (work item, k-stage) sequence of one CTA over all phases
+// (kPhases is 1 for single-GEMM launches, so the phase folds to a constant).
+template <int kPhases>
 struct FillCursor {
-  int item, ks, n_items, ksteps, m_tiles, step;
+  // per-launch constants, copied once (no parameter-space reads per item)
+  const int4* chunks;
+  int step, n0, ntot;      // n0: items of phase 0; ntot: items of all phases
+  int mtl[2], kst[2];      // tile pairs per chunk and k-stages per item, per phase
+  // position
+  int item, ks, phase, mt, ksteps, chunk;
   int4 ch;
-  int mt;
-  __device__ __forceinline__ void start(int first, int n, int kst, int mtl, int stp,
-                                        const int4* chunks) {
+  __device__ __forceinline__ void start(const TcParams& p, int first, int stp, int items0,
+                                        int items_all) {
+    chunks = p.chunks;
+    step = stp;
+    n0 = items0;
+    ntot = items_all;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      mtl[i] = p.ph[i < kPhases ? i : 0].m_tiles;
+      kst[i] = p.ph[i < kPhases ? i : 0].K / kBlockK;
+    }
     item = first;
     ks = 0;
-    n_items = n;
-    ksteps = kst;
-    m_tiles = mtl;
-    step = stp;
-    ch = make_int4(0, 0, 0, 0);
+    phase = 0;
     mt = 0;
-    load(chunks);
+    ksteps = 1;
+    chunk = 0;
+    ch = make_int4(0, 0, 0, 0);
+    load();
   }
-  __device__ __forceinline__ bool valid() const { return item < n_items; }
-  __device__ __forceinline__ void load(const int4* chunks) {
-    if (item < n_items) {
-      ch = chunks[item / m_tiles];
-      mt = item % m_tiles;
+  __device__ __forceinline__ bool valid() const { return item < ntot; }
+  __device__ __forceinline__ void load() {
+    if (item < ntot) {
+      phase = (kPhases > 1 && item >= n0) ? 1 : 0;
+      const int local = item - (phase ? n0 : 0);
+      const int m = phase ? mtl[1] : mtl[0];
+      chunk = local / m;
+      mt = local % m;
+      ch = chunks[chunk];
+      ksteps = phase ? kst[1] : kst[0];
     }
   }
-  __device__ __forceinline__ void next(const int4* chunks) {
-    if (++ks == ksteps) {
-      ks = 0;
-      item += step;
-      load(chunks);
-    }
+  __device__ __forceinline__ void next() {
+    if (++ks == ksteps) next_item();
+  }
+  __device__ __forceinline__ void next_item() {
+    ks = 0;
+    item += step;
+    load();
   }
 };
 
-template <bool kGated, int kNMax>
+__device__ __forceinline__ int ld_acquire(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_add(int* ptr, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// bounded wait until GEMM1 has published every tile pair of `chunk`
+__device__ __forceinline__ bool wait_chunk_ready(const TcParams& p, int chunk, int target,
+                                                 unsigned long long timeout_ns,
+                                                 const volatile int* abort) {
+  const uint64_t deadline = ptx::globaltimer() + timeout_ns;
+  while (ld_acquire(p.gemm1_done + chunk) < target) {
+    if (*abort || ptx::globaltimer() > deadline) return false;
+  }
+  return true;
+}
+
+template <int kNMax, int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using C = TcCfg<kGated, kNMax>;
+  using C = TcCfg<kNMax>;
+  constexpr int kPhases = kMode == kModeBoth ? 2 : 1;
+  using Cursor = FillCursor<kPhases>;
+  // is this phase the SwiGLU GEMM1 / a GEMM2 waiting on same-launch h?
+  auto gated_phase = [](int phase) { return kMode == kModeGemm1 || (kMode == kModeBoth && phase == 0); };
+  auto dep_phase = [](int phase) { return kMode == kModeBoth && phase == 1; };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -155,7 +207,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile uint32_t* prod_fill = reinterpret_cast<volatile uint32_t*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -163,13 +214,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ptx::mbar_init(&full[s], 1 + 4);  // TMA arrive.expect_tx + one arrival per scale warp
       ptx::mbar_init(&empty[s], 1);     // MMA commit
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 2; ++b) {       // (only C::kAccBufs of the two are used)
       ptx::mbar_init(&acc_full[b], 1);   // MMA commit
       ptx::mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
-    }  // (only C::kAccBufs of the two are used)
+    }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
-    *prod_fill = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -177,17 +227,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     ptx::tmem_relinquish();
   }
   if (warp == 0 && lane == 0) {
-    ptx::prefetch_tmap(&p.map_w);
-    ptx::prefetch_tmap(&p.map_x);
+    for (int ph = 0; ph < kPhases; ++ph) {
+      ptx::prefetch_tmap(&p.ph[ph].map_w);
+      ptx::prefetch_tmap(&p.ph[ph].map_x);
+    }
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  const int n_items = p.meta[0] * p.m_tiles;
-  const int ksteps = p.K / kBlockK;
-  const int sf_row = p.K / 32;  // scale bytes per row
+  const int n_chunks = p.meta[0];
+  const int items0 = n_chunks * p.ph[0].m_tiles;
+  const int items_all = items0 + (kPhases > 1 ? n_chunks * p.ph[1].m_tiles : 0);
   auto fail = [&](int code) {
     set_status(p.status, code);
     *abort_flag = 1;
@@ -198,20 +250,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
-      FillCursor pf;  // lookahead: weight tiles prefetched into L2 MOE_TC_PF_W fills ahead
-      pf.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
-      auto pf_step = [&]() {
-        if (pf.valid() && (pf.ks % MOE_TC_PF_EVERY) == 0) {
-          const int prow = pf.ch.x * p.R + pf.mt * p.m_stride;
-          ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow);
-          ptx::tma_prefetch_2d(&p.map_w, pf.ks * kBlockK, prow + p.half);
+      Cursor c;
+      c.start(p, blockIdx.x, gridDim.x, items0, items_all);
+      for (uint32_t fill = 0; c.valid(); ++fill, c.next()) {
+        const TcPhase& ph = p.ph[c.phase];
+        if (c.ks == 0 && dep_phase(c.phase)) {  // h of this chunk must be published by GEMM1
+          if (!wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag)) {
+            fail(kStatusTimeout);
+            break;
+          }
+          fence_proxy_async_global();
         }
-        pf.next(p.chunks);
-      };
-      for (int i = 0; i < MOE_TC_PF_W; ++i) pf_step();
-      FillCursor c;
-      c.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
-      for (uint32_t fill = 0; c.valid(); ++fill, c.next(p.chunks)) {
         const int s = (int)(fill % C::kStages);
         const uint32_t use = fill / C::kStages;
         if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
@@ -219,56 +268,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           break;
         }
         const int nrows = (c.ch.z + 15) & ~15;
-        const int row0 = c.ch.x * p.R + c.mt * p.m_stride;
+        const int row0 = c.ch.x * ph.R + c.mt * ph.m_stride;
         const uint32_t tx = C::kA * C::kTxA + (uint32_t)nrows * 128;
         uint8_t* st = smem + s * C::kStageBytes;
         ptx::mbar_arrive_expect_tx(&full[s], tx);
-        ptx::tma_load_2d(st, &p.map_w, &full[s], c.ks * kBlockK, row0, pol_w);
-        ptx::tma_load_2d(st + C::kATile, &p.map_w, &full[s], c.ks * kBlockK, row0 + p.half, pol_w);
+        ptx::tma_load_2d(st, &ph.map_w, &full[s], c.ks * kBlockK, row0, pol_w);
+        ptx::tma_load_2d(st + C::kATile, &ph.map_w, &full[s], c.ks * kBlockK, row0 + ph.half,
+                         pol_w);
         for (int r = 0; r < nrows; r += kBoxRowsB)
-          ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &p.map_x, &full[s], c.ks * kBlockK,
+          ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &ph.map_x, &full[s], c.ks * kBlockK,
                            c.ch.y + r, pol_x);
-        if (MOE_TC_PF_W > 0) pf_step();
-        if (MOE_TC_PF_LSU > 0) *prod_fill = fill + 1;
-      }
-    }
-  } else if (warp == 1 && MOE_TC_PF_LSU > 0) {
-    // ------------------------------------------------------------ L2 prefetcher
-    // Keeps the weight rows of the fills MOE_TC_PF_LSU ahead of the TMA
-    // producer in L2; one 128-byte line per row covers two k-stages.
-    FillCursor pf;
-    pf.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
-    const uint8_t* wbase = reinterpret_cast<const uint8_t*>(p.w_packed);
-    const int64_t row_bytes = p.K / 2;
-    uint32_t pfill = 0;
-    uint64_t idle_since = ptx::globaltimer();
-    while (pf.valid() && !*abort_flag) {
-      if (pfill < *prod_fill + MOE_TC_PF_LSU) {
-        if ((pf.ks & 1) == 0) {
-          const int64_t row0 = (int64_t)pf.ch.x * p.R + pf.mt * p.m_stride;
-#pragma unroll
-          for (int a = 0; a < 2; ++a)
-#pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-              const int64_t row = row0 + a * p.half + qq * 32 + lane;
-              if (row < p.rows_total) ptx::prefetch_l2(wbase + row * row_bytes + pf.ks * 64);
-            }
-        }
-        ++pfill;
-        pf.next(p.chunks);
-        idle_since = ptx::globaltimer();
-      } else if (ptx::globaltimer() - idle_since > p.timeout_ns) {
-        break;  // the producer stopped advancing; nothing to report, just stop prefetching
       }
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // A plain item loop: only N and the k-step count are needed here, and
+      // the issuer's loop overhead is on the critical path of every stage.
       uint32_t fill = 0;
       bool ok = true;
       int j = 0;
-      for (int item = blockIdx.x; ok && item < n_items; item += gridDim.x, ++j) {
-        const int4 ch = p.chunks[item / p.m_tiles];
+      for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x, ++j) {
+        const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
+        const int local = item - (phase ? items0 : 0);
+        const int4 ch = p.chunks[local / p.ph[phase].m_tiles];
+        const int ksteps = p.ph[phase].K / kBlockK;
         const uint32_t N = (uint32_t)((ch.z + 15) & ~15);
         const int b = j % C::kAccBufs;
         const uint32_t u = (uint32_t)(j / C::kAccBufs);
@@ -313,81 +337,138 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ scale stagers
     // Scale words are loaded a group of kSfGroup fills at a time, one group
-    // ahead of the group being written into TMEM.  When the scale rows allow it
-    // (K a multiple of 512), one 16-byte load per row covers the whole group,
-    // which keeps the scale traffic to a quarter of the L2 requests.
+    // ahead of the group being written into TMEM.  When every phase's scale
+    // rows allow it (K a multiple of 512), one 16-byte load per row covers a
+    // group (a quarter of the L2 requests of per-stage loads) and a group never
+    // straddles two work items.  Scales of a chunk whose h is not yet
+    // published are never loaded ahead: the group is loaded at store time,
+    // after the (bounded) wait, so a stager never blocks ahead of fills it
+    // still has to stage.
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    const bool vec = (sf_row % 16) == 0 && (ksteps % kSfGroup) == 0;
-    FillCursor ld, stc;
-    ld.start(blockIdx.x, n_items, ksteps, p.m_tiles, gridDim.x, p.chunks);
+    bool vec = true;
+    for (int ph = 0; ph < kPhases; ++ph) vec = vec && (p.ph[ph].K % (32 * 16)) == 0;
+    Cursor ld, stc;
+    ld.start(p, blockIdx.x, gridDim.x, items0, items_all);
     stc = ld;
-    // words of one fill for this lane: A scales of rows 32q+lane (+ second
-    // tile), then B scales of tokens 32j+lane; absent words are 0
     uint32_t grp[2][kSfGroup][C::kWords];
-    auto load_group = [&](uint32_t (&g)[kSfGroup][C::kWords]) {
+    bool deferred[2] = {false, false};
+    Cursor grp_at[2];
+    auto words_of_fill = [&](uint32_t (&w)[C::kWords], const Cursor& c) {
+      const TcPhase& ph = p.ph[c.phase];
+      const int sf_row = ph.K / 32;
+      const int64_t row = (int64_t)c.ch.x * ph.R + c.mt * ph.m_stride + q * 32 + lane;
+#pragma unroll
+      for (int a = 0; a < C::kA; ++a)
+        if (row + a * ph.half < ph.rows_total)
+          w[a] = __ldg(reinterpret_cast<const uint32_t*>(ph.w_sf + (row + a * ph.half) * sf_row +
+                                                         c.ks * 4));
+#pragma unroll
+      for (int jb = 0; jb < kNMax / 32; ++jb) {
+        const int n = jb * 32 + lane;
+        if (n < c.ch.z) {
+          const unsigned int* src = reinterpret_cast<const unsigned int*>(
+              ph.x_sf + (int64_t)(c.ch.y + n) * sf_row + c.ks * 4);
+          // h scales written earlier in this launch need a coherent load
+          w[C::kA + jb] = dep_phase(c.phase) ? __ldcg(src) : __ldg(src);
+        }
+      }
+    };
+    auto words_of_group = [&](uint32_t (&g)[kSfGroup][C::kWords], const Cursor& c0) {
+      // the group's fills are ks .. ks+3 of one work item (vector path)
+      const TcPhase& ph = p.ph[c0.phase];
+      const int sf_row = ph.K / 32;
+      const int64_t row = (int64_t)c0.ch.x * ph.R + c0.mt * ph.m_stride + q * 32 + lane;
+#pragma unroll
+      for (int a = 0; a < C::kA; ++a) {
+        if (row + a * ph.half < ph.rows_total) {
+          const uint4 v = __ldg(
+              reinterpret_cast<const uint4*>(ph.w_sf + (row + a * ph.half) * sf_row + c0.ks * 4));
+          g[0][a] = v.x;
+          g[1][a] = v.y;
+          g[2][a] = v.z;
+          g[3][a] = v.w;
+        }
+      }
+#pragma unroll
+      for (int jb = 0; jb < kNMax / 32; ++jb) {
+        const int n = jb * 32 + lane;
+        if (n < c0.ch.z) {
+          const uint4* src = reinterpret_cast<const uint4*>(
+              ph.x_sf + (int64_t)(c0.ch.y + n) * sf_row + c0.ks * 4);
+          const uint4 v = dep_phase(c0.phase) ? __ldcg(src) : __ldg(src);
+          g[0][C::kA + jb] = v.x;
+          g[1][C::kA + jb] = v.y;
+          g[2][C::kA + jb] = v.z;
+          g[3][C::kA + jb] = v.w;
+        }
+      }
+    };
+    // does any fill of the group starting at c0 belong to an unpublished chunk?
+    auto group_blocked = [&](const Cursor& c0) {
+      Cursor c = c0;
+      for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next()) {
+        const TcPhase& ph = p.ph[c.phase];
+        if (dep_phase(c.phase) && ld_acquire(p.gemm1_done + c.chunk) < ph.dep_target) return true;
+      }
+      return false;
+    };
+    auto load_group = [&](int gi, uint32_t (&g)[kSfGroup][C::kWords]) {
 #pragma unroll
       for (int i = 0; i < kSfGroup; ++i)
 #pragma unroll
         for (int w = 0; w < C::kWords; ++w) g[i][w] = 0;
-      if (vec) {  // the group's fills are ks .. ks+3 of one work item
-        if (ld.valid()) {
-          const int64_t row = (int64_t)ld.ch.x * p.R + ld.mt * p.m_stride + q * 32 + lane;
+      grp_at[gi] = ld;
+      if (kMode == kModeBoth) deferred[gi] = __any_sync(0xffffffffu, group_blocked(ld));
+      if (!deferred[gi]) {
+        if (vec) {
+          if (ld.valid()) words_of_group(g, ld);
+        } else {
+          Cursor c = ld;
 #pragma unroll
-          for (int a = 0; a < C::kA; ++a) {
-            if (row + a * p.half < p.rows_total) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                  p.w_sf + (row + a * p.half) * sf_row + ld.ks * 4));
-              g[0][a] = v.x;
-              g[1][a] = v.y;
-              g[2][a] = v.z;
-              g[3][a] = v.w;
-            }
+          for (int i = 0; i < kSfGroup; ++i) {
+            if (c.valid()) words_of_fill(g[i], c);
+            c.next();
           }
-#pragma unroll
-          for (int jb = 0; jb < kNMax / 32; ++jb) {
-            const int n = jb * 32 + lane;
-            if (n < ld.ch.z) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(
-                  p.x_sf + (int64_t)(ld.ch.y + n) * sf_row + ld.ks * 4));
-              g[0][C::kA + jb] = v.x;
-              g[1][C::kA + jb] = v.y;
-              g[2][C::kA + jb] = v.z;
-              g[3][C::kA + jb] = v.w;
-            }
-          }
-        }
-#pragma unroll
-        for (int i = 0; i < kSfGroup; ++i) ld.next(p.chunks);
-      } else {
-#pragma unroll
-        for (int i = 0; i < kSfGroup; ++i) {
-          if (ld.valid()) {
-            const int64_t row = (int64_t)ld.ch.x * p.R + ld.mt * p.m_stride + q * 32 + lane;
-#pragma unroll
-            for (int a = 0; a < C::kA; ++a)
-              if (row + a * p.half < p.rows_total)
-                g[i][a] = __ldg(reinterpret_cast<const uint32_t*>(
-                    p.w_sf + (row + a * p.half) * sf_row + ld.ks * 4));
-#pragma unroll
-            for (int jb = 0; jb < kNMax / 32; ++jb) {
-              const int n = jb * 32 + lane;
-              if (n < ld.ch.z)
-                g[i][C::kA + jb] = __ldg(reinterpret_cast<const uint32_t*>(
-                    p.x_sf + (int64_t)(ld.ch.y + n) * sf_row + ld.ks * 4));
-            }
-          }
-          ld.next(p.chunks);
         }
       }
+#pragma unroll
+      for (int i = 0; i < kSfGroup; ++i) ld.next();
     };
-    load_group(grp[0]);
-    load_group(grp[1]);
+    // complete a deferred group: wait for its chunks (bounded), then load it
+    auto finish_group = [&](int gi, uint32_t (&g)[kSfGroup][C::kWords]) {
+      Cursor c = grp_at[gi];
+      for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next()) {
+        const TcPhase& ph = p.ph[c.phase];
+        if (dep_phase(c.phase) &&
+            !wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag))
+          return false;
+      }
+      if (vec) {
+        if (grp_at[gi].valid()) words_of_group(g, grp_at[gi]);
+      } else {
+        c = grp_at[gi];
+#pragma unroll
+        for (int i = 0; i < kSfGroup; ++i) {
+          if (c.valid()) words_of_fill(g[i], c);
+          c.next();
+        }
+      }
+      deferred[gi] = false;
+      return true;
+    };
+    load_group(0, grp[0]);
+    load_group(1, grp[1]);
     bool ok = true;
     uint32_t fill = 0;
     while (ok && stc.valid()) {
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
+        if (kMode == kModeBoth && ok && stc.valid() && deferred[gi] &&
+            !finish_group(gi, grp[gi])) {
+          if (lane == 0) fail(kStatusTimeout);
+          ok = false;
+        }
 #pragma unroll
         for (int i = 0; i < kSfGroup; ++i) {
           if (ok && stc.valid()) {
@@ -409,21 +490,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
               __syncwarp();
               if (lane == 0) ptx::mbar_arrive(&full[s]);
               ++fill;
-              stc.next(p.chunks);
+              stc.next();
             }
           }
         }
-        if (ok && stc.valid()) load_group(grp[gi]);  // the group two ahead
+        if (ok && stc.valid()) load_group(gi, grp[gi]);  // the group two ahead
       }
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-    int j = 0;
-    for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++j) {
-      const int4 ch = p.chunks[item / p.m_tiles];
-      const int mt = item % p.m_tiles;
+    Cursor c;
+    c.start(p, blockIdx.x, gridDim.x, items0, items_all);
+    for (int j = 0; c.valid(); ++j) {
+      const TcPhase& ph = p.ph[c.phase];
+      const int4 ch = c.ch;
+      const int mt = c.mt, chunk = c.chunk;
       const int b = j % C::kAccBufs;
       const uint32_t u = (uint32_t)(j / C::kAccBufs);
       if (!ptx::mbar_wait(&acc_full[b], u & 1, deadline(), abort_flag)) {
@@ -432,7 +515,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
       ptx::tc_fence_after();
       const uint32_t acc0 = tbase + lane_off + b * C::kAccCols;
-      const int row = mt * p.m_stride + q * 32 + lane;  // output row within the expert
+      const int row = mt * ph.m_stride + q * 32 + lane;  // output row within the expert
       for (int n0 = 0; n0 < ch.z; n0 += 8) {
         uint32_t v0[8], v1[8];
         ptx::tmem_ld_x8(acc0 + n0, v0);
@@ -442,15 +525,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         for (int t = 0; t < 8; ++t) {
           if (n0 + t < ch.z) {  // warp-uniform
             const int64_t slot = ch.y + n0 + t;
-            if (kGated) {
+            if (gated_phase(c.phase)) {
               const float g = __uint_as_float(v0[t]), up = __uint_as_float(v1[t]);
               const float h = g / (1.0f + expf(-g)) * up;
               const int code = block_scale_code(warp_max(fabsf(h)), 8);
-              p.hq[slot * p.out_dim + row] = e4m3_encode_satfinite(h * exp2_exact(127 - code));
-              if (lane == 0) p.hs[slot * (p.out_dim / 32) + row / 32] = (uint8_t)code;
+              p.hq[slot * ph.out_dim + row] = e4m3_encode_satfinite(h * exp2_exact(127 - code));
+              if (lane == 0) p.hs[slot * (ph.out_dim / 32) + row / 32] = (uint8_t)code;
             } else {
-              p.yp[slot * p.out_dim + row] = __uint_as_float(v0[t]);
-              if (row + 128 < p.out_dim) p.yp[slot * p.out_dim + row + 128] = __uint_as_float(v1[t]);
+              p.yp[slot * ph.out_dim + row] = __uint_as_float(v0[t]);
+              if (row + 128 < ph.out_dim)
+                p.yp[slot * ph.out_dim + row + 128] = __uint_as_float(v1[t]);
             }
           }
         }
@@ -458,6 +542,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);
+      if (kMode == kModeBoth && gated_phase(c.phase)) {
+        // publish this warp's quarter of h: its generic stores made visible to
+        // other CTAs' TMA reads (async proxy) and loads, then one release
+        // increment per warp (four per tile pair)
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_add(p.gemm1_done + chunk, 1);
+      }
+      c.next_item();
     }
   }
 

@@ -59,6 +59,28 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+template <int kN>
+bool set_gemm_smem() {
+  const int bytes = (int)TcCfg<kN>::kSmem;
+  return cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeGemm1>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeGemm2>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeBoth>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+template <int kN>
+void launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm) {
+  const size_t smem = TcCfg<kN>::kSmem;
+  if (mode == kModeGemm1)
+    gemm_tc_kernel<kN, kModeGemm1><<<grid, kTcThreads, smem, stream>>>(prm);
+  else if (mode == kModeGemm2)
+    gemm_tc_kernel<kN, kModeGemm2><<<grid, kTcThreads, smem, stream>>>(prm);
+  else
+    gemm_tc_kernel<kN, kModeBoth><<<grid, kTcThreads, smem, stream>>>(prm);
+}
+
 // current device; checks compute capability 10.3 and caches per-device data
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -79,18 +101,7 @@ int device_state(DeviceState** out) {
     const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
     if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              permute_smem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<true, kChunkNarrow>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<true, kChunkNarrow>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<false, kChunkNarrow>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<false, kChunkNarrow>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<true, kChunkWide>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<true, kChunkWide>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_tc_kernel<false, kChunkWide>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)TcCfg<false, kChunkWide>::kSmem) != cudaSuccess)
+        !set_gemm_smem<kChunkNarrow>() || !set_gemm_smem<kChunkWide>())
       return MOE_ERR_CUDA;
     d.ready = true;
   }
@@ -131,7 +142,7 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
 }
 
 struct Layout {
-  size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, meta, xq, xs, hq, hs, yp, total;
+  size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, done, meta, xq, xs, hq, hs, yp, total;
   int max_chunks;
 };
 
@@ -153,6 +164,7 @@ Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act
   L.perm = take(TK * 4);
   L.pos = take(TK * 4);
   L.chunks = take((size_t)L.max_chunks * 16);
+  L.done = take((size_t)L.max_chunks * 4);
   L.meta = take(64 * 4);
   L.xq = take(TK * H * act_bytes);
   L.xs = take(TK * (H / 32));
@@ -173,6 +185,7 @@ Work carve(void* base, const Layout& L) {
   w.perm = reinterpret_cast<int32_t*>(b + L.perm);
   w.pos = reinterpret_cast<int32_t*>(b + L.pos);
   w.chunks = reinterpret_cast<int4*>(b + L.chunks);
+  w.done = reinterpret_cast<int32_t*>(b + L.done);
   w.meta = reinterpret_cast<int32_t*>(b + L.meta);
   w.xq = b + L.xq;
   w.xs = b + L.xs;
@@ -231,10 +244,23 @@ int enqueue_route(const float* logits, int T, int E, int k, int chunk_max, const
   st.mark();
   const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
   route_permute_kernel<<<1, 1024, smem, s>>>(w.topk_idx, T, k, E, w.cnt, w.off, w.perm, w.pos,
-                                             w.chunks, w.max_chunks, chunk_max, w.meta,
+                                             w.chunks, w.max_chunks, chunk_max, w.meta, w.done,
                                              d->status);
   st.launched();
   return launch_status();
+}
+
+// The path MOE_PATH_AUTO takes.  One launch removes the gap and the tail
+// between the two GEMMs, which matters when each SM gets only a few work
+// items; with many items per SM the two specialised launches stream weights
+// faster.  The bound on work items uses at most min(T*k, E) touched experts.
+int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
+  if (act != MOE_ACT_MXFP8) return MOE_PATH_MULTI;  // the bf16 GEMMs are two launches
+  const int64_t TK = (int64_t)T * k;
+  const bool wide = T >= kWideMinTokens;
+  const int64_t chunk_bound = std::min<int64_t>(TK, E) + TK / (wide ? kChunkWide : kChunkNarrow);
+  const int64_t item_bound = chunk_bound * (I / 128 + (H + 255) / 256);
+  return item_bound <= (int64_t)kPersistentItemsPerSm * sms ? MOE_PATH_PERSISTENT : MOE_PATH_MULTI;
 }
 
 int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
@@ -284,63 +310,66 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   if (act == MOE_ACT_MXFP8) {
     const unsigned long long timeout_ns =
         (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
-    TcParams p1{};
-    if ((rc = make_map(&p1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
+    TcPhase g1{}, g2{};
+    if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
                        H / 2, 128, 128)) ||
-        (rc = make_map(&p1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)))
-      return rc;
-    p1.w_packed = w13;
-    p1.w_sf = w13s;
-    p1.x_sf = w.xs;
-    p1.chunks = w.chunks;
-    p1.meta = w.meta;
-    p1.hq = w.hq;
-    p1.hs = w.hs;
-    p1.K = H;
-    p1.R = 2 * I;
-    p1.m_tiles = I / 128;
-    p1.m_stride = 128;
-    p1.half = I;
-    p1.out_dim = I;
-    p1.rows_total = E * 2 * I;
-    p1.status = d->status;
-    p1.timeout_ns = timeout_ns;
-    TcParams p2{};
-    if ((rc = make_map(&p2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
+        (rc = make_map(&g1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)) ||
+        (rc = make_map(&g2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
                        I / 2, 128, 128)) ||
-        (rc = make_map(&p2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
+        (rc = make_map(&g2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
       return rc;
-    p2.w_packed = w2;
-    p2.w_sf = w2s;
-    p2.x_sf = w.hs;
-    p2.chunks = w.chunks;
-    p2.meta = w.meta;
-    p2.yp = w.yp;
-    p2.K = I;
-    p2.R = H;
-    p2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
-    p2.m_stride = 256;
-    p2.half = 128;
-    p2.out_dim = H;
-    p2.rows_total = E * H;
-    p2.status = d->status;
-    p2.timeout_ns = timeout_ns;
-    st.mark();
-    if (wide)
-      gemm_tc_kernel<true, kChunkWide>
-          <<<d->sms, kTcThreads, TcCfg<true, kChunkWide>::kSmem, stream>>>(p1);
-    else
-      gemm_tc_kernel<true, kChunkNarrow>
-          <<<d->sms, kTcThreads, TcCfg<true, kChunkNarrow>::kSmem, stream>>>(p1);
-    st.launched();
-    st.mark();
-    if (wide)
-      gemm_tc_kernel<false, kChunkWide>
-          <<<d->sms, kTcThreads, TcCfg<false, kChunkWide>::kSmem, stream>>>(p2);
-    else
-      gemm_tc_kernel<false, kChunkNarrow>
-          <<<d->sms, kTcThreads, TcCfg<false, kChunkNarrow>::kSmem, stream>>>(p2);
-    st.launched();
+    g1.w_sf = w13s;
+    g1.x_sf = w.xs;
+    g1.K = H;
+    g1.R = 2 * I;
+    g1.m_tiles = I / 128;
+    g1.m_stride = 128;
+    g1.half = I;
+    g1.out_dim = I;
+    g1.rows_total = E * 2 * I;
+    g2.w_sf = w2s;
+    g2.x_sf = w.hs;
+    g2.K = I;
+    g2.R = H;
+    g2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
+    g2.m_stride = 256;
+    g2.half = 128;
+    g2.out_dim = H;
+    g2.rows_total = E * H;
+    TcParams p{};
+    p.chunks = w.chunks;
+    p.meta = w.meta;
+    p.hq = w.hq;
+    p.hs = w.hs;
+    p.yp = w.yp;
+    p.status = d->status;
+    p.timeout_ns = timeout_ns;
+    auto launch = [&](int mode, const TcParams& prm) {
+      if (wide)
+        launch_gemm<kChunkWide>(mode, d->sms, stream, prm);
+      else
+        launch_gemm<kChunkNarrow>(mode, d->sms, stream, prm);
+      st.launched();
+    };
+    const bool persistent = path == MOE_PATH_PERSISTENT ||
+                            (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) ==
+                                                          MOE_PATH_PERSISTENT);
+    if (!persistent) {
+      p.gemm1_done = nullptr;
+      p.ph[0] = g1;
+      st.mark();
+      launch(kModeGemm1, p);
+      p.ph[0] = g2;
+      st.mark();
+      launch(kModeGemm2, p);
+    } else {  // persistent: both GEMMs in one launch
+      g2.dep_target = 4 * g1.m_tiles;  // four epilogue warps publish per tile pair
+      p.gemm1_done = w.done;
+      p.ph[0] = g1;
+      p.ph[1] = g2;
+      st.mark();
+      launch(kModeBoth, p);
+    }
   } else {
     const int ggrid = d->sms * 4;
     st.mark();
@@ -386,6 +415,15 @@ size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode)
   if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
   return layout_for(T, H, I, E, k, act_mode).total;
+}
+
+int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode) {
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  return auto_path(T, H, I, E, k, act_mode, d->sms);
 }
 
 int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4, uint8_t* out_e8m0,

@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
     const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ cnt_out,
     int32_t* __restrict__ off_out, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
     int4* __restrict__ chunks, int max_chunks, int chunk_max, int32_t* __restrict__ meta,
-    int* status) {
+    int32_t* __restrict__ done, int* status) {
   extern __shared__ int smem[];
   int* s_cnt = smem;          // E
   int* s_off = s_cnt + E;     // E + 1
@@ -121,6 +121,8 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
     s_cnt[e] = 0;
     s_run[e] = 0;
   }
+  if (done)
+    for (int i = tid; i < max_chunks; i += 1024) done[i] = 0;  // per-call completion counters
   __syncthreads();
   for (int f = tid; f < TK; f += 1024) {
     int e = idx[f];

@@ -98,3 +98,10 @@ def test_forward_ex_rejects_small_workspace(moe):
     rc = moe.lib().moe_mxfp4_forward_ex(256, 512, 1024, 2048, 4096, 8192, 4, 256, 128, 8, 2,
                                         16384, None, ctypes.byref(o))
     assert rc == -1
+
+
+def test_select_path_validates_on_host(moe):
+    L = moe.lib()
+    assert L.moe_mxfp4_select_path(16, 250, 128, 8, 2, 0) == -2     # H % 128
+    assert L.moe_mxfp4_select_path(16, 256, 128, 8, 9, 0) == -1     # k > E
+    assert L.moe_mxfp4_select_path(16, 256, 128, 8, 2, 5) == -1     # bad act mode

@@ -123,11 +123,15 @@ def test_route_ties_and_shapes(O, T, E, k):
 
 # ------------------------------------------------------------------ the layer
 
+PATHS = [moe.MOE_PATH_MULTI, moe.MOE_PATH_PERSISTENT]
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", SMALL)
-def test_forward_mxfp8_small(O, name):
+def test_forward_mxfp8_small(O, name, path):
     L = LY.LAYERS[name]
     inp = device_layer(L)
-    y = bf16_to_f64(host_bf16(gpu_forward(L, inp)))
+    y = bf16_to_f64(host_bf16(gpu_forward(L, inp, path=path)))
     w = _oracle_layer(O, L)
     _, yref, _ = O.moe_forward(LY.host_x(L), LY.host_logits(L), *w, L.k, O.ACT_MXFP8)
     _, yex, _ = O.moe_forward(LY.host_x(L), LY.host_logits(L), *w, L.k, O.ACT_EXACT)
@@ -194,13 +198,15 @@ def _layer_inputs(O, T, H, I, E, k, seed, logits=None):
                                             (33, 512, 128, 16, 16, False),
                                             (600, 256, 128, 4, 2, False),
                                             (520, 128, 256, 3, 1, True)])
-@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
-def test_forward_edge_shapes(O, T, H, I, E, k, ties, act):
+@pytest.mark.parametrize("act,path", [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI),
+                                      (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
+                                      (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)])
+def test_forward_edge_shapes(O, T, H, I, E, k, ties, act, path):
     lg = np.zeros((T, E), np.float32) if ties else None   # ties: all tokens on experts 0..k-1
     L, x, lg, w = _layer_inputs(O, T, H, I, E, k, T + H, lg)
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     moe.moe_mxfp4_forward_ex(dev(x), dev(lg), *(dev(a) for a in w), T, H, I, E, k, y,
-                             act_mode=act)
+                             act_mode=act, path=path)
     assert moe.moe_mxfp4_get_status() == 0
     yg = bf16_to_f64(host_bf16(y))
     if act == moe.MOE_ACT_MXFP8:
@@ -209,6 +215,28 @@ def test_forward_edge_shapes(O, T, H, I, E, k, ties, act):
     else:
         _, yref, _ = O.moe_forward(x, lg, *w, k, O.ACT_EXACT)
         assert rel_fro(yg, yref) <= BF16_FRO
+
+
+@pytest.mark.parametrize("name", SMALL + FULL)
+def test_persistent_equals_multi_kernel_bitwise(name):
+    """Both execution paths run the same arithmetic in the same order."""
+    L = LY.LAYERS[name]
+    inp = device_layer(L)
+    ym = gpu_forward(L, inp, path=moe.MOE_PATH_MULTI)
+    yp = gpu_forward(L, inp, path=moe.MOE_PATH_PERSISTENT)
+    assert torch.equal(ym.view(torch.int16), yp.view(torch.int16))
+    del inp
+    torch.cuda.empty_cache()
+
+
+def test_auto_path_choice():
+    """One launch for layers with few GEMM work items per SM, two for large ones."""
+    sel = moe.moe_mxfp4_select_path
+    assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT      # 8 tokens, mid shape
+    assert sel(64, 6144, 2048, 32, 8) == moe.MOE_PATH_PERSISTENT     # 32 experts, 64 tokens
+    assert sel(256, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # full shape, 256 tokens
+    assert sel(1024, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI
+    assert sel(8, 2048, 1024, 64, 8, moe.MOE_ACT_BF16) == moe.MOE_PATH_MULTI
 
 
 def test_zero_weights_give_zero(O):

@@ -26,7 +26,7 @@ constexpr int kWideMinTokens = MOE_WIDE_MIN_TOKENS;
 // automatic path choice: one persistent launch for both GEMMs when the bound
 // on GEMM work items is at most this many per SM
 #ifndef MOE_PERSISTENT_ITEMS_PER_SM
-#define MOE_PERSISTENT_ITEMS_PER_SM 24
+#define MOE_PERSISTENT_ITEMS_PER_SM 8
 #endif
 constexpr int kPersistentItemsPerSm = MOE_PERSISTENT_ITEMS_PER_SM;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;

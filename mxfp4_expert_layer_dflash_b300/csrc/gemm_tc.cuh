@@ -282,58 +282,61 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      // A plain item loop: only N and the k-step count are needed here, and
-      // the issuer's loop overhead is on the critical path of every stage.
-      uint32_t fill = 0;
-      bool ok = true;
-      int j = 0;
-      for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x, ++j) {
-        const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
-        const int local = item - (phase ? items0 : 0);
-        const int4 ch = p.chunks[local / p.ph[phase].m_tiles];
-        const int ksteps = p.ph[phase].K / kBlockK;
-        const uint32_t N = (uint32_t)((ch.z + 15) & ~15);
-        const int b = j % C::kAccBufs;
-        const uint32_t u = (uint32_t)(j / C::kAccBufs);
-        if (!ptx::mbar_wait(&acc_empty[b], (u & 1) ^ 1, deadline(), abort_flag)) {
-          fail(kStatusTimeout);
+    // The whole warp runs the loop on warp-uniform values and one elected lane
+    // issues each tcgen05 instruction; wait outcomes are made warp-uniform.
+    // A plain item loop: only N and the k-step count are needed here, and the
+    // issuer's loop overhead is on the critical path of every stage.
+    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
+    };
+    uint32_t fill = 0;
+    bool ok = true;
+    int j = 0;
+    for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x, ++j) {
+      const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
+      const int local = item - (phase ? items0 : 0);
+      const int4 ch = p.chunks[local / p.ph[phase].m_tiles];
+      const int ksteps = p.ph[phase].K / kBlockK;
+      const uint32_t N = (uint32_t)((ch.z + 15) & ~15);
+      const int b = j % C::kAccBufs;
+      const uint32_t u = (uint32_t)(j / C::kAccBufs);
+      if (!wait_all(&acc_empty[b], (u & 1) ^ 1)) {
+        if (lane == 0) fail(kStatusTimeout);
+        break;
+      }
+      ptx::tc_fence_after();
+      const uint32_t acc0 = tbase + b * C::kAccCols;
+      const uint32_t acc1 = acc0 + kNMax;
+      for (int ks = 0; ks < ksteps; ++ks, ++fill) {
+        const int s = (int)(fill % C::kStages);
+        const uint32_t use = fill / C::kStages;
+        if (!wait_all(&full[s], use & 1)) {
+          if (lane == 0) fail(kStatusTimeout);
+          ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t acc0 = tbase + b * C::kAccCols;
-        const uint32_t acc1 = acc0 + kNMax;
-        for (int ks = 0; ks < ksteps; ++ks, ++fill) {
-          const int s = (int)(fill % C::kStages);
-          const uint32_t use = fill / C::kStages;
-          if (!ptx::mbar_wait(&full[s], use & 1, deadline(), abort_flag)) {
-            fail(kStatusTimeout);
-            ok = false;
-            break;
-          }
-          ptx::tc_fence_after();
-          const uint32_t st = ptx::smem_u32(smem + s * C::kStageBytes);
-          const uint32_t sa0 = st, sa1 = st + C::kATile, sb = st + C::kA * C::kATile;
-          const uint32_t tsf = tbase + C::kSfBase + s * C::kSfStride;
+        const uint32_t st = ptx::smem_u32(smem + s * C::kStageBytes);
+        const uint32_t sa0 = st, sa1 = st + C::kATile, sb = st + C::kA * C::kATile;
+        const uint32_t tsf = tbase + C::kSfBase + s * C::kSfStride;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint32_t idesc = ptx::idesc_mxf8f6f4(N, kk, kk);
-            const uint32_t accum = (ks | kk) ? 1u : 0u;
-            ptx::mma_mxf8f6f4(acc0, ptx::desc_kmajor_sw128(sa0 + 32 * kk),
-                              ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf, tsf + C::kSfbCol,
-                              accum);
-            ptx::mma_mxf8f6f4(acc1, ptx::desc_kmajor_sw128(sa1 + 32 * kk),
-                              ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf + 4,
-                              tsf + C::kSfbCol, accum);
-          }
-          ptx::mma_commit(&empty[s]);  // frees the smem stage and its scale columns
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t idesc = ptx::idesc_mxf8f6f4(N, kk, kk);
+          const uint32_t accum = (ks | kk) ? 1u : 0u;
+          ptx::mma_mxf8f6f4_warp(acc0, ptx::desc_kmajor_sw128(sa0 + 32 * kk),
+                                 ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf,
+                                 tsf + C::kSfbCol, accum);
+          ptx::mma_mxf8f6f4_warp(acc1, ptx::desc_kmajor_sw128(sa1 + 32 * kk),
+                                 ptx::desc_kmajor_sw128(sb + 32 * kk), idesc, tsf + 4,
+                                 tsf + C::kSfbCol, accum);
         }
-        if (!ok) break;
-        ptx::mma_commit(&acc_full[b]);
+        ptx::mma_commit_warp(&empty[s]);  // frees the smem stage and its scale columns
       }
-      ptx::mma_commit(drain);
-      if (!ptx::mbar_wait(drain, 0, deadline(), abort_flag)) fail(kStatusTimeout);
+      if (!ok) break;
+      ptx::mma_commit_warp(&acc_full[b]);
     }
+    ptx::mma_commit_warp(drain);
+    if (!wait_all(drain, 0) && lane == 0) fail(kStatusTimeout);
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ scale stagers
     // Scale words are loaded a group of kSfGroup fills at a time, one group

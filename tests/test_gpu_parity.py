@@ -233,7 +233,7 @@ def test_auto_path_choice():
     """One launch for layers with few GEMM work items per SM, two for large ones."""
     sel = moe.moe_mxfp4_select_path
     assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT      # 8 tokens, mid shape
-    assert sel(64, 6144, 2048, 32, 8) == moe.MOE_PATH_PERSISTENT     # 32 experts, 64 tokens
+    assert sel(1, 6144, 2048, 384, 8) == moe.MOE_PATH_PERSISTENT     # one token, full shape
     assert sel(256, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # full shape, 256 tokens
     assert sel(1024, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI
     assert sel(8, 2048, 1024, 64, 8, moe.MOE_ACT_BF16) == moe.MOE_PATH_MULTI

@@ -9,9 +9,11 @@ B300 peak.  One JSON line on stdout (rank 0).
 
 ours       K forward calls through the C ABI with all inputs resident in HBM (the 7.7 GB of
            packed weights exceed L2, so no L2 flush is needed), timed with CUDA events on the
-           launching stream; then K end-to-end calls with host buffers (pinned x and logits
-           copied in, y copied out, inside the timed region); then the CPU oracle on a bounded
-           sample (rank 0, N = 1).
+           launching stream; then the same K calls again with an event before each kernel
+           (the per-kernel split and the dominant kernel's duration for the roofline); then
+           K end-to-end calls with host buffers (pinned x and logits copied in, y copied out,
+           inside the timed region); then µs per layer of every config, hot and with L2
+           flushed (rank 0, N = 1); then the CPU oracle on a bounded sample (rank 0, N = 1).
 reference  the fp64 CPU oracle on the host cores, each step a bounded sample of the workload.
 N > 1      one process per GPU (torchrun); each rank runs an independent replica of the layer
            (the layer needs no exchange on one GPU), value = all ranks' tokens / max time.
@@ -228,6 +230,61 @@ def run_reference(args, L, rank):
 
 # ------------------------------------------------------------------------- our path
 
+CONFIG_LAYERS = [("c0", "tiny"), ("c1", "mid_t8"), ("c2", "full_t8"), ("c3", "full_t256"),
+                 ("c4", "full_t1024_zipf")]
+
+
+def measure_config(L, steps, flush_buf):
+    """µs per layer of one config: hot (back-to-back forwards, L2 warm) and cold (L2
+    flushed before each forward by writing a buffer twice its size; the forward alone is
+    timed with events around it), plus the routing's touched experts."""
+    import torch
+    import mxfp4_expert_layer_dflash_b300 as moe
+    from synth import layers as LY
+    x = torch.from_numpy(LY.host_x(L).view(np.int16)).view(torch.bfloat16).cuda()
+    lg = torch.from_numpy(LY.host_logits(L)).cuda()
+    w = LY.device_packed_weights(L, moe.mxfp4_quantize)
+    y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
+    cnt = torch.empty(L.E, dtype=torch.int32, device="cuda")
+    aux = [torch.empty(n, dtype=dt, device="cuda") for n, dt in
+           ((L.T * L.k, torch.int32), (L.T * L.k, torch.float32), (L.E + 1, torch.int32),
+            (L.T * L.k, torch.int32), (L.T * L.k, torch.int32))]
+    moe.moe_mxfp4_route(lg, L.T, L.E, L.k, aux[0], aux[1], cnt, *aux[2:])
+    touched, _, _, b_layer = layer_bytes(L, cnt.cpu().numpy())
+
+    def fwd():
+        moe.moe_mxfp4_forward(x, lg, *w, L.T, L.H, L.I, L.E, L.k, y)
+    for _ in range(5):
+        fwd()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(steps):
+        fwd()
+    b.record()
+    torch.cuda.synchronize()
+    hot_us = a.elapsed_time(b) / steps * 1e3
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(min(steps, 50))]
+    for e0, e1 in ev:
+        flush_buf.add_(1)
+        e0.record()
+        fwd()
+        e1.record()
+    torch.cuda.synchronize()
+    cold_us = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError(f"device status error in config {L.name}")
+    del w
+    torch.cuda.empty_cache()
+    return {"layer": L.desc, "touched_experts": touched, "alg_bytes": b_layer,
+            "path": {1: "multi", 2: "persistent"}[moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E,
+                                                                             L.k)],
+            "us_hot": hot_us, "us_cold_l2_flushed": cold_us,
+            "tokens_per_s_cold": L.T / (cold_us * 1e-6),
+            "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9}
+
+
 def run_ours(args, L, rank, world, local_rank):
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
@@ -274,12 +331,14 @@ def run_ours(args, L, rank, world, local_rank):
         dist.barrier()
     torch.cuda.synchronize()
 
+    # timed region: plain forward calls (event records between kernels cost about a
+    # microsecond each, so the per-kernel split comes from a second, marked pass)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     launches0 = moe.moe_mxfp4_launch_count()
     with ClockSampler(local_rank) as clk:
         start.record(stream)
         for i in range(args.steps):
-            fwd(marks[i])
+            fwd()
         stop.record(stream)
         torch.cuda.synchronize()
     launches = moe.moe_mxfp4_launch_count() - launches0
@@ -289,6 +348,17 @@ def run_ours(args, L, rank, world, local_rank):
     status = moe.moe_mxfp4_get_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
+
+    # marked pass: the same K forwards with an event before each kernel and after the last
+    m_start, m_stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    m_start.record(stream)
+    for i in range(args.steps):
+        fwd(marks[i])
+    m_stop.record(stream)
+    torch.cuda.synchronize()
+    marked_ms = m_start.elapsed_time(m_stop) / args.steps
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError("device status error in the marked pass")
 
     per_step = {n: [] for n in names}
     for m in marks:
@@ -357,11 +427,30 @@ def run_ours(args, L, rank, world, local_rank):
                            "frac": layer_gbs / hbm, "algorithmic_bytes": b_layer,
                            "us_per_layer": ms * 1e3},
         "step_ms": step_ms,
+        "marked_pass_ms_per_step": marked_ms,
         "gpu_launches": int(launches),
         "e2e": {"value": world * L.T / (e2e_ms * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "clocks": clk.summary(),
     }
+    if world == 1 and not args.no_config_sweep:
+        log("[rank 0] measuring every config (hot and L2-flushed)")
+        flush = torch.empty(2 * 126 * 2**20 // 4, dtype=torch.float32, device="cuda")
+        rep = {}
+        for tag, name in CONFIG_LAYERS:
+            r = measure_config(LY.LAYERS[name], 200 if LY.LAYERS[name].T < 256 else 50, flush)
+            r["hbm_frac_cold"] = r["hbm_gbs_cold"] / hbm
+            Lc = LY.LAYERS[name]
+            flops = 2.0 * Lc.T * Lc.k * 3 * Lc.H * Lc.I
+            r["tflops_cold"] = flops / (r["us_cold_l2_flushed"] * 1e-6) / 1e12
+            # the block-scaled FP4 x FP8 MMA runs at the FP8 rate: 2 x the bf16 peak
+            r["tensor_frac_cold"] = r["tflops_cold"] / (2.0 * float(pk["bf16_tflops"]))
+            rep[tag] = r
+        out["configs_report_peaks"] = {
+            "hbm_gbs": hbm, "fp8_tflops": 2.0 * float(pk["bf16_tflops"]),
+            "source": f"{pk_src}: hbm_gbs; bf16_tflops (burst) x 2, the nominal FP8/bf16 ratio"}
+        del flush
+        out["configs_report"] = rep
     if world == 1 and not args.no_cpu_baseline:
         log("[rank 0] timing the CPU oracle on a bounded sample")
         n_tok = min(args.cpu_tokens, L.T)
@@ -393,6 +482,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-config-sweep", action="store_true",
+                    help="skip the per-config µs/layer report")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -11,9 +11,13 @@ namespace moe {
 
 // Assignments of one expert are processed in chunks of at most this many
 // slots (tokens); a chunk is the N dimension of one GEMM work item.  Narrow
-// chunks keep the GEMM pipeline deep (small activation tiles); wide chunks
-// halve the MMA instructions per token when experts receive many tokens.
-constexpr int kChunkNarrow = 64;
+// chunks keep the GEMM pipeline deep (small activation tiles: six stages in
+// flight); wide chunks cut the MMA instructions per token when experts
+// receive many tokens.
+#ifndef MOE_CHUNK_NARROW
+#define MOE_CHUNK_NARROW 32
+#endif
+constexpr int kChunkNarrow = MOE_CHUNK_NARROW;
 #ifndef MOE_CHUNK_WIDE
 #define MOE_CHUNK_WIDE 96
 #endif

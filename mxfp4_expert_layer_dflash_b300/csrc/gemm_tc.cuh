@@ -246,38 +246,53 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   };
   auto deadline = [&]() { return ptx::globaltimer() + p.timeout_ns; };
 
+  // bounded wait whose outcome is the same in every lane of the warp
+  auto wait_all = [&](uint64_t* bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
-      Cursor c;
-      c.start(p, blockIdx.x, gridDim.x, items0, items_all);
-      for (uint32_t fill = 0; c.valid(); ++fill, c.next()) {
-        const TcPhase& ph = p.ph[c.phase];
-        if (c.ks == 0 && dep_phase(c.phase)) {  // h of this chunk must be published by GEMM1
-          if (!wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag)) {
-            fail(kStatusTimeout);
-            break;
-          }
-          fence_proxy_async_global();
-        }
-        const int s = (int)(fill % C::kStages);
-        const uint32_t use = fill / C::kStages;
-        if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
-          fail(kStatusTimeout);
+    // Like the MMA issuer: a convergent warp walks the fills and one elected
+    // lane issues each copy.
+    const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
+    uint32_t fill = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x) {
+      const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
+      const TcPhase& ph = p.ph[phase];
+      const int local = item - (phase ? items0 : 0);
+      const int chunk = local / ph.m_tiles;
+      const int mt = local - chunk * ph.m_tiles;
+      const int4 ch = p.chunks[chunk];
+      if (dep_phase(phase)) {  // h of this chunk must be published by GEMM1
+        const bool ready = wait_chunk_ready(p, chunk, ph.dep_target, p.timeout_ns, abort_flag);
+        if (!__all_sync(0xffffffffu, ready)) {
+          if (lane == 0) fail(kStatusTimeout);
           break;
         }
-        const int nrows = (c.ch.z + 15) & ~15;
-        const int row0 = c.ch.x * ph.R + c.mt * ph.m_stride;
-        const uint32_t tx = C::kA * C::kTxA + (uint32_t)nrows * 128;
+        fence_proxy_async_global();
+      }
+      const int ksteps = ph.K / kBlockK;
+      const int nrows = (ch.z + 15) & ~15;
+      const int row0 = ch.x * ph.R + mt * ph.m_stride;
+      const uint32_t tx = C::kA * C::kTxA + (uint32_t)nrows * 128;
+      for (int ks = 0; ks < ksteps; ++ks, ++fill) {
+        const int s = (int)(fill % C::kStages);
+        const uint32_t use = fill / C::kStages;
+        if (!wait_all(&empty[s], (use & 1) ^ 1)) {
+          if (lane == 0) fail(kStatusTimeout);
+          ok = false;
+          break;
+        }
         uint8_t* st = smem + s * C::kStageBytes;
-        ptx::mbar_arrive_expect_tx(&full[s], tx);
-        ptx::tma_load_2d(st, &ph.map_w, &full[s], c.ks * kBlockK, row0, pol_w);
-        ptx::tma_load_2d(st + C::kATile, &ph.map_w, &full[s], c.ks * kBlockK, row0 + ph.half,
-                         pol_w);
+        ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
+        ptx::tma_load_2d_warp(st, &ph.map_w, &full[s], ks * kBlockK, row0, pol_w);
+        ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[s], ks * kBlockK, row0 + ph.half,
+                              pol_w);
         for (int r = 0; r < nrows; r += kBoxRowsB)
-          ptx::tma_load_2d(st + C::kA * C::kATile + r * 128, &ph.map_x, &full[s], c.ks * kBlockK,
-                           c.ch.y + r, pol_x);
+          ptx::tma_load_2d_warp(st + C::kA * C::kATile + r * 128, &ph.map_x, &full[s],
+                                ks * kBlockK, ch.y + r, pol_x);
       }
     }
   } else if (warp == 2) {
@@ -286,9 +301,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     // issues each tcgen05 instruction; wait outcomes are made warp-uniform.
     // A plain item loop: only N and the k-step count are needed here, and the
     // issuer's loop overhead is on the critical path of every stage.
-    auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-      return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
-    };
     uint32_t fill = 0;
     bool ok = true;
     int j = 0;

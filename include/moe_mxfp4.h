@@ -124,6 +124,13 @@ typedef struct {
 /* debug_flags: cap every bounded device wait at ~1 ms instead of ~2 s; used
  * to exercise the timeout path without faulting anything */
 #define MOE_DEBUG_SHORT_TIMEOUT 1u
+/* debug_flags: on the single-launch path (MOE_PATH_PERSISTENT, MXFP8 mode),
+ * make GEMM2 wait for a GEMM1 completion count that is never reached, so the
+ * cross-CTA dependency wait runs out (after ~1 ms with MOE_DEBUG_SHORT_TIMEOUT):
+ * the call then reports MOE_ERR_DEVICE_TIMEOUT through moe_mxfp4_get_status and
+ * y is unspecified.  Exercises the device timeout path without any fault;
+ * ignored by the other paths. */
+#define MOE_DEBUG_FORCE_DEP_TIMEOUT 2u
 
 /*
  * moe_mxfp4_forward_ex — moe_mxfp4_forward with options (NULL opts = defaults).

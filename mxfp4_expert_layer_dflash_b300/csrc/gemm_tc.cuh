@@ -246,7 +246,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   };
   auto deadline = [&]() { return ptx::globaltimer() + p.timeout_ns; };
 
-  // bounded wait whose outcome is the same in every lane of the warp
+  // Bounded wait whose outcome is the same in every lane of the warp: lanes can
+  // see a timeout or the abort flag at different moments, and the warp-wide
+  // tcgen05 / shuffle instructions after a wait need the whole warp.
   auto wait_all = [&](uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
   };
@@ -456,7 +458,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next()) {
         const TcPhase& ph = p.ph[c.phase];
         if (dep_phase(c.phase) &&
-            !wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag))
+            !__all_sync(0xffffffffu,
+                        wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag)))
           return false;
       }
       if (vec) {
@@ -489,7 +492,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           if (ok && stc.valid()) {
             const int s = (int)(fill % C::kStages);
             const uint32_t use = fill / C::kStages;
-            if (!ptx::mbar_wait(&empty[s], (use & 1) ^ 1, deadline(), abort_flag)) {
+            if (!wait_all(&empty[s], (use & 1) ^ 1)) {
               if (lane == 0) fail(kStatusTimeout);
               ok = false;
             } else {
@@ -524,7 +527,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const int mt = c.mt, chunk = c.chunk;
       const int b = j % C::kAccBufs;
       const uint32_t u = (uint32_t)(j / C::kAccBufs);
-      if (!ptx::mbar_wait(&acc_full[b], u & 1, deadline(), abort_flag)) {
+      if (!wait_all(&acc_full[b], u & 1)) {
         if (lane == 0) fail(kStatusTimeout);
         break;
       }

@@ -11,6 +11,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -70,15 +71,32 @@ bool set_gemm_smem() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
 }
 
+// Returns the launch's error (cudaSuccess when enqueued).
 template <int kN>
-void launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm) {
+cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm) {
   const size_t smem = TcCfg<kN>::kSmem;
-  if (mode == kModeGemm1)
+  if (mode == kModeGemm1) {
     gemm_tc_kernel<kN, kModeGemm1><<<grid, kTcThreads, smem, stream>>>(prm);
-  else if (mode == kModeGemm2)
+    return cudaGetLastError();
+  }
+  if (mode == kModeGemm2) {
     gemm_tc_kernel<kN, kModeGemm2><<<grid, kTcThreads, smem, stream>>>(prm);
-  else
-    gemm_tc_kernel<kN, kModeBoth><<<grid, kTcThreads, smem, stream>>>(prm);
+    return cudaGetLastError();
+  }
+  // Both GEMMs in one launch: GEMM2 items wait for other CTAs' GEMM1 items, so
+  // every CTA must be resident at once.  A cooperative launch guarantees that,
+  // or fails without running anything.
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
 }
 
 // current device; checks compute capability 10.3 and caches per-device data
@@ -345,30 +363,41 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     p.status = d->status;
     p.timeout_ns = timeout_ns;
     auto launch = [&](int mode, const TcParams& prm) {
-      if (wide)
-        launch_gemm<kChunkWide>(mode, d->sms, stream, prm);
-      else
-        launch_gemm<kChunkNarrow>(mode, d->sms, stream, prm);
-      st.launched();
+      const cudaError_t e = wide ? launch_gemm<kChunkWide>(mode, d->sms, stream, prm)
+                                 : launch_gemm<kChunkNarrow>(mode, d->sms, stream, prm);
+      if (e == cudaSuccess) st.launched();
+      return e;
     };
-    const bool persistent = path == MOE_PATH_PERSISTENT ||
-                            (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) ==
-                                                          MOE_PATH_PERSISTENT);
-    if (!persistent) {
-      p.gemm1_done = nullptr;
-      p.ph[0] = g1;
-      st.mark();
-      launch(kModeGemm1, p);
-      p.ph[0] = g2;
-      st.mark();
-      launch(kModeGemm2, p);
-    } else {  // persistent: both GEMMs in one launch
+    bool persistent = path == MOE_PATH_PERSISTENT ||
+                      (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) ==
+                                                    MOE_PATH_PERSISTENT);
+    if (persistent) {  // both GEMMs in one launch
       g2.dep_target = 4 * g1.m_tiles;  // four epilogue warps publish per tile pair
+      if (opts && (opts->debug_flags & MOE_DEBUG_FORCE_DEP_TIMEOUT))
+        g2.dep_target = INT_MAX;  // never reached: the dependency wait runs out
       p.gemm1_done = w.done;
       p.ph[0] = g1;
       p.ph[1] = g2;
       st.mark();
-      launch(kModeBoth, p);
+      const cudaError_t e = launch(kModeBoth, p);
+      if (e == cudaErrorCooperativeLaunchTooLarge) {
+        // the GPU cannot hold every CTA at once (e.g. a partitioned device):
+        // nothing ran, so take the two-launch path
+        (void)cudaGetLastError();
+        persistent = false;
+      } else if (e != cudaSuccess) {
+        return MOE_ERR_CUDA;
+      }
+    }
+    if (!persistent) {
+      p.gemm1_done = nullptr;
+      p.ph[1] = TcPhase{};
+      p.ph[0] = g1;
+      st.mark();
+      if (launch(kModeGemm1, p) != cudaSuccess) return MOE_ERR_CUDA;
+      p.ph[0] = g2;
+      st.mark();
+      if (launch(kModeGemm2, p) != cudaSuccess) return MOE_ERR_CUDA;
     }
   } else {
     const int ggrid = d->sms * 4;

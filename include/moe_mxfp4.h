@@ -144,12 +144,13 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
 /*
  * moe_mxfp4_select_path — the path MOE_PATH_AUTO takes for this shape on the
  * current device: MOE_PATH_PERSISTENT when a bound on the GEMM work items
- * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is at most 8 per SM,
- * else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  The single
- * launch saves the gap and tail between the GEMMs on layers with few work
- * items per SM; two launches stream weights faster on large ones.  The paths
- * give bitwise equal results.  Returns a negative moe_status on invalid
- * arguments.  No counterpart in the papers: a support call.
+ * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is between 5 and 8 per
+ * SM, else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  The
+ * single launch saves the gap and tail between the GEMMs on layers with a
+ * handful of work items per SM; two launches stream weights faster on large
+ * layers and start sooner on tiny ones.  The paths give bitwise equal
+ * results.  Returns a negative moe_status on invalid arguments.  No
+ * counterpart in the papers: a support call.
  */
 int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode);
 

@@ -13,6 +13,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
                                                       const int32_t* __restrict__ pos,
                                                       const float* __restrict__ gate, int T, int H,
                                                       int k, uint16_t* __restrict__ y) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int64_t per_tok = H / 8;
   const int64_t total = (int64_t)T * per_tok;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;

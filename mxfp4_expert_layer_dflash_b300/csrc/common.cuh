@@ -28,11 +28,17 @@ constexpr int kChunkWide = MOE_CHUNK_WIDE;
 #endif
 constexpr int kWideMinTokens = MOE_WIDE_MIN_TOKENS;
 // automatic path choice: one persistent launch for both GEMMs when the bound
-// on GEMM work items is at most this many per SM
+// on GEMM work items per SM lies in [kPersistentMinItemsPerSm,
+// kPersistentItemsPerSm] (measured window: below it the cooperative launch's
+// fixed cost dominates, above it the single kernel's slower stages do)
 #ifndef MOE_PERSISTENT_ITEMS_PER_SM
 #define MOE_PERSISTENT_ITEMS_PER_SM 8
 #endif
+#ifndef MOE_PERSISTENT_MIN_ITEMS_PER_SM
+#define MOE_PERSISTENT_MIN_ITEMS_PER_SM 5
+#endif
 constexpr int kPersistentItemsPerSm = MOE_PERSISTENT_ITEMS_PER_SM;
+constexpr int kPersistentMinItemsPerSm = MOE_PERSISTENT_MIN_ITEMS_PER_SM;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 
@@ -55,6 +61,22 @@ struct Work {
   float* yp;          // [T*k, H] per-slot expert outputs (fp32)
   int max_chunks;
 };
+
+// Programmatic dependent launch.  The kernels of a forward after the first
+// are launched with the programmatic stream-serialization attribute, so one
+// may start while the previous kernel still runs.  Such a kernel calls
+// grid_dependency_wait() before touching any global memory that an earlier
+// kernel of the call reads or writes: the wait returns once the preceding
+// grid has completed and its writes are visible (at once when the kernel was
+// launched without the attribute).  grid_launch_dependents() lets the next
+// kernel be scheduled before this one ends.
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void set_status(int* status, int code) {
   atomicCAS(status, 0, code);

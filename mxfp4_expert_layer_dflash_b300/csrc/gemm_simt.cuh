@@ -62,6 +62,8 @@ __global__ void __launch_bounds__(128) gemm1_simt_kernel(
     const int32_t* __restrict__ meta, int H, int I, uint8_t* __restrict__ hq,
     uint8_t* __restrict__ hs) {
   __shared__ float hbuf[kSimtRows][kChunkNarrow];  // bf16 mode always uses narrow chunks
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int iblocks = I / kSimtRows;
   const int64_t items = (int64_t)meta[0] * iblocks;
@@ -117,6 +119,8 @@ __global__ void __launch_bounds__(128) gemm2_simt_kernel(
     const uint8_t* __restrict__ w2, const uint8_t* __restrict__ w2s,
     const uint8_t* __restrict__ hq, const uint8_t* __restrict__ hs, const int4* __restrict__ chunks,
     const int32_t* __restrict__ meta, int H, int I, float* __restrict__ yp) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int oblocks = H / kSimtRows;
   const int64_t items = (int64_t)meta[0] * oblocks;

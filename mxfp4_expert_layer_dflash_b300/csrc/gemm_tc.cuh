@@ -174,6 +174,28 @@ __device__ __forceinline__ void red_release_add(int* ptr, int v) {
   asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ int ld_relaxed(const int* ptr) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+__device__ __forceinline__ void st_release_cta(int* ptr, int v) {
+  asm volatile("st.release.cta.shared::cta.b32 [%0], %1;" ::"r"(ptx::smem_u32(ptr)), "r"(v)
+               : "memory");
+}
+
+__device__ __forceinline__ int ld_acquire_cta(const int* ptr) {
+  int v;
+  asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];" : "=r"(v) : "r"(ptx::smem_u32(ptr))
+               : "memory");
+  return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -207,6 +229,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // single-launch path: the last work item whose GEMM1 inputs the producer has
+  // seen published (items of a CTA only increase); the scale stagers read it
+  // instead of polling the global counters themselves
+  int* dep_ready = reinterpret_cast<int*>(tmem_slot + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -220,6 +246,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
+    *dep_ready = -1;
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -236,6 +263,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  // everything above touches only this CTA's shared memory and TMEM; the
+  // routing outputs, activations and (for GEMM2) h come from earlier kernels
+  grid_dependency_wait();
 
   const int n_chunks = p.meta[0];
   const int items0 = n_chunks * p.ph[0].m_tiles;
@@ -267,14 +297,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const int chunk = local / ph.m_tiles;
       const int mt = local - chunk * ph.m_tiles;
       const int4 ch = p.chunks[chunk];
-      if (dep_phase(phase)) {  // h of this chunk must be published by GEMM1
+      // h of this chunk must be published by GEMM1 (unless the look-ahead of
+      // the previous item already saw it complete)
+      if (dep_phase(phase) && ld_acquire_cta(dep_ready) < item) {
         const bool ready = wait_chunk_ready(p, chunk, ph.dep_target, p.timeout_ns, abort_flag);
         if (!__all_sync(0xffffffffu, ready)) {
           if (lane == 0) fail(kStatusTimeout);
           break;
         }
         fence_proxy_async_global();
+        if (lane == 0) st_release_cta(dep_ready, item);
       }
+      // Look-ahead (single-launch path): read the next item's chunk counter now
+      // and look at it a few fills later, so the load's latency hides behind
+      // this item's copies; if the chunk is complete, publish the next item
+      // early so the scale stagers can load its h scales ahead of time.
+      const int nxt = item + (int)gridDim.x;
+      bool look = kPhases > 1 && nxt < items_all && nxt >= items0;
+      int look_cnt = 0;
+      if (look) look_cnt = ld_relaxed(p.gemm1_done + (nxt - items0) / p.ph[1].m_tiles);
       const int ksteps = ph.K / kBlockK;
       const int nrows = (ch.z + 15) & ~15;
       const int row0 = ch.x * ph.R + mt * ph.m_stride;
@@ -295,8 +336,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         for (int r = 0; r < nrows; r += kBoxRowsB)
           ptx::tma_load_2d_warp(st + C::kA * C::kATile + r * 128, &ph.map_x, &full[s],
                                 ks * kBlockK, ch.y + r, pol_x);
+        if (look && ks == min(3, ksteps - 1)) {
+          if (__all_sync(0xffffffffu, look_cnt >= p.ph[1].dep_target)) {
+            fence_acq_rel_gpu();  // the relaxed load plus this fence: an acquire
+            fence_proxy_async_global();
+            if (lane == 0) st_release_cta(dep_ready, nxt);
+          }
+          look = false;
+        }
       }
     }
+    // every copy of this CTA is issued: the next kernel may be scheduled
+    grid_launch_dependents();
   } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     // The whole warp runs the loop on warp-uniform values and one elected lane
@@ -421,14 +472,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         }
       }
     };
-    // does any fill of the group starting at c0 belong to an unpublished chunk?
+    // does any fill of the group starting at c0 belong to an item whose h the
+    // producer has not yet seen published?  (a shared-memory read: the
+    // producer's acquire of the chunk counter, then its release here, orders
+    // GEMM1's stores of h before this warp's loads of h's scales)
     auto group_blocked = [&](const Cursor& c0) {
+      if (vec)  // the group's fills all belong to c0's work item
+        return dep_phase(c0.phase) && ld_acquire_cta(dep_ready) < c0.item;
       Cursor c = c0;
-      for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next()) {
-        const TcPhase& ph = p.ph[c.phase];
-        if (dep_phase(c.phase) && ld_acquire(p.gemm1_done + c.chunk) < ph.dep_target) return true;
-      }
+      for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next())
+        if (dep_phase(c.phase) && ld_acquire_cta(dep_ready) < c.item) return true;
       return false;
+    };
+    // bounded wait until the producer has published `item`
+    auto wait_item_ready = [&](int item) {
+      const uint64_t until = deadline();
+      while (ld_acquire_cta(dep_ready) < item) {
+        if (*abort_flag || ptx::globaltimer() > until) return false;
+      }
+      return true;
     };
     auto load_group = [&](int gi, uint32_t (&g)[kSfGroup][C::kWords]) {
 #pragma unroll
@@ -455,12 +517,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     // complete a deferred group: wait for its chunks (bounded), then load it
     auto finish_group = [&](int gi, uint32_t (&g)[kSfGroup][C::kWords]) {
       Cursor c = grp_at[gi];
-      for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next()) {
-        const TcPhase& ph = p.ph[c.phase];
-        if (dep_phase(c.phase) &&
-            !__all_sync(0xffffffffu,
-                        wait_chunk_ready(p, c.chunk, ph.dep_target, p.timeout_ns, abort_flag)))
-          return false;
+      if (vec) {
+        if (dep_phase(c.phase) && !__all_sync(0xffffffffu, wait_item_ready(c.item))) return false;
+      } else {
+        for (int i = 0; i < kSfGroup && c.valid(); ++i, c.next())
+          if (dep_phase(c.phase) && !__all_sync(0xffffffffu, wait_item_ready(c.item)))
+            return false;
       }
       if (vec) {
         if (grp_at[gi].valid()) words_of_group(g, grp_at[gi]);

@@ -15,6 +15,7 @@
 #include <atomic>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "combine.cuh"
 #include "common.cuh"
@@ -71,30 +72,57 @@ bool set_gemm_smem() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
 }
 
+// Launches `kernel` with programmatic stream serialization: it may be
+// scheduled while the previous kernel in the stream still runs and orders
+// itself with grid_dependency_wait() (every kernel launched this way calls it
+// before touching global memory).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Returns the launch's error (cudaSuccess when enqueued).
 template <int kN>
 cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm) {
   const size_t smem = TcCfg<kN>::kSmem;
-  if (mode == kModeGemm1) {
-    gemm_tc_kernel<kN, kModeGemm1><<<grid, kTcThreads, smem, stream>>>(prm);
-    return cudaGetLastError();
-  }
-  if (mode == kModeGemm2) {
-    gemm_tc_kernel<kN, kModeGemm2><<<grid, kTcThreads, smem, stream>>>(prm);
-    return cudaGetLastError();
-  }
+  if (mode == kModeGemm1)
+    return launch_pdl(gemm_tc_kernel<kN, kModeGemm1>, dim3(grid), dim3(kTcThreads), smem, stream,
+                      prm);
+  if (mode == kModeGemm2)
+    return launch_pdl(gemm_tc_kernel<kN, kModeGemm2>, dim3(grid), dim3(kTcThreads), smem, stream,
+                      prm);
   // Both GEMMs in one launch: GEMM2 items wait for other CTAs' GEMM1 items, so
   // every CTA must be resident at once.  A cooperative launch guarantees that,
-  // or fails without running anything.
+  // or fails without running anything.  It is also programmatic when the
+  // driver accepts both attributes: CTAs that start early block in
+  // grid_dependency_wait() before any cross-CTA wait, and the preceding kernel
+  // never waits on them.
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kTcThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
   attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
+  if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge) return e;
+  (void)cudaGetLastError();  // the combination was refused: cooperative only
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
 }
@@ -261,24 +289,29 @@ int enqueue_route(const float* logits, int T, int E, int k, int chunk_max, const
   st.launched();
   st.mark();
   const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
-  route_permute_kernel<<<1, 1024, smem, s>>>(w.topk_idx, T, k, E, w.cnt, w.off, w.perm, w.pos,
-                                             w.chunks, w.max_chunks, chunk_max, w.meta, w.done,
-                                             d->status);
+  if (launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, s, w.topk_idx, T, k, E, w.cnt,
+                 w.off, w.perm, w.pos, w.chunks, w.max_chunks, chunk_max, w.meta, w.done,
+                 d->status) != cudaSuccess)
+    return MOE_ERR_CUDA;
   st.launched();
   return launch_status();
 }
 
 // The path MOE_PATH_AUTO takes.  One launch removes the gap and the tail
-// between the two GEMMs, which matters when each SM gets only a few work
-// items; with many items per SM the two specialised launches stream weights
-// faster.  The bound on work items uses at most min(T*k, E) touched experts.
+// between the two GEMMs, which pays when each SM gets a handful of work items;
+// with many items per SM the two specialised launches stream weights faster,
+// and with very few the cooperative launch's fixed cost outweighs the gain.
+// The bound on work items uses at most min(T*k, E) touched experts.
 int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
   if (act != MOE_ACT_MXFP8) return MOE_PATH_MULTI;  // the bf16 GEMMs are two launches
   const int64_t TK = (int64_t)T * k;
   const bool wide = T >= kWideMinTokens;
   const int64_t chunk_bound = std::min<int64_t>(TK, E) + TK / (wide ? kChunkWide : kChunkNarrow);
   const int64_t item_bound = chunk_bound * (I / 128 + (H + 255) / 256);
-  return item_bound <= (int64_t)kPersistentItemsPerSm * sms ? MOE_PATH_PERSISTENT : MOE_PATH_MULTI;
+  return item_bound >= (int64_t)kPersistentMinItemsPerSm * sms &&
+                 item_bound <= (int64_t)kPersistentItemsPerSm * sms
+             ? MOE_PATH_PERSISTENT
+             : MOE_PATH_MULTI;
 }
 
 int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
@@ -318,12 +351,15 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   const int cap = d->sms * 8;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   st.mark();
-  if (act == MOE_ACT_MXFP8)
-    mxfp8_rows_kernel<<<grid_for(TK, 8, cap), 256, 0, stream>>>(x, w.perm, TK, H, T, w.xq, w.xs,
-                                                               d->status);
-  else
-    gather_bf16_rows_kernel<<<grid_for(TK, 8, cap), 256, 0, stream>>>(
-        x, w.perm, TK, H, T, reinterpret_cast<uint16_t*>(w.xq), d->status);
+  const cudaError_t qe =
+      act == MOE_ACT_MXFP8
+          ? launch_pdl(mxfp8_rows_kernel, dim3(grid_for(TK, 8, cap)), dim3(256), 0, stream, x,
+                       (const int32_t*)w.perm, (int64_t)TK, (int64_t)H, (int64_t)T, w.xq, w.xs,
+                       d->status)
+          : launch_pdl(gather_bf16_rows_kernel, dim3(grid_for(TK, 8, cap)), dim3(256), 0, stream,
+                       x, (const int32_t*)w.perm, (int64_t)TK, (int64_t)H, (int64_t)T,
+                       reinterpret_cast<uint16_t*>(w.xq), d->status);
+  if (qe != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
   if (act == MOE_ACT_MXFP8) {
     const unsigned long long timeout_ns =
@@ -402,17 +438,23 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   } else {
     const int ggrid = d->sms * 4;
     st.mark();
-    gemm1_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w13, w13s, w.xq, w.xs, w.chunks,
-                                                              w.meta, H, I, w.hq, w.hs);
+    if (launch_pdl(gemm1_simt_kernel<MOE_ACT_BF16>, dim3(ggrid), dim3(128), 0, stream, w13, w13s,
+                   (const uint8_t*)w.xq, (const uint8_t*)w.xs, (const int4*)w.chunks,
+                   (const int32_t*)w.meta, H, I, w.hq, w.hs) != cudaSuccess)
+      return MOE_ERR_CUDA;
     st.launched();
     st.mark();
-    gemm2_simt_kernel<MOE_ACT_BF16><<<ggrid, 128, 0, stream>>>(w2, w2s, w.hq, w.hs, w.chunks,
-                                                              w.meta, H, I, w.yp);
+    if (launch_pdl(gemm2_simt_kernel<MOE_ACT_BF16>, dim3(ggrid), dim3(128), 0, stream, w2, w2s,
+                   (const uint8_t*)w.hq, (const uint8_t*)w.hs, (const int4*)w.chunks,
+                   (const int32_t*)w.meta, H, I, w.yp) != cudaSuccess)
+      return MOE_ERR_CUDA;
     st.launched();
   }
   st.mark();
-  combine_kernel<<<grid_for((int64_t)T * H / 8, 256, cap), 256, 0, stream>>>(
-      w.yp, w.pos, w.topk_w, T, H, k, static_cast<uint16_t*>(y));
+  if (launch_pdl(combine_kernel, dim3(grid_for((int64_t)T * H / 8, 256, cap)), dim3(256), 0,
+                 stream, (const float*)w.yp, (const int32_t*)w.pos, (const float*)w.topk_w, T, H,
+                 k, static_cast<uint16_t*>(y)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   st.launched();
   st.mark();
   return launch_status();

@@ -78,6 +78,8 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t* __restr
                                                          int64_t rows, int64_t K, int64_t src_rows,
                                                          uint8_t* __restrict__ q,
                                                          uint8_t* __restrict__ s, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t nb = K / 32;
@@ -106,6 +108,8 @@ __global__ void __launch_bounds__(256) gather_bf16_rows_kernel(const uint16_t* _
                                                                int64_t src_rows,
                                                                uint16_t* __restrict__ out,
                                                                int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;

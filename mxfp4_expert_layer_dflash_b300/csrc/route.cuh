@@ -20,6 +20,8 @@ template <int MAXPL>
 __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
                                                          int E, int k, int32_t* __restrict__ idx,
                                                          float* __restrict__ w, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
   if (t >= T) return;
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
   int* s_tot = s_warp + 32;   // 2
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int TK = T * k;
+  grid_dependency_wait();
+  grid_launch_dependents();
 
   for (int e = tid; e < E; e += 1024) {
     s_cnt[e] = 0;

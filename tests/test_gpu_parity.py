@@ -230,10 +230,12 @@ def test_persistent_equals_multi_kernel_bitwise(name):
 
 
 def test_auto_path_choice():
-    """One launch for layers with few GEMM work items per SM, two for large ones."""
+    """One launch for layers with a handful of GEMM work items per SM, two otherwise."""
     sel = moe.moe_mxfp4_select_path
     assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT      # 8 tokens, mid shape
-    assert sel(1, 6144, 2048, 384, 8) == moe.MOE_PATH_PERSISTENT     # one token, full shape
+    assert sel(32, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT     # 32 tokens, mid shape
+    assert sel(1, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI          # too few items per SM
+    assert sel(16, 256, 128, 8, 2) == moe.MOE_PATH_MULTI
     assert sel(256, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # full shape, 256 tokens
     assert sel(1024, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI
     assert sel(8, 2048, 1024, 64, 8, moe.MOE_ACT_BF16) == moe.MOE_PATH_MULTI

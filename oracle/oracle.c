@@ -351,3 +351,74 @@ int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
   free(d);
   return 0;
 }
+
+/* --------------------------------------------------- the router and a dense
+ * FP8 projection (the steps beside the expert layer) */
+
+/* Router: one logit per expert from the token's hidden state.  The pages name
+ * expert routing as part of the pipeline the runtime is built around
+ * (techllm.github.io, "Xiaomi MiMo and TileRT ...", section "3. TileRT") but
+ * give no formula; read as the usual linear layer, logits = x W_r^T, with bf16
+ * weights W_r [E, H].  Exact fp64 dot products of the decoded bf16 values. */
+void oracle_router_logits(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t T,
+                          int64_t H, int64_t E, double* out) {
+#pragma omp parallel for schedule(static)
+  for (int64_t t = 0; t < T; ++t) {
+    for (int64_t e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int64_t h = 0; h < H; ++h)
+        s += oracle_bf16_value(x_bf16[t * H + h]) * oracle_bf16_value(w_bf16[e * H + h]);
+      out[t * E + e] = s;
+    }
+  }
+}
+
+/* MXFP8 packing of fp32 rows [R, K] (K % 32 == 0), the rule of
+ * oracle_mxfp8_quantize_row applied to each row */
+void oracle_mxfp8_quantize(const float* w, int64_t R, int64_t K, uint8_t* codes,
+                           uint8_t* scales) {
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) {
+    double* v = (double*)malloc(sizeof(double) * (size_t)K);
+    for (int64_t i = 0; i < K; ++i) v[i] = (double)w[r * K + i];
+    oracle_mxfp8_quantize_row(v, K, codes + r * K, scales + r * (K / 32));
+    free(v);
+  }
+}
+
+/* Dense FP8 projection, a layer outside the experts: the pages keep every
+ * module but the MoE experts at FP8 (techllm.github.io, "Xiaomi MiMo and
+ * TileRT ...", section "1. MXFP4 — MoE에만 걸린 양자화"; ai.appwright.xyz, tag
+ * page "投機的デコード", section "第1層：FP4量子化": o_proj stays out of FP4).
+ * Read as MXFP8 weights (E4M3 codes [N, K], E8M0 scales [N, K/32], decoded
+ * exactly as e4m3(code) * 2^(scale - 127)) and
+ *   y[t, n] = bf16_RNE( sum_k act(x[t, k]) * w[n, k] ),
+ * act = MXFP8 of x along K (the same rule as the experts' inputs) or the
+ * identity (exact mode).  y_f64 / y_bf16 [T, N] may each be NULL. */
+int oracle_dense_forward(const uint16_t* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
+                         int64_t T, int64_t K, int64_t N, int act_mode, double* y_f64,
+                         uint16_t* y_bf16) {
+  if (T < 0 || K <= 0 || N <= 0 || K % 32) return -1;
+  if (act_mode != ORACLE_ACT_EXACT && act_mode != ORACLE_ACT_MXFP8) return -1;
+  init_mags();
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t t = 0; t < T; ++t) {
+    double* a = (double*)malloc(sizeof(double) * (size_t)K);
+    uint8_t* tc = (uint8_t*)malloc((size_t)K);
+    uint8_t* ts = (uint8_t*)malloc((size_t)K / 32);
+    for (int64_t i = 0; i < K; ++i) a[i] = oracle_bf16_value(x_bf16[t * K + i]);
+    apply_act(a, K, act_mode, tc, ts);
+    for (int64_t n = 0; n < N; ++n) {
+      double s = 0.0;
+      for (int64_t i = 0; i < K; ++i)
+        s += a[i] * oracle_e4m3_value(w_e4m3[n * K + i]) *
+             oracle_e8m0_value(w_e8m0[n * (K / 32) + i / 32]);
+      if (y_f64) y_f64[t * N + n] = s;
+      if (y_bf16) y_bf16[t * N + n] = oracle_bf16_from_double(s);
+    }
+    free(a);
+    free(tc);
+    free(ts);
+  }
+  return 0;
+}

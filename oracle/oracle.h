@@ -19,6 +19,10 @@
  * per 32 along the reduction dimension) in MXFP8-emulation mode, and bf16
  * rounding of the intermediate in bf16-emulation mode.
  *
+ * Beside the layer: the router logits that feed its top-k (a linear layer
+ * with bf16 weights), and a dense projection with MXFP8 weights (a layer
+ * outside the experts, kept at FP8).
+ *
  * Parity pins: every function below is checked by the CPU test-suite against
  * closed forms, format tables, library routines or brute force (see the
  * tests named test_oracle_*).  No function here is unpinned.
@@ -77,6 +81,21 @@ int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
                        int64_t I, int64_t E, int k, int act_mode, const int64_t* tokens,
                        int64_t n_tokens, double* y_f64, uint16_t* y_bf16, double* h_out,
                        int n_threads);
+
+/* router logits [T, E] = x [T, H] (bf16) times W_r^T (W_r [E, H] bf16), exact fp64 */
+void oracle_router_logits(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t T,
+                          int64_t H, int64_t E, double* out);
+
+/* MXFP8 packing of fp32 rows [R, K] (K % 32 == 0): E4M3 codes [R, K], E8M0 [R, K/32] */
+void oracle_mxfp8_quantize(const float* w, int64_t R, int64_t K, uint8_t* codes,
+                           uint8_t* scales);
+
+/* dense FP8 projection y [T, N] = act(x [T, K]) W^T with MXFP8 weights W [N, K];
+ * act_mode ORACLE_ACT_EXACT or ORACLE_ACT_MXFP8; y_f64 / y_bf16 may be NULL.
+ * Returns 0, or -1 on invalid arguments. */
+int oracle_dense_forward(const uint16_t* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
+                         int64_t T, int64_t K, int64_t N, int act_mode, double* y_f64,
+                         uint16_t* y_bf16);
 
 #ifdef __cplusplus
 }

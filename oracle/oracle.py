@@ -56,6 +56,12 @@ def lib():
         L.oracle_moe_forward.restype = i32
         L.oracle_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
                                          vp, i64, vp, vp, vp, i32]
+        L.oracle_router_logits.restype = None
+        L.oracle_router_logits.argtypes = [vp, vp, i64, i64, i64, vp]
+        L.oracle_mxfp8_quantize.restype = None
+        L.oracle_mxfp8_quantize.argtypes = [vp, i64, i64, vp, vp]
+        L.oracle_dense_forward.restype = i32
+        L.oracle_dense_forward.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp]
         _lib = L
     return _lib
 
@@ -132,3 +138,41 @@ def moe_forward(x_bf16, logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, k, act_mode=
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected the arguments ({rc})")
     return y16, y64, h
+
+
+def router_logits(x_bf16: np.ndarray, w_bf16: np.ndarray) -> np.ndarray:
+    """Router logits [T, E] in fp64 from x [T, H] and W_r [E, H] (bf16 bit patterns)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
+    T, H = x.shape
+    E = w.shape[0]
+    assert w.shape[1] == H
+    out = np.empty((T, E), dtype=np.float64)
+    lib().oracle_router_logits(_p(x), _p(w), T, H, E, _p(out))
+    return out
+
+
+def mxfp8_quantize(w: np.ndarray):
+    """fp32 [R, K] -> (E4M3 codes [R, K] uint8, E8M0 scales [R, K/32] uint8)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    K = w.shape[-1]
+    R = w.size // K
+    codes = np.empty(w.shape, dtype=np.uint8)
+    sc = np.empty(w.shape[:-1] + (K // 32,), dtype=np.uint8)
+    lib().oracle_mxfp8_quantize(_p(w), R, K, _p(codes), _p(sc))
+    return codes, sc
+
+
+def dense_forward(x_bf16, w_e4m3, w_e8m0, act_mode=ACT_MXFP8):
+    """Dense FP8 projection: returns (y_bf16 uint16 [T, N], y_f64 [T, N])."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    w = np.ascontiguousarray(w_e4m3, dtype=np.uint8)
+    s = np.ascontiguousarray(w_e8m0, dtype=np.uint8)
+    T, K = x.shape
+    N = w.shape[0]
+    y16 = np.empty((T, N), dtype=np.uint16)
+    y64 = np.empty((T, N), dtype=np.float64)
+    rc = lib().oracle_dense_forward(_p(x), _p(w), _p(s), T, K, N, act_mode, _p(y64), _p(y16))
+    if rc != 0:
+        raise ValueError("oracle_dense_forward: invalid arguments")
+    return y16, y64

@@ -1,8 +1,9 @@
 /*
  * Host build of the counter-based synthetic input generator (definitions in
  * synth_core.h).  Test and benchmark infrastructure: it fills the inputs of
- * the MoE layer (x, router logits, fp32 expert weights before packing) and
- * holds none of the layer's arithmetic.
+ * the MoE layer (x, router logits, fp32 expert weights before packing, bf16
+ * router weights, fp32 dense-projection weights) and holds none of the
+ * layer's arithmetic.
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (see synth.py).
  * -ffp-contract=off keeps the single fp32 multiply a separate rounding, the
@@ -45,6 +46,18 @@ static uint16_t f32_to_bf16_rne(float f) {
   memcpy(&u, &f, 4);
   u += 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)(u >> 16);
+}
+
+/* out[j] = bf16_RNE(sigma * z(key(seed, id), start + j)), j in [0, n) */
+void synth_fill_bf16(uint64_t seed, uint32_t tensor_id, uint64_t start, uint64_t n,
+                     float sigma, uint16_t* out) {
+  const uint64_t key = synth_key(seed, tensor_id);
+  int64_t nn = (int64_t)n;
+#pragma omp parallel for schedule(static)
+  for (int64_t j = 0; j < nn; ++j) {
+    volatile float p = sigma * z_as_float(synth_z_num(key, start + (uint64_t)j));
+    out[j] = f32_to_bf16_rne(p);
+  }
 }
 
 /* x[t, h] = bf16_RNE(z(key(seed, X), t*H + h)), unit variance */

@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 HOST_LIB = os.path.join(_HERE, "libsynth.so")
 DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
 
-ID_X, ID_LOGITS, ID_W13, ID_W2 = 0, 1, 2, 3
+ID_X, ID_LOGITS, ID_W13, ID_W2, ID_WROUTER, ID_WDENSE = 0, 1, 2, 3, 4, 5
 W_SIGMA = 0.02
 
 
@@ -58,6 +58,8 @@ def _host_lib():
         lib.synth_fill_normal_f32.argtypes = [u64, u32, u64, u64, ctypes.c_float, ctypes.c_void_p]
         lib.synth_fill_x_bf16.restype = None
         lib.synth_fill_x_bf16.argtypes = [u64, i64, i64, ctypes.c_void_p]
+        lib.synth_fill_bf16.restype = None
+        lib.synth_fill_bf16.argtypes = [u64, u32, u64, u64, ctypes.c_float, ctypes.c_void_p]
         lib.synth_fill_logits.restype = None
         lib.synth_fill_logits.argtypes = [u64, i64, i64, ctypes.c_int, ctypes.c_void_p]
         _host = lib
@@ -101,6 +103,33 @@ def x_bf16(seed: int, T: int, H: int) -> np.ndarray:
     out = np.empty((T, H), dtype=np.uint16)
     if T * H:
         _host_lib().synth_fill_x_bf16(seed, T, H, out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def router_sigma(H: int) -> float:
+    """Router weight scale: the power of two nearest below 1/sqrt(H), so that logits of
+    unit-variance x have a standard deviation in [0.5, 1)."""
+    s = 1.0
+    while s * s * H > 1.0:
+        s *= 0.5
+    return s
+
+
+def router_bf16(seed: int, E: int, H: int) -> np.ndarray:
+    """Router weights [E, H] as bf16 bit patterns (uint16): bf16(router_sigma(H) * z)."""
+    out = np.empty((E, H), dtype=np.uint16)
+    if E * H:
+        _host_lib().synth_fill_bf16(seed, ID_WROUTER, 0, E * H, router_sigma(H),
+                                    out.ctypes.data_as(ctypes.c_void_p))
+    return out
+
+
+def dense_w_f32(seed: int, N: int, K: int) -> np.ndarray:
+    """fp32 dense-projection weights [N, K] (before MXFP8 packing)."""
+    out = np.empty((N, K), dtype=np.float32)
+    if N * K:
+        _host_lib().synth_fill_normal_f32(seed, ID_WDENSE, 0, N * K, W_SIGMA,
+                                          out.ctypes.data_as(ctypes.c_void_p))
     return out
 
 

@@ -47,6 +47,8 @@
 #define SYNTH_ID_LOGITS 1u
 #define SYNTH_ID_W13 2u
 #define SYNTH_ID_W2 3u
+#define SYNTH_ID_WROUTER 4u
+#define SYNTH_ID_WDENSE 5u
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;

@@ -45,3 +45,23 @@ def test_zipf_bias(synth_mod):
     bias = np.array([3.0 * math.log(1.0 / (e + 1)) for e in range(E)])
     assert np.allclose(b - a, bias[None, :], atol=1e-5)
     assert b[:, 0].mean() > b[:, -1].mean()
+
+
+def test_router_and_dense_weight_draws(synth_mod):
+    """The bf16 router fill is bf16_RNE(sigma * z) of the pinned z draws (tensor id 4); the
+    dense weight fill is sigma * z in fp32 (tensor id 5)."""
+    import torch
+    E, H, seed = 3, 256, 9
+    sigma = synth_mod.router_sigma(H)
+    assert sigma == 2.0 ** -4
+    w = synth_mod.router_bf16(seed, E, H)
+    z = np.array([synth_mod.z_numerator(seed, synth_mod.ID_WROUTER, i) for i in range(E * H)],
+                 dtype=np.float64) * 2.0 ** -16
+    want = torch.from_numpy((np.float32(sigma) * z.astype(np.float32)).astype(np.float32)).to(
+        torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(w.ravel(), want)
+    d = synth_mod.dense_w_f32(seed, 2, 64)
+    zd = np.array([synth_mod.z_numerator(seed, synth_mod.ID_WDENSE, i) for i in range(128)],
+                  dtype=np.float64) * 2.0 ** -16
+    assert np.array_equal(d.ravel(), (np.float32(synth_mod.W_SIGMA) * zd.astype(np.float32)))
+    assert synth_mod.router_sigma(6144) == 2.0 ** -7 and synth_mod.router_sigma(2048) == 2.0 ** -6

@@ -285,6 +285,86 @@ def measure_config(L, steps, flush_buf):
             "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9}
 
 
+def _time_cold(fn, steps, flush_buf):
+    """median µs of fn() with L2 flushed before each call (events around the call only)"""
+    import torch
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush_buf.add_(1)
+        e0.record()
+        fn()
+        e1.record()
+    torch.cuda.synchronize()
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+
+
+def measure_next_rows(pk, flush_buf):
+    """The steps beside the layer: the router (split-K bf16 GEMM + top-k), the layer with the
+    router in front, and a dense MXFP8 projection (K = N = 6144), each against its roofline."""
+    import torch
+    import mxfp4_expert_layer_dflash_b300 as moe
+    from synth import layers as LY
+    from synth import synth as S
+    hbm = float(pk["hbm_gbs"])
+    bf16_tf = float(pk["bf16_tflops"])
+    rep = {}
+    for T in (8, 256):
+        H, E, k = 6144, 384, 8
+        x = torch.from_numpy(S.x_bf16(100 + T, T, H).view(np.int16)).view(torch.bfloat16).cuda()
+        w = torch.from_numpy(S.router_bf16(100 + T, E, H).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        us = _time_cold(lambda: moe.moe_router_topk(x, w, T, H, E, k, idx, gate), 50, flush_buf)
+        byt = E * H * 2 + T * H * 2 + T * k * 8
+        fl = 2.0 * T * H * E
+        rep[f"router_t{T}"] = {
+            "shape": f"T={T} H={H} E={E} top-{k}, bf16 router weights", "us_cold": us,
+            "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
+            "tflops": fl / (us * 1e-6) / 1e12, "tensor_frac_bf16": fl / (us * 1e-6) / 1e12 / bf16_tf}
+    for T in (8, 256):
+        K = N = 6144
+        x = torch.from_numpy(S.x_bf16(200 + T, T, K).view(np.int16)).view(torch.bfloat16).cuda()
+        wf = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        S.dev_fill_normal_f32(200 + T, S.ID_WDENSE, 0, N * K, S.W_SIGMA, wf.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+        codes = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((N, K // 32), dtype=torch.uint8, device="cuda")
+        moe.mxfp8_quantize(wf, N, K, codes, sc)
+        del wf
+        y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        us = _time_cold(lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y), 50, flush_buf)
+        byt = N * K + N * K // 32 + T * K * 2 + T * N * 2
+        fl = 2.0 * T * K * N
+        rep[f"dense_fp8_t{T}"] = {
+            "shape": f"T={T} K={K} N={N}, MXFP8 weights and activations", "us_cold": us,
+            "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
+            "tflops": fl / (us * 1e-6) / 1e12,
+            "tensor_frac_fp8": fl / (us * 1e-6) / 1e12 / (2.0 * bf16_tf)}
+    L = LY.LAYERS["full_t256"]
+    x = torch.from_numpy(LY.host_x(L).view(np.int16)).view(torch.bfloat16).cuda()
+    lg = torch.from_numpy(LY.host_logits(L)).cuda()
+    wts = LY.device_packed_weights(L, moe.mxfp4_quantize)
+    w_r = torch.from_numpy(S.router_bf16(L.seed, L.E, L.H).view(np.int16)).view(
+        torch.bfloat16).cuda()
+    y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
+    us_r = _time_cold(lambda: moe.moe_mxfp4_forward_routed(x, w_r, *wts, L.T, L.H, L.I, L.E, L.k,
+                                                           y), 20, flush_buf)
+    us_l = _time_cold(lambda: moe.moe_mxfp4_forward(x, lg, *wts, L.T, L.H, L.I, L.E, L.k, y), 20,
+                      flush_buf)
+    rep["routed_layer_t256"] = {"shape": L.desc + ", router in front", "us_cold": us_r,
+                                "us_cold_layer_on_given_logits": us_l}
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError("device status error in the next-rows report")
+    del wts
+    torch.cuda.empty_cache()
+    return rep
+
+
 def run_ours(args, L, rank, world, local_rank):
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
@@ -449,8 +529,10 @@ def run_ours(args, L, rank, world, local_rank):
         out["configs_report_peaks"] = {
             "hbm_gbs": hbm, "fp8_tflops": 2.0 * float(pk["bf16_tflops"]),
             "source": f"{pk_src}: hbm_gbs; bf16_tflops (burst) x 2, the nominal FP8/bf16 ratio"}
-        del flush
         out["configs_report"] = rep
+        log("[rank 0] measuring the router, the routed layer and the dense projection")
+        out["next_rows"] = measure_next_rows(pk, flush)
+        del flush
     if world == 1 and not args.no_cpu_baseline:
         log("[rank 0] timing the CPU oracle on a bounded sample")
         n_tok = min(args.cpu_tokens, L.T)

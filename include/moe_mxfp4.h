@@ -230,6 +230,80 @@ int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
                               int E, int k, void* y_bf16, cudaStream_t stream);
 
 /*
+ * moe_router_topk — the router in front of the layer: logits = x W_r^T, then
+ * the layer's top-k and softmax (step (1) of moe_mxfp4_forward).  The pages
+ * name expert routing as part of the pipeline the runtime is built around
+ * (techllm.github.io, "Xiaomi MiMo and TileRT ...", section "3. TileRT") but
+ * give no formula; read as a linear layer with bf16 weights.
+ *
+ *  x_bf16         [T, H] bf16, device
+ *  w_router_bf16  [E, H] bf16, device (one row of weights per expert)
+ *  logits_out     [T, E] fp32, device, or NULL: the fp32 logits the top-k used
+ *  topk_idx       [T, k] int32, device: experts in descending logit order,
+ *                 the lower index first among equal logits
+ *  topk_w         [T, k] fp32, device: softmax over the k selected logits
+ * Shapes as moe_mxfp4_forward (H a multiple of 128, 1 <= E <= MOE_MAX_E,
+ * 1 <= k <= min(E, MOE_MAX_K)); pointers 16-byte aligned.  The logits are
+ * fp32 sums of exact bf16 products, accumulated on the tensor cores in K
+ * ranges whose partial sums are added in a fixed order: deterministic run to
+ * run.  Scratch from the library-owned cache.  Returns MOE_OK or an error.
+ * No counterpart in the papers beyond the routing step itself.
+ */
+int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H, int E, int k,
+                    float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream);
+
+/*
+ * moe_mxfp4_forward_routed — moe_mxfp4_forward_ex with the router fused in
+ * front: router weights instead of router logits (see moe_router_topk); the
+ * logits never leave the call.  opts as moe_mxfp4_forward_ex (NULL =
+ * defaults); a caller workspace must hold moe_mxfp4_workspace_size_routed
+ * bytes.
+ */
+int moe_mxfp4_forward_routed(const void* x_bf16, const void* w_router_bf16,
+                             const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                             const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int T, int H, int I,
+                             int E, int k, void* y_bf16, cudaStream_t stream,
+                             const moe_opts* opts);
+
+/* scratch bytes of moe_mxfp4_forward_routed (0 on invalid arguments) */
+size_t moe_mxfp4_workspace_size_routed(int T, int H, int I, int E, int k, int act_mode);
+
+/*
+ * mxfp8_quantize — MXFP8 packing of fp32 rows (weights of a dense FP8 layer):
+ * per block of 32 along K, scale code = clamp(floor(log2(amax)) - 8 + 127,
+ * 0, 254) (amax = 0 gives code 0), elements = E4M3(w / 2^(code - 127)),
+ * round to nearest even, saturating at +-448 — the rule of the layer's
+ * activations.
+ *  w         [rows, K] fp32, device, 16-byte aligned; K a multiple of 32
+ *  out_e4m3  [rows, K] uint8, device, 16-byte aligned
+ *  out_e8m0  [rows, K/32] uint8, device
+ */
+int mxfp8_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_e4m3, uint8_t* out_e8m0,
+                   cudaStream_t stream);
+
+/*
+ * moe_fp8_dense_forward — a dense projection with MXFP8 weights, the
+ * precision the pages keep outside the experts (techllm.github.io, "Xiaomi
+ * MiMo and TileRT ...", section "1. MXFP4 — MoE에만 걸린 양자화";
+ * ai.appwright.xyz, tag page "投機的デコード", section "第1層：FP4量子化": o_proj
+ * stays out of FP4):
+ *   y[t, n] = bf16_RNE( sum_k mxfp8(x)[t, k] * w[n, k] ),
+ * w = e4m3(code) * 2^(scale - 127), x quantized to MXFP8 along K exactly as
+ * the layer's activations.
+ *  x_bf16    [T, K] bf16, device
+ *  w_e4m3    [N, K] uint8 E4M3 codes, device (see mxfp8_quantize)
+ *  w_e8m0    [N, K/32] uint8 scale codes, device
+ *  y_bf16    [T, N] bf16, device, overwritten
+ * K a multiple of 128, N a multiple of 4, T >= 0 (0 = no-op); pointers
+ * 16-byte aligned.  The MMA accumulates in fp32 over K ranges whose partial
+ * sums are added in a fixed order (deterministic).  Scratch from the
+ * library-owned cache.  Returns MOE_OK or an error (host-detected errors
+ * launch nothing).
+ */
+int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
+                          int T, int K, int N, void* y_bf16, cudaStream_t stream);
+
+/*
  * moe_mxfp4_get_status — synchronizes `stream`, returns the first device-side
  * error recorded since the last call (MOE_OK if none) and clears it.  A CUDA
  * error seen while synchronizing returns MOE_ERR_CUDA.

@@ -62,6 +62,16 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_forward_ex.restype = i
         L.moe_mxfp4_forward_noalloc.argtypes = fwd
         L.moe_mxfp4_forward_noalloc.restype = i
+        L.moe_mxfp4_forward_routed.argtypes = fwd + [ctypes.POINTER(moe_opts)]
+        L.moe_mxfp4_forward_routed.restype = i
+        L.moe_mxfp4_workspace_size_routed.argtypes = [i, i, i, i, i, i]
+        L.moe_mxfp4_workspace_size_routed.restype = sz
+        L.moe_router_topk.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, vp]
+        L.moe_router_topk.restype = i
+        L.mxfp8_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
+        L.mxfp8_quantize.restype = i
+        L.moe_fp8_dense_forward.argtypes = [vp, vp, vp, i, i, i, vp, vp]
+        L.moe_fp8_dense_forward.restype = i
         L.moe_mxfp4_select_path.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_select_path.restype = i
         L.moe_mxfp4_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -136,6 +146,43 @@ def moe_mxfp4_forward_noalloc(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, 
 
 def moe_mxfp4_workspace_size(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
     return int(lib().moe_mxfp4_workspace_size(T, H, I, E, k, act_mode))
+
+
+def moe_mxfp4_forward_routed(x_bf16, w_router_bf16, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,
+                             I, E, k, y_bf16, stream=None, act_mode=MOE_ACT_MXFP8,
+                             path=MOE_PATH_AUTO, workspace=None, workspace_bytes=0,
+                             debug_flags=0, step_events=None):
+    """The layer with the router in front: router weights [E, H] bf16 instead of logits."""
+    o = moe_opts(act_mode, path, _ptr(workspace), workspace_bytes, debug_flags)
+    if step_events is not None:
+        o.step_events = ctypes.cast(step_events, ctypes.POINTER(ctypes.c_void_p))
+        o.n_step_events = len(step_events)
+    return _check(lib().moe_mxfp4_forward_routed(
+        _ptr(x_bf16), _ptr(w_router_bf16), _ptr(w13_fp4), _ptr(w13_e8m0), _ptr(w2_fp4),
+        _ptr(w2_e8m0), T, H, I, E, k, _ptr(y_bf16), _stream(stream), ctypes.byref(o)),
+        "moe_mxfp4_forward_routed")
+
+
+def moe_mxfp4_workspace_size_routed(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
+    return int(lib().moe_mxfp4_workspace_size_routed(T, H, I, E, k, act_mode))
+
+
+def moe_router_topk(x_bf16, w_router_bf16, T, H, E, k, topk_idx, topk_w, logits_out=None,
+                    stream=None):
+    return _check(lib().moe_router_topk(_ptr(x_bf16), _ptr(w_router_bf16), T, H, E, k,
+                                        _ptr(logits_out), _ptr(topk_idx), _ptr(topk_w),
+                                        _stream(stream)), "moe_router_topk")
+
+
+def mxfp8_quantize(w, rows, K, out_e4m3, out_e8m0, stream=None):
+    return _check(lib().mxfp8_quantize(_ptr(w), rows, K, _ptr(out_e4m3), _ptr(out_e8m0),
+                                       _stream(stream)), "mxfp8_quantize")
+
+
+def moe_fp8_dense_forward(x_bf16, w_e4m3, w_e8m0, T, K, N, y_bf16, stream=None):
+    return _check(lib().moe_fp8_dense_forward(_ptr(x_bf16), _ptr(w_e4m3), _ptr(w_e8m0), T, K, N,
+                                              _ptr(y_bf16), _stream(stream)),
+                  "moe_fp8_dense_forward")
 
 
 def moe_mxfp4_select_path(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:

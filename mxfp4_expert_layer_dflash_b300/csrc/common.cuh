@@ -59,6 +59,8 @@ struct Work {
   uint8_t* hq;        // [T*k, I] E4M3 or bf16
   uint8_t* hs;        // [T*k, I/32]
   float* yp;          // [T*k, H] per-slot expert outputs (fp32)
+  float* part;        // router split-K partials [splits][T][E] (routed forward only)
+  float* rlogits;     // router logits [T, E] (routed forward only)
   int max_chunks;
 };
 

@@ -23,13 +23,16 @@
 // "TileRT", for this layer): every CTA walks its GEMM1 items, then its GEMM2
 // items, and a GEMM2 item waits (bounded) until all GEMM1 items of its token
 // chunk have published h.  Each CTA finishes its GEMM1 items before any GEMM2
-// item and all CTAs are resident, so every wait is on work that is running.
+// item and the launch is cooperative (all CTAs resident), so every wait is on
+// work that is running.
 // Two weight boxes per pipeline round keep the fixed cost of a round small
 // against the bytes it moves.
 //
 // Warp roles (384 threads, one CTA per SM, persistent over work items):
-//   warp 0      TMA producer (weight tiles + activation tile), one lane
-//   warp 2      TMEM owner and MMA issuer, one lane
+//   warp 0      TMA producer (weight tiles + activation tile): the warp walks
+//               the fills convergently, one elected lane issues each copy
+//   warp 2      TMEM owner and MMA issuer, convergent like the producer (a
+//               single lane in a divergent branch issues MMAs far slower)
 //   warps 4-7   scale stagers: warp w owns TMEM lanes 32*(w%4).. and writes the
 //               E8M0 words of each stage there with tcgen05.st, loading them
 //               from global memory four to eight stages ahead into registers

@@ -19,6 +19,7 @@
 
 #include "combine.cuh"
 #include "common.cuh"
+#include "dense_tc.cuh"
 #include "fmt.cuh"
 #include "gemm_simt.cuh"
 #include "gemm_tc.cuh"
@@ -127,6 +128,58 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
   return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
 }
 
+constexpr int kRouterNMax = 256;                        // router tokens per work item
+constexpr int kDenseNMax = 128;                         // projection tokens per work item
+constexpr int64_t kRouterPartBytes = 24ll << 20;       // cap on router split partials
+constexpr int64_t kDensePartBytes = 64ll << 20;        // cap on projection split partials
+
+// Work decomposition of a dense split-K GEMM: 128-row weight tiles x token
+// blocks x K splits.  The split count minimises a simple time model (µs):
+// waves of work items x (K blocks per item x a stage's bytes at the ~45 GB/s an
+// SM ingests by TMA + 2 of fixed cost per item), plus the fp32 partials
+// written and read back at about 5 TB/s; under a cap on the partials' bytes,
+// and only splits that leave no item empty.
+struct DensePlan {
+  int m_tiles, n_blocks, k_splits, kb_per_split, kb_total;
+};
+
+DensePlan plan_dense(int64_t M, int64_t T, int kb_total, int n_max, int sms, int64_t cap) {
+  DensePlan P{};
+  P.m_tiles = (int)((M + 127) / 128);
+  P.n_blocks = (int)((T + n_max - 1) / n_max);
+  P.kb_total = kb_total;
+  const int64_t base = (int64_t)P.m_tiles * P.n_blocks;
+  const int64_t split_bytes = T * M * 4;
+  const int64_t rows_b = (std::min<int64_t>(T, n_max) + 15) & ~int64_t(15);
+  const double stage_us = (double)(128 * 128 + rows_b * 128) / 45.0e3;
+  int best = 1;
+  double best_t = -1.0;
+  for (int ks = 1; ks <= std::min(kb_total, kDenseMaxSplits); ++ks) {
+    if (ks > 1 && split_bytes * ks > cap) break;
+    const int per = (kb_total + ks - 1) / ks;
+    if ((kb_total + per - 1) / per != ks) continue;
+    const int64_t items = base * ks;
+    const double t = (double)((items + sms - 1) / sms) * (stage_us * per + 2.0) +
+                     (ks > 1 ? 2.0 * (double)(split_bytes * ks) / 5.0e6 : 0.0);
+    if (best_t < 0.0 || t < best_t) {
+      best_t = t;
+      best = ks;
+    }
+  }
+  P.kb_per_split = (kb_total + best - 1) / best;
+  P.k_splits = (kb_total + P.kb_per_split - 1) / P.kb_per_split;
+  return P;
+}
+
+// bytes of router partials a layer of this shape may need (any device)
+int64_t router_part_bytes(int64_t T, int64_t E) {
+  return std::max<int64_t>(T * E * 4, std::min<int64_t>(kRouterPartBytes,
+                                                         (int64_t)kDenseMaxSplits * T * E * 4));
+}
+
+// token rows per activation TMA box: no wider than the token count needs
+int box_rows_for(int64_t T) { return T <= 16 ? 16 : T <= 32 ? 32 : kDenseBoxRowsB; }
+
 // current device; checks compute capability 10.3 and caches per-device data
 int device_state(DeviceState** out) {
   int dev = 0;
@@ -147,7 +200,13 @@ int device_state(DeviceState** out) {
     const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
     if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              permute_smem) != cudaSuccess ||
-        !set_gemm_smem<kChunkNarrow>() || !set_gemm_smem<kChunkWide>())
+        !set_gemm_smem<kChunkNarrow>() || !set_gemm_smem<kChunkWide>() ||
+        cudaFuncSetAttribute(dense_tc_kernel<kDenseBf16, kRouterNMax>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DenseCfg<kDenseBf16, kRouterNMax>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(dense_tc_kernel<kDenseMxf8, kDenseNMax>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DenseCfg<kDenseMxf8, kDenseNMax>::kSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
     d.ready = true;
   }
@@ -188,11 +247,14 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
 }
 
 struct Layout {
-  size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, done, meta, xq, xs, hq, hs, yp, total;
+  size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, done, meta, xq, xs, hq, hs, yp, part,
+      rlogits, total;
   int max_chunks;
 };
 
-Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act_mode) {
+// routed: the layer computes its router logits (split-K partials in `part`)
+Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act_mode,
+                  bool routed = false) {
   Layout L{};
   const int64_t TK = T * k;
   const int64_t act_bytes = act_mode == MOE_ACT_BF16 ? 2 : 1;
@@ -217,6 +279,8 @@ Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act
   L.hq = take(TK * I * act_bytes);
   L.hs = take(TK * (I / 32));
   L.yp = take(TK * H * 4);
+  L.part = take(routed ? (size_t)router_part_bytes(T, E) : 0);
+  L.rlogits = take(routed ? (size_t)(T * E * 4) : 0);
   L.total = o;
   return L;
 }
@@ -238,6 +302,8 @@ Work carve(void* base, const Layout& L) {
   w.hq = b + L.hq;
   w.hs = b + L.hs;
   w.yp = reinterpret_cast<float*>(b + L.yp);
+  w.part = reinterpret_cast<float*>(b + L.part);
+  w.rlogits = reinterpret_cast<float*>(b + L.rlogits);
   w.max_chunks = L.max_chunks;
   return w;
 }
@@ -275,18 +341,75 @@ int grid_for(int64_t work, int per_block, int cap) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(g, cap));
 }
 
-// routing steps (1)-(4) into w
-int enqueue_route(const float* logits, int T, int E, int k, int chunk_max, const Work& w,
-                  DeviceState* d, cudaStream_t s, Steps& st) {
-  const int grid = grid_for((int64_t)T * 32, 256, 1 << 30);
+// Router logits [T, E] = x [T, H] (bf16) times W_r^T (W_r [E, H] bf16): a
+// split-K GEMM into part[ks][t][e], then the partials summed in split order
+// into `logits`.  The first kernels of a call.
+int enqueue_router(const void* x_bf16, const void* w_router, int T, int H, int E, float* part,
+                   float* logits, DeviceState* d, cudaStream_t s, unsigned long long timeout_ns,
+                   Steps& st) {
+  const DensePlan P =
+      plan_dense(E, T, H / 64, kRouterNMax, d->sms, router_part_bytes(T, E));
+  DenseParams dp{};
+  int rc;
+  if ((rc = make_map(&dp.map_a, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w_router, H, E,
+                     (uint64_t)H * 2, 64, 128)) ||
+      (rc = make_map(&dp.map_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x_bf16, H, T,
+                     (uint64_t)H * 2, 64, box_rows_for(T))))
+    return rc;
+  dp.box_rows_b = box_rows_for(T);
+  dp.part = part;
+  dp.M = E;
+  dp.T = T;
+  dp.m_tiles = P.m_tiles;
+  dp.n_blocks = P.n_blocks;
+  dp.k_splits = P.k_splits;
+  dp.kb_per_split = P.kb_per_split;
+  dp.kb_total = P.kb_total;
+  dp.status = d->status;
+  dp.timeout_ns = timeout_ns;
+  const int items = P.m_tiles * P.n_blocks * P.k_splits;
   st.mark();
-  if (E <= 128)
-    route_topk_kernel<4><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
-  else if (E <= 384)
-    route_topk_kernel<12><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
-  else
-    route_topk_kernel<32><<<grid, 256, 0, s>>>(logits, T, E, k, w.topk_idx, w.topk_w, d->status);
+  dense_tc_kernel<kDenseBf16, kRouterNMax>
+      <<<std::min(items, d->sms), kDenseThreads, DenseCfg<kDenseBf16, kRouterNMax>::kSmem, s>>>(
+          dp);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
+  st.mark();
+  if (launch_pdl(splitk_reduce_f32_kernel, dim3(grid_for((int64_t)T * E, 32, d->sms * 8)),
+                 dim3(256), 0, s,
+                 (const float*)part, P.k_splits, T, E, logits) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st.launched();
+  return MOE_OK;
+}
+
+// step (1): top-k + softmax into topk_idx / topk_w (see enqueue_route); an
+// ordinary launch when it is the call's first kernel, else programmatic
+int enqueue_topk(const float* logits, bool first, int T, int E, int k, int32_t* topk_idx,
+                 float* topk_w, DeviceState* d, cudaStream_t s, Steps& st) {
+  const dim3 grid(grid_for((int64_t)T * 32, 256, 1 << 30));
+  st.mark();
+  auto topk = [&](auto kernel) {
+    if (first) {
+      kernel<<<grid, 256, 0, s>>>(logits, T, E, k, topk_idx, topk_w, d->status);
+      return cudaGetLastError();
+    }
+    return launch_pdl(kernel, grid, dim3(256), 0, s, logits, T, E, k, topk_idx, topk_w,
+                      d->status);
+  };
+  const cudaError_t te = E <= 128   ? topk(route_topk_kernel<4>)
+                         : E <= 384 ? topk(route_topk_kernel<12>)
+                                    : topk(route_topk_kernel<32>);
+  if (te != cudaSuccess) return MOE_ERR_CUDA;
+  st.launched();
+  return MOE_OK;
+}
+
+// Routing steps (1)-(4) into w; `first`: the top-k is the call's first kernel
+int enqueue_route(const float* logits, bool first, int T, int E, int k, int chunk_max,
+                  const Work& w, DeviceState* d, cudaStream_t s, Steps& st) {
+  int rc = enqueue_topk(logits, first, T, E, k, w.topk_idx, w.topk_w, d, s, st);
+  if (rc) return rc;
   st.mark();
   const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
   if (launch_pdl(route_permute_kernel, dim3(1), dim3(1024), smem, s, w.topk_idx, T, k, E, w.cnt,
@@ -314,12 +437,19 @@ int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
              : MOE_PATH_MULTI;
 }
 
+// The layer.  Exactly one of `logits` (router logits [T, E]) and `w_router`
+// (router weights [E, H] bf16: the router GEMM runs in front of the top-k)
+// is given.
 int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
                  const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
-                 void* y, cudaStream_t stream, const moe_opts* opts) {
-  if (!x_bf16 || !logits || !w13 || !w13s || !w2 || !w2s || !y) return MOE_ERR_INVALID_ARG;
+                 void* y, cudaStream_t stream, const moe_opts* opts,
+                 const void* w_router = nullptr) {
+  if (!x_bf16 || (!logits == !w_router) || !w13 || !w13s || !w2 || !w2s || !y)
+    return MOE_ERR_INVALID_ARG;
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
+  const bool routed = w_router != nullptr;
+  if (routed && !aligned(w_router, 16)) return MOE_ERR_ALIGNMENT;
   const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
   const int path = opts ? opts->path : MOE_PATH_AUTO;
   if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
@@ -328,7 +458,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
       !aligned(y, 16))
     return MOE_ERR_ALIGNMENT;
-  const Layout L = layout_for(T, H, I, E, k, act);
+  const Layout L = layout_for(T, H, I, E, k, act, routed);
   if (opts && opts->workspace) {
     if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
     if (opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
@@ -345,15 +475,22 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   // Wide token chunks halve the MMA instructions per token when experts get
   // many tokens (large T); narrow chunks keep the weight pipeline deepest.
   const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
+  const unsigned long long timeout_ns =
+      (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
-  if ((rc = enqueue_route(logits, T, E, k, wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
+  if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
+                                     timeout_ns, st)))
+    return rc;
+  if ((rc = enqueue_route(routed ? w.rlogits : logits, !routed, T, E, k,
+                          wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
     return rc;
   const int cap = d->sms * 8;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   st.mark();
   const cudaError_t qe =
       act == MOE_ACT_MXFP8
-          ? launch_pdl(mxfp8_rows_kernel, dim3(grid_for(TK, 8, cap)), dim3(256), 0, stream, x,
+          ? launch_pdl(mxfp8_rows_kernel, dim3(grid_for((int64_t)TK * ((H / 32 + 31) / 32), 8, cap)),
+                       dim3(256), 0, stream, x,
                        (const int32_t*)w.perm, (int64_t)TK, (int64_t)H, (int64_t)T, w.xq, w.xs,
                        d->status)
           : launch_pdl(gather_bf16_rows_kernel, dim3(grid_for(TK, 8, cap)), dim3(256), 0, stream,
@@ -362,8 +499,6 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   if (qe != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
   if (act == MOE_ACT_MXFP8) {
-    const unsigned long long timeout_ns =
-        (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
     TcPhase g1{}, g2{};
     if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
                        H / 2, 128, 128)) ||
@@ -534,7 +669,7 @@ int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* to
   w.perm = perm;
   w.pos = pos;
   Steps st{nullptr, stream};
-  return enqueue_route(router_logits, T, E, k, kChunkNarrow, w, d, stream, st);
+  return enqueue_route(router_logits, true, T, E, k, kChunkNarrow, w, d, stream, st);
 }
 
 int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t* codes,
@@ -546,10 +681,121 @@ int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t
   DeviceState* d = nullptr;
   int rc = device_state(&d);
   if (rc) return rc;
-  mxfp8_rows_kernel<<<grid_for(rows, 8, d->sms * 8), 256, 0, stream>>>(
+  mxfp8_rows_kernel<<<grid_for(rows * ((K / 32 + 31) / 32), 8, d->sms * 8), 256, 0, stream>>>(
       static_cast<const uint16_t*>(x_bf16), nullptr, rows, K, rows, codes, scales, d->status);
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return launch_status();
+}
+
+int moe_mxfp4_forward_routed(const void* x_bf16, const void* w_router_bf16,
+                             const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
+                             const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int T, int H, int I,
+                             int E, int k, void* y_bf16, cudaStream_t stream,
+                             const moe_opts* opts) {
+  if (!w_router_bf16) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x_bf16, nullptr, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I, E, k, y_bf16,
+                      stream, opts, w_router_bf16);
+}
+
+size_t moe_mxfp4_workspace_size_routed(int T, int H, int I, int E, int k, int act_mode) {
+  if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
+  return layout_for(T, H, I, E, k, act_mode, true).total;
+}
+
+int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H, int E, int k,
+                    float* logits_out, int32_t* topk_idx, float* topk_w, cudaStream_t stream) {
+  if (!x_bf16 || !w_router_bf16 || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, 128, E, k);
+  if (rc) return rc;
+  if (!aligned(x_bf16, 16) || !aligned(w_router_bf16, 16)) return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  const size_t part_bytes = align256((size_t)router_part_bytes(T, E));
+  void* ws = nullptr;
+  if ((rc = cached_workspace(d, part_bytes + (size_t)T * E * 4, &ws))) return rc;
+  float* part = static_cast<float*>(ws);
+  float* lg = logits_out ? logits_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
+                                                                   part_bytes);
+  Steps st{nullptr, stream};
+  if ((rc = enqueue_router(x_bf16, w_router_bf16, T, H, E, part, lg, d, stream, 2000000000ull,
+                           st)))
+    return rc;
+  return enqueue_topk(lg, false, T, E, k, topk_idx, topk_w, d, stream, st);
+}
+
+int mxfp8_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_e4m3, uint8_t* out_e8m0,
+                   cudaStream_t stream) {
+  if (!w || !out_e4m3 || !out_e8m0 || rows < 0 || K <= 0) return MOE_ERR_INVALID_ARG;
+  if (K % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(w, 16) || !aligned(out_e4m3, 16)) return MOE_ERR_ALIGNMENT;
+  if (rows == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  mxfp8_rows_f32_kernel<<<grid_for(rows, 8, d->sms * 8), 256, 0, stream>>>(w, rows, K, out_e4m3,
+                                                                          out_e8m0);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return launch_status();
+}
+
+int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
+                          int T, int K, int N, void* y_bf16, cudaStream_t stream) {
+  if (!x_bf16 || !w_e4m3 || !w_e8m0 || !y_bf16 || T < 0 || K <= 0 || N <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (K % 128 || N % 4) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned(x_bf16, 16) || !aligned(w_e4m3, 16) || !aligned(w_e8m0, 16) || !aligned(y_bf16, 16))
+    return MOE_ERR_ALIGNMENT;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  const DensePlan P = plan_dense(N, T, K / 128, kDenseNMax, d->sms, kDensePartBytes);
+  const size_t xq_bytes = align256((size_t)T * K), xs_bytes = align256((size_t)T * (K / 32));
+  const size_t part_bytes = (size_t)P.k_splits * T * N * 4;
+  void* ws = nullptr;
+  if ((rc = cached_workspace(d, xq_bytes + xs_bytes + part_bytes, &ws))) return rc;
+  uint8_t* xq = static_cast<uint8_t*>(ws);
+  uint8_t* xs = xq + xq_bytes;
+  float* part = reinterpret_cast<float*>(xs + xs_bytes);
+
+  mxfp8_rows_kernel<<<grid_for((int64_t)T * ((K / 32 + 31) / 32), 8, d->sms * 8), 256, 0,
+                      stream>>>(
+      static_cast<const uint16_t*>(x_bf16), nullptr, T, K, T, xq, xs, d->status);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+
+  DenseParams dp{};
+  if ((rc = make_map(&dp.map_a, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_e4m3, K, N, K, 128, 128)) ||
+      (rc = make_map(&dp.map_b, CU_TENSOR_MAP_DATA_TYPE_UINT8, xq, K, T, K, 128,
+                     box_rows_for(T))))
+    return rc;
+  dp.box_rows_b = box_rows_for(T);
+  dp.a_sf = w_e8m0;
+  dp.b_sf = xs;
+  dp.part = part;
+  dp.M = N;
+  dp.T = T;
+  dp.m_tiles = P.m_tiles;
+  dp.n_blocks = P.n_blocks;
+  dp.k_splits = P.k_splits;
+  dp.kb_per_split = P.kb_per_split;
+  dp.kb_total = P.kb_total;
+  dp.status = d->status;
+  dp.timeout_ns = 2000000000ull;
+  const int items = P.m_tiles * P.n_blocks * P.k_splits;
+  if (launch_pdl(dense_tc_kernel<kDenseMxf8, kDenseNMax>, dim3(std::min(items, d->sms)),
+                 dim3(kDenseThreads), DenseCfg<kDenseMxf8, kDenseNMax>::kSmem, stream, dp) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (launch_pdl(splitk_reduce_bf16_kernel, dim3(grid_for((int64_t)T * N / 4, 256, d->sms * 8)),
+                 dim3(256), 0, stream, (const float*)part, P.k_splits, T, N,
+                 static_cast<uint16_t*>(y_bf16)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return MOE_OK;
 }
 
 int moe_mxfp4_get_status(cudaStream_t stream) {

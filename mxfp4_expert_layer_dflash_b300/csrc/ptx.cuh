@@ -221,6 +221,18 @@ __device__ __forceinline__ void mma_mxf8f6f4_warp(uint32_t d_tmem, uint64_t a_de
       : "memory");
 }
 
+// warp-collective form of mma_bf16 (see mma_mxf8f6f4_warp)
+__device__ __forceinline__ void mma_bf16_warp(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred e, p;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[smem] x B[smem]^T, bf16 inputs, fp32 accumulation
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                          uint32_t idesc, uint32_t accumulate) {
@@ -325,10 +337,13 @@ __device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t saddr) {
 }
 
 // instruction descriptor, kind::mxf8f6f4 with block scaling:
-// A = E2M1 (5), B = E4M3 (0), both K-major, UE8M0 scales, M = 128
+// A = E2M1 (5) by default or E4M3 (0), B = E4M3 (0), both K-major, UE8M0
+// scales, M = 128
+constexpr uint32_t kFmtE4M3 = 0, kFmtE2M1 = 5;
 __device__ __forceinline__ uint32_t idesc_mxf8f6f4(uint32_t n, uint32_t sf_id_a,
-                                                   uint32_t sf_id_b) {
-  return (sf_id_b << 4) | (5u << 7) | (0u << 10) | ((n >> 3) << 17) | (1u << 23) |
+                                                   uint32_t sf_id_b,
+                                                   uint32_t a_fmt = kFmtE2M1) {
+  return (sf_id_b << 4) | (a_fmt << 7) | (kFmtE4M3 << 10) | ((n >> 3) << 17) | (1u << 23) |
          ((128u >> 4) << 24) | (sf_id_a << 29);
 }
 

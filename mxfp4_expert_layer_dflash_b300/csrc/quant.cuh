@@ -71,8 +71,9 @@ __device__ __forceinline__ void store_u8x32(uint8_t* p, const uint8_t* c) {
   reinterpret_cast<uint4*>(p)[1] = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
-// MXFP8 rows: one warp per row, lane-strided blocks of 32.  src_row(r) selects
-// the source row (identity, or the permutation slot -> token).
+// MXFP8 rows: one warp per (row, segment of 32 blocks of 32), a block per
+// lane.  row_map selects the source row (identity when null, or the
+// permutation slot -> token).
 __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t* __restrict__ x,
                                                          const int32_t* __restrict__ row_map,
                                                          int64_t rows, int64_t K, int64_t src_rows,
@@ -83,17 +84,50 @@ __global__ void __launch_bounds__(256) mxfp8_rows_kernel(const uint16_t* __restr
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
   const int64_t nb = K / 32;
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
+  const int64_t segs = (nb + 31) / 32;
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); u < rows * segs;
+       u += warps) {
+    const int64_t r = u / segs;
+    const int64_t b = (u - r * segs) * 32 + lane;
     int64_t src = row_map ? row_map[r] : r;
     if (src < 0 || src >= src_rows) {
       if (lane == 0) set_status(status, kStatusFault);
       src = 0;
     }
-    for (int64_t b = lane; b < nb; b += 32) {
+    if (b < nb) {
       float v[32];
       uint8_t c[32];
       load_bf16x32(x + src * K + b * 32, v);
+      const int code = mxfp8_block(v, c);
+      store_u8x32(q + r * K + b * 32, c);
+      s[r * nb + b] = (uint8_t)code;
+    }
+  }
+}
+
+// MXFP8 packing of fp32 rows [rows, K] (weights of a dense FP8 layer): one
+// warp per row, lane-strided blocks of 32, the same rule as the activations
+__global__ void __launch_bounds__(256) mxfp8_rows_f32_kernel(const float* __restrict__ w,
+                                                             int64_t rows, int64_t K,
+                                                             uint8_t* __restrict__ q,
+                                                             uint8_t* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t nb = K / 32;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
+       r += warps) {
+    for (int64_t b = lane; b < nb; b += 32) {
+      float v[32];
+      uint8_t c[32];
+      const float4* src = reinterpret_cast<const float4*>(w + r * K + b * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 f = src[i];
+        v[4 * i] = f.x;
+        v[4 * i + 1] = f.y;
+        v[4 * i + 2] = f.z;
+        v[4 * i + 3] = f.w;
+      }
       const int code = mxfp8_block(v, c);
       store_u8x32(q + r * K + b * 32, c);
       s[r * nb + b] = (uint8_t)code;

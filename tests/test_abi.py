@@ -105,3 +105,27 @@ def test_select_path_validates_on_host(moe):
     assert L.moe_mxfp4_select_path(16, 250, 128, 8, 2, 0) == -2     # H % 128
     assert L.moe_mxfp4_select_path(16, 256, 128, 8, 9, 0) == -1     # k > E
     assert L.moe_mxfp4_select_path(16, 256, 128, 8, 2, 5) == -1     # bad act mode
+
+
+def test_next_rows_validate_on_host(moe):
+    L = moe.lib()
+    # dense projection: K % 128, N % 4, null pointers, alignment; T == 0 is a no-op
+    assert L.moe_fp8_dense_forward(256, 512, 1024, 4, 200, 64, 2048, None) == -2
+    assert L.moe_fp8_dense_forward(256, 512, 1024, 4, 256, 66, 2048, None) == -2
+    assert L.moe_fp8_dense_forward(None, 512, 1024, 4, 256, 64, 2048, None) == -1
+    assert L.moe_fp8_dense_forward(256, 520, 1024, 4, 256, 64, 2048, None) == -3
+    assert L.moe_fp8_dense_forward(256, 512, 1024, 0, 256, 64, 2048, None) == 0
+    # router: shapes as the layer
+    assert L.moe_router_topk(256, 512, 4, 250, 8, 2, None, 1024, 2048, None) == -2
+    assert L.moe_router_topk(256, 512, 4, 256, 8, 9, None, 1024, 2048, None) == -1
+    assert L.moe_router_topk(256, None, 4, 256, 8, 2, None, 1024, 2048, None) == -1
+    assert L.moe_router_topk(256, 512, 0, 256, 8, 2, None, 1024, 2048, None) == 0
+    assert L.mxfp8_quantize(256, 4, 48, 512, 1024, None) == -2
+    assert L.mxfp8_quantize(256, 0, 64, 512, 1024, None) == 0
+    # routed layer: router weights required; workspace larger than the unrouted one
+    o = moe.moe_opts(0, 0, None, 0, 0, None, 0)
+    import ctypes
+    assert L.moe_mxfp4_forward_routed(256, None, 1024, 2048, 4096, 8192, 4, 256, 128, 8, 2,
+                                      16384, None, ctypes.byref(o)) == -1
+    assert (moe.moe_mxfp4_workspace_size_routed(256, 6144, 2048, 384, 8)
+            > moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8))

@@ -422,3 +422,78 @@ int oracle_dense_forward(const uint16_t* x_bf16, const uint8_t* w_e4m3, const ui
   }
   return 0;
 }
+
+/* ------------------------------------------------ speculative verification */
+
+/* Inverse-CDF draw over masses m[x] = floor(w[x] * 2^62) (w = fp32 weights in
+ * [0, 1], the scaling exact): with M = sum m, the drawn index is the first x
+ * whose running sum exceeds floor(U * M / 2^64).  Returns -1 when M == 0. */
+static int64_t draw_fixed_point(const float* w, int64_t V, uint64_t U) {
+  uint64_t M = 0;
+  for (int64_t x = 0; x < V; ++x) M += (uint64_t)floor((double)w[x] * 0x1p62);
+  if (M == 0) return -1;
+  const unsigned __int128 prod = (unsigned __int128)U * (unsigned __int128)M;
+  const uint64_t t = (uint64_t)(prod >> 64);
+  uint64_t run = 0;
+  for (int64_t x = 0; x < V; ++x) {
+    run += (uint64_t)floor((double)w[x] * 0x1p62);
+    if (run > t) return x;
+  }
+  return V - 1; /* not reached: t < M */
+}
+
+/* Rejection-sampling verification of one block of drafted tokens per
+ * sequence (lossless speculative decoding: techllm.github.io, "Xiaomi MiMo and
+ * TileRT ...", section "2. DFlash"; the block is at most 8 positions:
+ * dothoosh.com, section "جزئیات پیاده‌سازی DFlash").  For sequence s, drafted
+ * tokens d_0..d_{g-1} with draft distributions q_i and target distributions
+ * p_0..p_g (p_g for the position after the block):
+ *   accept d_i while u_i * q_i(d_i) < p_i(d_i) (exact: fp32 values compared
+ *   in fp64; for u uniform on [0, 1) this happens with probability
+ *   min(1, p_i(d_i) / q_i(d_i)), and a token with p_i(d_i) = 0 is never
+ *   accepted);
+ *   at the first rejection i, emit a token drawn from max(0, p_i - q_i) (the
+ *   fp32 difference), else after g acceptances emit one drawn from p_g; draws
+ *   use draw_fixed_point with the sequence's 64-bit uniform U[s] (from p_i
+ *   itself if the residual mass is 0).
+ * Outputs: n_acc[s] in [0, g]; tokens[s, 0..n_acc] = accepted drafts then the
+ * emitted token (tokens [S, g+1]; entries past n_acc are -1).
+ * p [S, g+1, V], q [S, g, V] fp32; draft [S, g] int32; u [S, g] fp32 in [0, 1). */
+int oracle_verify(const float* p, const float* q, const int32_t* draft, const float* u,
+                  const uint64_t* U, int64_t S, int g, int64_t V, int32_t* n_acc,
+                  int32_t* tokens) {
+  if (S < 0 || g < 1 || V < 1) return -1;
+  float* r = (float*)malloc(sizeof(float) * (size_t)V);
+  for (int64_t s = 0; s < S; ++s) {
+    const float* ps = p + s * (int64_t)(g + 1) * V;
+    const float* qs = q + s * (int64_t)g * V;
+    int32_t* out = tokens + s * (int64_t)(g + 1);
+    for (int i = 0; i <= g; ++i) out[i] = -1;
+    int i = 0;
+    for (; i < g; ++i) {
+      const int32_t d = draft[s * g + i];
+      if (d < 0 || d >= V) { free(r); return -1; }
+      const double lhs = (double)u[s * g + i] * (double)qs[i * V + d];
+      if (lhs < (double)ps[i * V + d]) {
+        out[i] = d;
+      } else {
+        break;
+      }
+    }
+    n_acc[s] = i;
+    int64_t x;
+    if (i < g) {
+      for (int64_t v = 0; v < V; ++v) {
+        const float diff = ps[i * V + v] - qs[i * V + v];
+        r[v] = diff > 0.0f ? diff : 0.0f;
+      }
+      x = draw_fixed_point(r, V, U[s]);
+      if (x < 0) x = draw_fixed_point(ps + i * V, V, U[s]);
+    } else {
+      x = draw_fixed_point(ps + (int64_t)g * V, V, U[s]);
+    }
+    out[i] = (int32_t)(x < 0 ? 0 : x);
+  }
+  free(r);
+  return 0;
+}

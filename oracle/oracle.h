@@ -20,8 +20,9 @@
  * rounding of the intermediate in bf16-emulation mode.
  *
  * Beside the layer: the router logits that feed its top-k (a linear layer
- * with bf16 weights), and a dense projection with MXFP8 weights (a layer
- * outside the experts, kept at FP8).
+ * with bf16 weights), a dense projection with MXFP8 weights (a layer outside
+ * the experts, kept at FP8), and the rejection-sampling verification of a
+ * block of drafted tokens (the step after the verify forward).
  *
  * Parity pins: every function below is checked by the CPU test-suite against
  * closed forms, format tables, library routines or brute force (see the
@@ -96,6 +97,15 @@ void oracle_mxfp8_quantize(const float* w, int64_t R, int64_t K, uint8_t* codes,
 int oracle_dense_forward(const uint16_t* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
                          int64_t T, int64_t K, int64_t N, int act_mode, double* y_f64,
                          uint16_t* y_bf16);
+
+/* Rejection-sampling verification of a block of g drafted tokens per sequence
+ * (see oracle.c): p [S, g+1, V], q [S, g, V] fp32 probabilities, draft [S, g],
+ * u [S, g] fp32 uniforms in [0, 1), U [S] 64-bit uniforms; outputs n_acc [S]
+ * and tokens [S, g+1] (-1 past the emitted token).  Returns 0, or -1 on
+ * invalid arguments. */
+int oracle_verify(const float* p, const float* q, const int32_t* draft, const float* u,
+                  const uint64_t* U, int64_t S, int g, int64_t V, int32_t* n_acc,
+                  int32_t* tokens);
 
 #ifdef __cplusplus
 }

@@ -60,6 +60,8 @@ def lib():
         L.oracle_router_logits.argtypes = [vp, vp, i64, i64, i64, vp]
         L.oracle_mxfp8_quantize.restype = None
         L.oracle_mxfp8_quantize.argtypes = [vp, i64, i64, vp, vp]
+        L.oracle_verify.restype = i32
+        L.oracle_verify.argtypes = [vp, vp, vp, vp, vp, i64, i32, i64, vp, vp]
         L.oracle_dense_forward.restype = i32
         L.oracle_dense_forward.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp]
         _lib = L
@@ -176,3 +178,21 @@ def dense_forward(x_bf16, w_e4m3, w_e8m0, act_mode=ACT_MXFP8):
     if rc != 0:
         raise ValueError("oracle_dense_forward: invalid arguments")
     return y16, y64
+
+
+def verify(p, q, draft, u, U):
+    """Rejection-sampling verification: p [S, g+1, V], q [S, g, V] fp32, draft [S, g] int32,
+    u [S, g] fp32, U [S] uint64 -> (n_acc [S] int32, tokens [S, g+1] int32)."""
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    q = np.ascontiguousarray(q, dtype=np.float32)
+    draft = np.ascontiguousarray(draft, dtype=np.int32)
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    U = np.ascontiguousarray(U, dtype=np.uint64)
+    S, g, V = q.shape
+    assert p.shape == (S, g + 1, V) and draft.shape == (S, g) and u.shape == (S, g)
+    n_acc = np.empty(S, dtype=np.int32)
+    tok = np.empty((S, g + 1), dtype=np.int32)
+    if lib().oracle_verify(_p(p), _p(q), _p(draft), _p(u), _p(U), S, g, V, _p(n_acc),
+                           _p(tok)) != 0:
+        raise ValueError("oracle_verify: invalid arguments")
+    return n_acc, tok

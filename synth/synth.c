@@ -2,8 +2,9 @@
  * Host build of the counter-based synthetic input generator (definitions in
  * synth_core.h).  Test and benchmark infrastructure: it fills the inputs of
  * the MoE layer (x, router logits, fp32 expert weights before packing, bf16
- * router weights, fp32 dense-projection weights) and holds none of the
- * layer's arithmetic.
+ * router weights, fp32 dense-projection weights, the probabilities and
+ * uniforms of a speculative verification) and holds none of the arithmetic
+ * of the steps they feed.
  *
  * Build: gcc -O2 -ffp-contract=off -fopenmp -shared -fPIC (see synth.py).
  * -ffp-contract=off keeps the single fp32 multiply a separate rounding, the
@@ -11,6 +12,7 @@
  */
 #include <math.h>
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "synth_core.h"
@@ -86,4 +88,59 @@ void synth_fill_logits(uint64_t seed, int64_t T, int64_t E, int zipf_bias, float
       }
     }
   }
+}
+
+/* softmax of row[0..V) in double, written as fp32 probabilities */
+static void softmax_row_f32(const double* z, int64_t V, float* out) {
+  double m = z[0];
+  for (int64_t v = 1; v < V; ++v) m = z[v] > m ? z[v] : m;
+  double s = 0.0;
+  for (int64_t v = 0; v < V; ++v) s += exp(z[v] - m);
+  for (int64_t v = 0; v < V; ++v) out[v] = (float)(exp(z[v] - m) / s);
+}
+
+/* Inputs of the speculative verification of a drafted block, for S sequences
+ * of g drafted tokens over a vocabulary of V:
+ *   p [S, g+1, V]  target probabilities, softmax(sigma_t * z)          (id 6)
+ *   q [S, g, V]    draft probabilities, softmax(sigma_t * z + sigma_n * z'),
+ *                  z' a second stream (id 7): a correlated, imperfect drafter
+ *   d [S, g]       drafted tokens, drawn from q by inverse CDF in double with a
+ *                  53-bit uniform from splitmix(key(seed, 8), s*g + i)
+ *   u [S, g]       accept uniforms k / 2^24, k the top 24 bits of
+ *                  splitmix(key(seed, 9), s*g + i)
+ *   U [S]          64-bit resample uniforms splitmix(key(seed, 10), s) */
+void synth_fill_verify(uint64_t seed, int64_t S, int g, int64_t V, float sigma_t, float sigma_n,
+                       float* p, float* q, int32_t* d, float* u, uint64_t* U) {
+  const uint64_t kz = synth_key(seed, SYNTH_ID_VERIFY_Z), kn = synth_key(seed, SYNTH_ID_VERIFY_N);
+  const uint64_t kd = synth_key(seed, SYNTH_ID_VERIFY_D), ku = synth_key(seed, SYNTH_ID_VERIFY_U);
+  const uint64_t kU = synth_key(seed, SYNTH_ID_VERIFY_R);
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t row = 0; row < S * (g + 1); ++row) {
+    const int64_t s = row / (g + 1), i = row % (g + 1);
+    double* z = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int64_t v = 0; v < V; ++v)
+      z[v] = (double)sigma_t * (double)z_as_float(synth_z_num(kz, (uint64_t)(row * V + v)));
+    softmax_row_f32(z, V, p + row * V);
+    if (i < g) {
+      const int64_t qrow = s * g + i;
+      for (int64_t v = 0; v < V; ++v)
+        z[v] += (double)sigma_n * (double)z_as_float(synth_z_num(kn, (uint64_t)(qrow * V + v)));
+      float* qr = q + qrow * V;
+      softmax_row_f32(z, V, qr);
+      const double r = (double)(synth_splitmix(kd, (uint64_t)qrow) >> 11) * 0x1p-53;
+      double c = 0.0;
+      int64_t pick = V - 1;
+      for (int64_t v = 0; v < V; ++v) {
+        c += (double)qr[v];
+        if (c > r) {
+          pick = v;
+          break;
+        }
+      }
+      d[qrow] = (int32_t)pick;
+      u[qrow] = (float)(synth_splitmix(ku, (uint64_t)qrow) >> 40) * 0x1p-24f;
+    }
+    free(z);
+  }
+  for (int64_t s = 0; s < S; ++s) U[s] = synth_splitmix(kU, (uint64_t)s);
 }

@@ -24,6 +24,7 @@ HOST_LIB = os.path.join(_HERE, "libsynth.so")
 DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
 
 ID_X, ID_LOGITS, ID_W13, ID_W2, ID_WROUTER, ID_WDENSE = 0, 1, 2, 3, 4, 5
+ID_VERIFY_Z, ID_VERIFY_N, ID_VERIFY_D, ID_VERIFY_U, ID_VERIFY_R = 6, 7, 8, 9, 10
 W_SIGMA = 0.02
 
 
@@ -60,6 +61,10 @@ def _host_lib():
         lib.synth_fill_x_bf16.argtypes = [u64, i64, i64, ctypes.c_void_p]
         lib.synth_fill_bf16.restype = None
         lib.synth_fill_bf16.argtypes = [u64, u32, u64, u64, ctypes.c_float, ctypes.c_void_p]
+        lib.synth_fill_verify.restype = None
+        lib.synth_fill_verify.argtypes = [u64, i64, ctypes.c_int, i64, ctypes.c_float,
+                                          ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p,
+                                          ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.synth_fill_logits.restype = None
         lib.synth_fill_logits.argtypes = [u64, i64, i64, ctypes.c_int, ctypes.c_void_p]
         _host = lib
@@ -167,3 +172,18 @@ def dev_fill_normal_f32(seed: int, tensor_id: int, start: int, n: int, sigma: fl
                                               ctypes.c_void_p(dev_ptr), ctypes.c_void_p(stream))
     if rc != 0:
         raise RuntimeError(f"synth_dev_fill_normal_f32 failed ({rc})")
+
+
+def verify_inputs(seed: int, S: int, g: int, V: int, sigma_t: float = 3.0, sigma_n: float = 0.2):
+    """(p [S, g+1, V], q [S, g, V] fp32, draft [S, g] int32, u [S, g] fp32, U [S] uint64): the
+    probabilities and uniforms of a speculative verification (see synth_fill_verify).  The
+    default drafter noise accepts about 5.2 of 7 drafted tokens (6.2 emitted per round, near
+    the coding acceptance length the pages report)."""
+    p = np.empty((S, g + 1, V), dtype=np.float32)
+    q = np.empty((S, g, V), dtype=np.float32)
+    d = np.empty((S, g), dtype=np.int32)
+    u = np.empty((S, g), dtype=np.float32)
+    U = np.empty(S, dtype=np.uint64)
+    _host_lib().synth_fill_verify(seed, S, g, V, sigma_t, sigma_n,
+                                  *(a.ctypes.data_as(ctypes.c_void_p) for a in (p, q, d, u, U)))
+    return p, q, d, u, U

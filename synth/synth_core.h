@@ -49,6 +49,11 @@
 #define SYNTH_ID_W2 3u
 #define SYNTH_ID_WROUTER 4u
 #define SYNTH_ID_WDENSE 5u
+#define SYNTH_ID_VERIFY_Z 6u
+#define SYNTH_ID_VERIFY_N 7u
+#define SYNTH_ID_VERIFY_D 8u
+#define SYNTH_ID_VERIFY_U 9u
+#define SYNTH_ID_VERIFY_R 10u
 
 SYNTH_FN uint64_t synth_mix64(uint64_t z) {
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ULL;

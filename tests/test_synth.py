@@ -65,3 +65,15 @@ def test_router_and_dense_weight_draws(synth_mod):
                   dtype=np.float64) * 2.0 ** -16
     assert np.array_equal(d.ravel(), (np.float32(synth_mod.W_SIGMA) * zd.astype(np.float32)))
     assert synth_mod.router_sigma(6144) == 2.0 ** -7 and synth_mod.router_sigma(2048) == 2.0 ** -6
+
+
+def test_verify_inputs(synth_mod):
+    p, q, d, u, U = synth_mod.verify_inputs(3, 4, 7, 1000)
+    assert p.shape == (4, 8, 1000) and q.shape == (4, 7, 1000)
+    np.testing.assert_allclose(p.sum(axis=2), 1.0, atol=1e-5)
+    np.testing.assert_allclose(q.sum(axis=2), 1.0, atol=1e-5)
+    assert ((d >= 0) & (d < 1000)).all()
+    assert ((u >= 0) & (u < 1)).all() and np.array_equal(u * 2.0 ** 24, np.floor(u * 2.0 ** 24))
+    assert U[0] == synth_mod.splitmix_out(synth_mod.splitmix_out(3, synth_mod.ID_VERIFY_R + 1), 0)
+    again = synth_mod.verify_inputs(3, 4, 7, 1000)
+    assert all(np.array_equal(a, b) for a, b in zip((p, q, d, u, U), again))

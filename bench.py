@@ -304,7 +304,8 @@ def _time_cold(fn, steps, flush_buf):
 
 def measure_next_rows(pk, flush_buf):
     """The steps beside the layer: the router (split-K bf16 GEMM + top-k), the layer with the
-    router in front, and a dense MXFP8 projection (K = N = 6144), each against its roofline."""
+    router in front, a dense MXFP8 projection (K = N = 6144) and the rejection-sampling
+    verification of the drafted block, each against its roofline."""
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
     from synth import layers as LY
@@ -345,6 +346,22 @@ def measure_next_rows(pk, flush_buf):
             "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
             "tflops": fl / (us * 1e-6) / 1e12,
             "tensor_frac_fp8": fl / (us * 1e-6) / 1e12 / (2.0 * bf16_tf)}
+    # rejection-sampling verification: 32 sequences (T = 256 verify tokens) x 7 drafts + 1
+    Sq, g, V = 32, 7, 152064
+    pv, qv, dv, uv, Uv = S.verify_inputs(1, Sq, g, V)
+    tens = [torch.from_numpy(a).cuda() for a in (pv, qv, dv, uv)]
+    Ut = torch.from_numpy(Uv.view(np.int64)).cuda()
+    n_acc = torch.empty(Sq, dtype=torch.int32, device="cuda")
+    tok = torch.empty((Sq, g + 1), dtype=torch.int32, device="cuda")
+    us = _time_cold(lambda: moe.moe_verify_block(*tens, Ut, Sq, g, V, n_acc, tok), 50, flush_buf)
+    rows = int(sum(2 if a < g else 1 for a in n_acc.cpu().numpy()))
+    byt = rows * V * 4 + Sq * g * 16 + Sq * (g + 2) * 4
+    rep["verify_s32_g7"] = {
+        "shape": f"S={Sq} sequences x {g} drafted tokens (+1), V={V}; drafter accepting "
+                 f"{float(n_acc.float().mean()):.2f} of {g}",
+        "us_cold": us, "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
+        "note": "bytes: the row(s) each sequence's outcome reads (2 after a rejection, else 1)"}
+    del tens, pv, qv
     L = LY.LAYERS["full_t256"]
     x = torch.from_numpy(LY.host_x(L).view(np.int16)).view(torch.bfloat16).cuda()
     lg = torch.from_numpy(LY.host_logits(L)).cuda()

@@ -304,6 +304,37 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
                           int T, int K, int N, void* y_bf16, cudaStream_t stream);
 
 /*
+ * moe_verify_block — rejection-sampling verification of a block of drafted
+ * tokens per sequence, the step after the verify forward (lossless
+ * speculative decoding: techllm.github.io, "Xiaomi MiMo and TileRT ...",
+ * section "2. DFlash"; blocks of at most 8 positions: dothoosh.com, section
+ * "جزئیات پیاده‌سازی DFlash").  For sequence s:
+ *   drafted token d_i (i = 0..g-1) is accepted while u_i * q_i(d_i) < p_i(d_i),
+ *   the fp32 values compared exactly (in fp64);
+ *   at the first rejection i one token is drawn from max(0, p_i - q_i) (fp32
+ *   difference), after g acceptances from p_g; if the residual has no mass,
+ *   from p_i.  A draw is the first token x whose running sum of fixed-point
+ *   masses floor(w * 2^62) exceeds floor(U[s] * M / 2^64), M the total mass:
+ *   bit-reproducible, independent of any summation order.
+ *  p       [S, g+1, V] fp32 target probabilities (rows of at most 2 total mass)
+ *  q       [S, g, V]   fp32 draft probabilities
+ *  draft   [S, g]      int32 drafted tokens (outside [0, V): a rejection and
+ *                      MOE_ERR_DEVICE_FAULT in the status word)
+ *  u       [S, g]      fp32 uniforms in [0, 1) for the accept tests
+ *  U       [S]         64-bit uniforms for the draw
+ *  n_acc   [S]         int32 out: accepted drafts, 0..g
+ *  tokens  [S, g+1]    int32 out: the accepted drafts, then the drawn token,
+ *                      then -1
+ * All device pointers, 4-byte aligned (U 8-byte); 1 <= g <= MOE_VERIFY_MAX_DRAFT,
+ * 1 <= V < 2^31, S >= 0 (0 = no-op).  Scratch from the library-owned cache.
+ * The random numbers are inputs: the call is deterministic.
+ */
+#define MOE_VERIFY_MAX_DRAFT 64
+int moe_verify_block(const float* p, const float* q, const int32_t* draft, const float* u,
+                     const uint64_t* U, int S, int g, int64_t V, int32_t* n_acc, int32_t* tokens,
+                     cudaStream_t stream);
+
+/*
  * moe_mxfp4_get_status — synchronizes `stream`, returns the first device-side
  * error recorded since the last call (MOE_OK if none) and clears it.  A CUDA
  * error seen while synchronizing returns MOE_ERR_CUDA.

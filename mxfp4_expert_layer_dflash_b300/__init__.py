@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
         L.mxfp8_quantize.restype = i
         L.moe_fp8_dense_forward.argtypes = [vp, vp, vp, i, i, i, vp, vp]
         L.moe_fp8_dense_forward.restype = i
+        L.moe_verify_block.argtypes = [vp, vp, vp, vp, vp, i, i, i64, vp, vp, vp]
+        L.moe_verify_block.restype = i
         L.moe_mxfp4_select_path.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_select_path.restype = i
         L.moe_mxfp4_workspace_size.argtypes = [i, i, i, i, i, i]
@@ -183,6 +185,13 @@ def moe_fp8_dense_forward(x_bf16, w_e4m3, w_e8m0, T, K, N, y_bf16, stream=None):
     return _check(lib().moe_fp8_dense_forward(_ptr(x_bf16), _ptr(w_e4m3), _ptr(w_e8m0), T, K, N,
                                               _ptr(y_bf16), _stream(stream)),
                   "moe_fp8_dense_forward")
+
+
+def moe_verify_block(p, q, draft, u, U, S, g, V, n_acc, tokens, stream=None):
+    """Rejection-sampling verification of a drafted block per sequence (see the header)."""
+    return _check(lib().moe_verify_block(_ptr(p), _ptr(q), _ptr(draft), _ptr(u), _ptr(U), S, g,
+                                         V, _ptr(n_acc), _ptr(tokens), _stream(stream)),
+                  "moe_verify_block")
 
 
 def moe_mxfp4_select_path(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:

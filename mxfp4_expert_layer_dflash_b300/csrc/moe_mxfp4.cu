@@ -25,6 +25,7 @@
 #include "gemm_tc.cuh"
 #include "quant.cuh"
 #include "route.cuh"
+#include "verify.cuh"
 
 namespace moe {
 
@@ -796,6 +797,48 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
     return MOE_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return MOE_OK;
+}
+
+int moe_verify_block(const float* p, const float* q, const int32_t* draft, const float* u,
+                     const uint64_t* U, int S, int g, int64_t V, int32_t* n_acc, int32_t* tokens,
+                     cudaStream_t stream) {
+  if (!p || !q || !draft || !u || !U || !n_acc || !tokens) return MOE_ERR_INVALID_ARG;
+  if (S < 0 || g < 1 || g > MOE_VERIFY_MAX_DRAFT || V < 1 || V > INT32_MAX)
+    return MOE_ERR_INVALID_ARG;
+  if (!aligned(p, 4) || !aligned(q, 4) || !aligned(draft, 4) || !aligned(u, 4) ||
+      !aligned(U, 8) || !aligned(n_acc, 4) || !aligned(tokens, 4))
+    return MOE_ERR_ALIGNMENT;
+  if (S == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  // vocabulary ranges per sequence: about two CTAs per SM, ranges of >= 2048
+  int chunks = std::max(1, std::min(kVerifyMaxChunks, (2 * d->sms + S - 1) / S));
+  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, (V + 2047) / 2048));
+  const int64_t chunk_len = (V + chunks - 1) / chunks;
+  const size_t part_bytes = align256((size_t)S * chunks * 8);
+  void* ws = nullptr;
+  if ((rc = cached_workspace(d, part_bytes + (size_t)S * 4, &ws))) return rc;
+  VerifyParams P{};
+  P.p = p;
+  P.q = q;
+  P.draft = draft;
+  P.u = u;
+  P.U = U;
+  P.S = S;
+  P.g = g;
+  P.V = V;
+  P.chunks = chunks;
+  P.chunk_len = chunk_len;
+  P.part = static_cast<uint64_t*>(ws);
+  P.count = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + part_bytes);
+  P.n_acc = n_acc;
+  P.tokens = tokens;
+  P.status = d->status;
+  if (cudaMemsetAsync(P.count, 0, (size_t)S * 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  verify_kernel<<<S * chunks, kVerifyThreads, 0, stream>>>(P);
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  return launch_status();
 }
 
 int moe_mxfp4_get_status(cudaStream_t stream) {

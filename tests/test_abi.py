@@ -129,3 +129,14 @@ def test_next_rows_validate_on_host(moe):
                                       16384, None, ctypes.byref(o)) == -1
     assert (moe.moe_mxfp4_workspace_size_routed(256, 6144, 2048, 384, 8)
             > moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8))
+
+
+def test_verify_validates_on_host(moe):
+    L = moe.lib()
+    a = [256, 512, 768, 1024, 1280]
+    assert L.moe_verify_block(*a, 4, 0, 100, 1536, 1792, None) == -1       # g < 1
+    assert L.moe_verify_block(*a, 4, 65, 100, 1536, 1792, None) == -1      # g > 64
+    assert L.moe_verify_block(*a, 4, 7, 0, 1536, 1792, None) == -1         # V < 1
+    assert L.moe_verify_block(256, 512, 768, 1024, 1284, 4, 7, 100, 1536, 1792, None) == -3
+    assert L.moe_verify_block(*a, 0, 7, 100, 1536, 1792, None) == 0        # S = 0: no-op
+    assert L.moe_verify_block(None, 512, 768, 1024, 1280, 4, 7, 100, 1536, 1792, None) == -1

@@ -237,7 +237,8 @@ CONFIG_LAYERS = [("c0", "tiny"), ("c1", "mid_t8"), ("c2", "full_t8"), ("c3", "fu
 def measure_config(L, steps, flush_buf):
     """µs per layer of one config: hot (back-to-back forwards, L2 warm) and cold (L2
     flushed before each forward by writing a buffer twice its size; the forward alone is
-    timed with events around it), plus the routing's touched experts."""
+    timed with events around it), plus the routing's touched experts.  The forward is
+    replayed from a CUDA graph so that small layers are not timed by the host's enqueue."""
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
     from synth import layers as LY
@@ -254,25 +255,15 @@ def measure_config(L, steps, flush_buf):
 
     def fwd():
         moe.moe_mxfp4_forward(x, lg, *w, L.T, L.H, L.I, L.E, L.k, y)
-    for _ in range(5):
-        fwd()
-    torch.cuda.synchronize()
+    run, how = _replayable(fwd)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
     for _ in range(steps):
-        fwd()
+        run()
     b.record()
     torch.cuda.synchronize()
     hot_us = a.elapsed_time(b) / steps * 1e3
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(min(steps, 50))]
-    for e0, e1 in ev:
-        flush_buf.add_(1)
-        e0.record()
-        fwd()
-        e1.record()
-    torch.cuda.synchronize()
-    cold_us = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    cold_us, _ = _time_cold(fwd, min(steps, 50), flush_buf)
     if moe.moe_mxfp4_get_status() != 0:
         raise RuntimeError(f"device status error in config {L.name}")
     del w
@@ -280,26 +271,49 @@ def measure_config(L, steps, flush_buf):
     return {"layer": L.desc, "touched_experts": touched, "alg_bytes": b_layer,
             "path": {1: "multi", 2: "persistent"}[moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E,
                                                                              L.k)],
-            "us_hot": hot_us, "us_cold_l2_flushed": cold_us,
+            "us_hot": hot_us, "us_cold_l2_flushed": cold_us, "issued_as": how,
             "tokens_per_s_cold": L.T / (cold_us * 1e-6),
             "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9}
 
 
-def _time_cold(fn, steps, flush_buf):
-    """median µs of fn() with L2 flushed before each call (events around the call only)"""
+def _replayable(fn):
+    """fn captured once in a CUDA graph (after warm-up calls: scratch grown, one-time set-up
+    done), so that timing sees the device work and not the host's enqueue cost of a call of a
+    few microseconds; returns (callable, "graph"), or (fn, "eager") if capture fails."""
     import torch
-    for _ in range(3):
-        fn()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            fn()
+    torch.cuda.current_stream().wait_stream(side)
     torch.cuda.synchronize()
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay, "graph"
+    except Exception as e:  # noqa: BLE001 - fall back to plain calls, and say so
+        log(f"[bench] graph capture failed ({e}); timing plain calls")
+        torch.cuda.synchronize()
+        return fn, "eager"
+
+
+def _time_cold(fn, steps, flush_buf):
+    """median µs of one call with L2 flushed before each (events around the call only),
+    and how the call was issued ("graph" replay or "eager")"""
+    import torch
+    run, how = _replayable(fn)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for e0, e1 in ev:
         flush_buf.add_(1)
         e0.record()
-        fn()
+        run()
         e1.record()
     torch.cuda.synchronize()
-    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3
+    return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3, how
 
 
 def measure_next_rows(pk, flush_buf):
@@ -320,11 +334,13 @@ def measure_next_rows(pk, flush_buf):
             torch.bfloat16).cuda()
         idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
         gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
-        us = _time_cold(lambda: moe.moe_router_topk(x, w, T, H, E, k, idx, gate), 50, flush_buf)
+        us, how = _time_cold(lambda: moe.moe_router_topk(x, w, T, H, E, k, idx, gate), 50,
+                             flush_buf)
         byt = E * H * 2 + T * H * 2 + T * k * 8
         fl = 2.0 * T * H * E
         rep[f"router_t{T}"] = {
             "shape": f"T={T} H={H} E={E} top-{k}, bf16 router weights", "us_cold": us,
+            "issued_as": how,
             "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
             "tflops": fl / (us * 1e-6) / 1e12, "tensor_frac_bf16": fl / (us * 1e-6) / 1e12 / bf16_tf}
     for T in (8, 256):
@@ -338,11 +354,13 @@ def measure_next_rows(pk, flush_buf):
         moe.mxfp8_quantize(wf, N, K, codes, sc)
         del wf
         y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
-        us = _time_cold(lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y), 50, flush_buf)
+        us, how = _time_cold(lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y), 50,
+                             flush_buf)
         byt = N * K + N * K // 32 + T * K * 2 + T * N * 2
         fl = 2.0 * T * K * N
         rep[f"dense_fp8_t{T}"] = {
             "shape": f"T={T} K={K} N={N}, MXFP8 weights and activations", "us_cold": us,
+            "issued_as": how,
             "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
             "tflops": fl / (us * 1e-6) / 1e12,
             "tensor_frac_fp8": fl / (us * 1e-6) / 1e12 / (2.0 * bf16_tf)}
@@ -353,13 +371,15 @@ def measure_next_rows(pk, flush_buf):
     Ut = torch.from_numpy(Uv.view(np.int64)).cuda()
     n_acc = torch.empty(Sq, dtype=torch.int32, device="cuda")
     tok = torch.empty((Sq, g + 1), dtype=torch.int32, device="cuda")
-    us = _time_cold(lambda: moe.moe_verify_block(*tens, Ut, Sq, g, V, n_acc, tok), 50, flush_buf)
+    us, how = _time_cold(lambda: moe.moe_verify_block(*tens, Ut, Sq, g, V, n_acc, tok), 50,
+                         flush_buf)
     rows = int(sum(2 if a < g else 1 for a in n_acc.cpu().numpy()))
     byt = rows * V * 4 + Sq * g * 16 + Sq * (g + 2) * 4
     rep["verify_s32_g7"] = {
         "shape": f"S={Sq} sequences x {g} drafted tokens (+1), V={V}; drafter accepting "
                  f"{float(n_acc.float().mean()):.2f} of {g}",
-        "us_cold": us, "alg_bytes": byt, "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
+        "us_cold": us, "issued_as": how, "alg_bytes": byt,
+        "hbm_frac": byt / (us * 1e-6) / 1e9 / hbm,
         "note": "bytes: the row(s) each sequence's outcome reads (2 after a rejection, else 1)"}
     del tens, pv, qv
     L = LY.LAYERS["full_t256"]
@@ -369,12 +389,12 @@ def measure_next_rows(pk, flush_buf):
     w_r = torch.from_numpy(S.router_bf16(L.seed, L.E, L.H).view(np.int16)).view(
         torch.bfloat16).cuda()
     y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
-    us_r = _time_cold(lambda: moe.moe_mxfp4_forward_routed(x, w_r, *wts, L.T, L.H, L.I, L.E, L.k,
-                                                           y), 20, flush_buf)
-    us_l = _time_cold(lambda: moe.moe_mxfp4_forward(x, lg, *wts, L.T, L.H, L.I, L.E, L.k, y), 20,
-                      flush_buf)
+    us_r, how = _time_cold(lambda: moe.moe_mxfp4_forward_routed(x, w_r, *wts, L.T, L.H, L.I,
+                                                                L.E, L.k, y), 20, flush_buf)
+    us_l, _ = _time_cold(lambda: moe.moe_mxfp4_forward(x, lg, *wts, L.T, L.H, L.I, L.E, L.k, y),
+                         20, flush_buf)
     rep["routed_layer_t256"] = {"shape": L.desc + ", router in front", "us_cold": us_r,
-                                "us_cold_layer_on_given_logits": us_l}
+                                "us_cold_layer_on_given_logits": us_l, "issued_as": how}
     if moe.moe_mxfp4_get_status() != 0:
         raise RuntimeError("device status error in the next-rows report")
     del wts

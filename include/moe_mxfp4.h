@@ -326,7 +326,8 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
  *  tokens  [S, g+1]    int32 out: the accepted drafts, then the drawn token,
  *                      then -1
  * All device pointers, 4-byte aligned (U 8-byte); 1 <= g <= MOE_VERIFY_MAX_DRAFT,
- * 1 <= V < 2^31, S >= 0 (0 = no-op).  Scratch from the library-owned cache.
+ * 1 <= V <= 2^21 (MOE_ERR_UNSUPPORTED_SHAPE above), S >= 0 (0 = no-op).
+ * Scratch from the library-owned cache.
  * The random numbers are inputs: the call is deterministic.
  */
 #define MOE_VERIFY_MAX_DRAFT 64

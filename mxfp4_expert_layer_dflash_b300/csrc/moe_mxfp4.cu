@@ -812,13 +812,12 @@ int moe_verify_block(const float* p, const float* q, const int32_t* draft, const
   DeviceState* d = nullptr;
   int rc = device_state(&d);
   if (rc) return rc;
-  // vocabulary ranges per sequence: about two CTAs per SM, ranges of >= 2048
-  int chunks = std::max(1, std::min(kVerifyMaxChunks, (2 * d->sms + S - 1) / S));
-  chunks = (int)std::max<int64_t>(1, std::min<int64_t>(chunks, (V + 2047) / 2048));
-  const int64_t chunk_len = (V + chunks - 1) / chunks;
+  if (V > (int64_t)kVerifyMaxChunks * kVerifyRange) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const int chunks = (int)((V + kVerifyRange - 1) / kVerifyRange);
   const size_t part_bytes = align256((size_t)S * chunks * 8);
+  const size_t count_bytes = align256((size_t)S * 4);
   void* ws = nullptr;
-  if ((rc = cached_workspace(d, part_bytes + (size_t)S * 4, &ws))) return rc;
+  if ((rc = cached_workspace(d, part_bytes + count_bytes + (size_t)S * 4, &ws))) return rc;
   VerifyParams P{};
   P.p = p;
   P.q = q;
@@ -829,14 +828,19 @@ int moe_verify_block(const float* p, const float* q, const int32_t* draft, const
   P.g = g;
   P.V = V;
   P.chunks = chunks;
-  P.chunk_len = chunk_len;
+  P.chunk_len = kVerifyRange;
   P.part = static_cast<uint64_t*>(ws);
   P.count = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(ws) + part_bytes);
+  int32_t* jpos = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + part_bytes + count_bytes);
   P.n_acc = n_acc;
   P.tokens = tokens;
   P.status = d->status;
-  if (cudaMemsetAsync(P.count, 0, (size_t)S * 4, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  verify_kernel<<<S * chunks, kVerifyThreads, 0, stream>>>(P);
+  verify_decide_kernel<<<(S + 7) / 8, 256, 0, stream>>>(P, jpos);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (launch_pdl(verify_draw_kernel, dim3(S * chunks), dim3(kVerifyDrawThreads), 0, stream, P,
+                 (const int32_t*)jpos) != cudaSuccess)
+    return MOE_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   return launch_status();
 }

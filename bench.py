@@ -402,6 +402,58 @@ def measure_next_rows(pk, flush_buf):
     return rep
 
 
+ROWS = ("router_t8", "router_t256", "dense_fp8_t8", "dense_fp8_t256", "verify_s32_g7")
+
+
+def run_row(args):
+    """One call beside the layer, --warmup then --steps times back to back (a small, fixed
+    command for profilers); prints its mean µs.  Not the benchmark's contract line."""
+    import torch
+    import mxfp4_expert_layer_dflash_b300 as moe
+    from synth import synth as S
+    name = args.row
+    if name.startswith("router"):
+        T, H, E, k = int(name[len("router_t"):]), 6144, 384, 8
+        x = torch.from_numpy(S.x_bf16(100 + T, T, H).view(np.int16)).view(torch.bfloat16).cuda()
+        w = torch.from_numpy(S.router_bf16(100 + T, E, H).view(np.int16)).view(
+            torch.bfloat16).cuda()
+        idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
+        gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
+        fn = lambda: moe.moe_router_topk(x, w, T, H, E, k, idx, gate)  # noqa: E731
+    elif name.startswith("dense"):
+        T, K, N = int(name[len("dense_fp8_t"):]), 6144, 6144
+        x = torch.from_numpy(S.x_bf16(200 + T, T, K).view(np.int16)).view(torch.bfloat16).cuda()
+        wf = torch.empty((N, K), dtype=torch.float32, device="cuda")
+        S.dev_fill_normal_f32(200 + T, S.ID_WDENSE, 0, N * K, S.W_SIGMA, wf.data_ptr(),
+                              torch.cuda.current_stream().cuda_stream)
+        codes = torch.empty((N, K), dtype=torch.uint8, device="cuda")
+        sc = torch.empty((N, K // 32), dtype=torch.uint8, device="cuda")
+        moe.mxfp8_quantize(wf, N, K, codes, sc)
+        del wf
+        y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y)  # noqa: E731
+    else:
+        Sq, g, V = 32, 7, 152064
+        pv, qv, dv, uv, Uv = S.verify_inputs(1, Sq, g, V)
+        tens = [torch.from_numpy(a).cuda() for a in (pv, qv, dv, uv)]
+        Ut = torch.from_numpy(Uv.view(np.int64)).cuda()
+        n_acc = torch.empty(Sq, dtype=torch.int32, device="cuda")
+        tok = torch.empty((Sq, g + 1), dtype=torch.int32, device="cuda")
+        fn = lambda: moe.moe_verify_block(*tens, Ut, Sq, g, V, n_acc, tok)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError(f"device status error in row {name}")
+    print(json.dumps({"row": name, "us_per_call_back_to_back": a.elapsed_time(b) / args.steps * 1e3}))
+
+
 def run_ours(args, L, rank, world, local_rank):
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
@@ -598,6 +650,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layer", default="full_t256")
     ap.add_argument("--path", choices=sorted(PATHS), default="auto")
+    ap.add_argument("--row", choices=ROWS, default=None,
+                    help="only run one call beside the layer (a profiling command)")
     ap.add_argument("--cpu-tokens", type=int, default=32)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -611,7 +665,9 @@ def main():
     rank = int(os.environ.get("RANK", 0))
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
-    if args.impl == "reference":
+    if args.row:
+        run_row(args)
+    elif args.impl == "reference":
         run_reference(args, L, rank)
     else:
         run_ours(args, L, rank, world, local_rank)

@@ -116,7 +116,8 @@ typedef struct {
    * step_events[i] on `stream` just before the i-th kernel of the call and one
    * more after the last (i < n_step_events).  Kernel order: multi path —
    * route_topk, route_permute, act_quant, gemm1, gemm2, combine; persistent
-   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine. */
+   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine.
+   * moe_mxfp4_forward_routed puts router_gemm, router_reduce first. */
   cudaEvent_t* step_events;
   int n_step_events;
 } moe_opts;

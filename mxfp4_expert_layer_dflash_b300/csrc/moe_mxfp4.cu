@@ -21,7 +21,7 @@
 #include "common.cuh"
 #include "dense_tc.cuh"
 #include "fmt.cuh"
-#include "gemm_simt.cuh"
+#include "gemm_bf16.cuh"
 #include "gemm_tc.cuh"
 #include "quant.cuh"
 #include "route.cuh"
@@ -207,7 +207,11 @@ int device_state(DeviceState** out) {
                              (int)DenseCfg<kDenseBf16, kRouterNMax>::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(dense_tc_kernel<kDenseMxf8, kDenseNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)DenseCfg<kDenseMxf8, kDenseNMax>::kSmem) != cudaSuccess)
+                             (int)DenseCfg<kDenseMxf8, kDenseNMax>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kBfSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kBfSmem) != cudaSuccess)
       return MOE_ERR_CUDA;
     d.ready = true;
   }
@@ -234,7 +238,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // 2D row-major map: `inner` elements per row, `rows` rows, `stride` bytes
 // between rows, box of box_inner x box_rows, 128-byte swizzle
 int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
-             uint64_t rows, uint64_t stride, uint32_t box_inner, uint32_t box_rows) {
+             uint64_t rows, uint64_t stride, uint32_t box_inner, uint32_t box_rows,
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto enc = tensor_map_encoder();
   if (!enc) return MOE_ERR_CUDA;
   const cuuint64_t dims[2] = {inner, rows};
@@ -242,7 +247,7 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -572,17 +577,49 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
       if (launch(kModeGemm2, p) != cudaSuccess) return MOE_ERR_CUDA;
     }
   } else {
-    const int ggrid = d->sms * 4;
+    // bf16 activations: weights decoded to bf16 in TMEM, kind::f16 MMA
+    BfParams b1{}, b2{};
+    if ((rc = make_map(&b1.map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w13, H / 2, (uint64_t)E * 2 * I,
+                       H / 2, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) ||
+        (rc = make_map(&b1.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.xq, H, TK, (uint64_t)H * 2,
+                       64, 16)) ||
+        (rc = make_map(&b2.map_w, CU_TENSOR_MAP_DATA_TYPE_UINT8, w2, I / 2, (uint64_t)E * H, I / 2,
+                       64, 128, CU_TENSOR_MAP_SWIZZLE_64B)) ||
+        (rc = make_map(&b2.map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w.hq, I, TK, (uint64_t)I * 2,
+                       64, 16)))
+      return rc;
+    for (BfParams* b : {&b1, &b2}) {
+      b->chunks = reinterpret_cast<const int4*>(w.chunks);
+      b->meta = w.meta;
+      b->status = d->status;
+      b->timeout_ns = timeout_ns;
+    }
+    b1.w_sf = w13s;
+    b1.hq = reinterpret_cast<uint16_t*>(w.hq);
+    b1.K = H;
+    b1.R = 2 * I;
+    b1.m_tiles = I / 128;
+    b1.m_stride = 128;
+    b1.half = I;
+    b1.out_dim = I;
+    b1.rows_total = E * 2 * I;
+    b2.w_sf = w2s;
+    b2.yp = w.yp;
+    b2.K = I;
+    b2.R = H;
+    b2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
+    b2.m_stride = 256;
+    b2.half = 128;
+    b2.out_dim = H;
+    b2.rows_total = E * H;
     st.mark();
-    if (launch_pdl(gemm1_simt_kernel<MOE_ACT_BF16>, dim3(ggrid), dim3(128), 0, stream, w13, w13s,
-                   (const uint8_t*)w.xq, (const uint8_t*)w.xs, (const int4*)w.chunks,
-                   (const int32_t*)w.meta, H, I, w.hq, w.hs) != cudaSuccess)
+    if (launch_pdl(gemm_bf16_kernel<true>, dim3(d->sms), dim3(kBfThreads), kBfSmem, stream, b1) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
     st.launched();
     st.mark();
-    if (launch_pdl(gemm2_simt_kernel<MOE_ACT_BF16>, dim3(ggrid), dim3(128), 0, stream, w2, w2s,
-                   (const uint8_t*)w.hq, (const uint8_t*)w.hs, (const int4*)w.chunks,
-                   (const int32_t*)w.meta, H, I, w.yp) != cudaSuccess)
+    if (launch_pdl(gemm_bf16_kernel<false>, dim3(d->sms), dim3(kBfThreads), kBfSmem, stream, b2) !=
+        cudaSuccess)
       return MOE_ERR_CUDA;
     st.launched();
   }

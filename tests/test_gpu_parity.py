@@ -270,14 +270,51 @@ def test_deterministic_and_permutation_equivariant(O, act):
     assert torch.equal(yp.view(torch.int16), y1[p].view(torch.int16))
 
 
-def test_power_of_two_scale_plumbing(O):
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+def test_power_of_two_scale_plumbing(O, act):
     L = LY.LAYERS["tiny"]
     inp = device_layer(L)
-    y1 = gpu_forward(L, inp).float()
+    y1 = gpu_forward(L, inp, act_mode=act).float()
     s2 = (inp[5] + 1)
-    y2 = gpu_forward(L, inp[:5] + (s2,)).float()
+    y2 = gpu_forward(L, inp[:5] + (s2,), act_mode=act).float()
     assert torch.equal(y2, 2 * y1)
     s13 = inp[3].clone()
     s13[:, L.I:] += 1
-    y3 = gpu_forward(L, inp[:3] + (s13,) + inp[4:]).float()
+    y3 = gpu_forward(L, inp[:3] + (s13,) + inp[4:], act_mode=act).float()
     assert torch.equal(y3, 2 * y1)
+
+
+# E8M0 codes across the range a quantiser of fp32 weights can emit (0..252), one per K block
+EXTREME_CODES = [0, 1, 2, 3, 60, 125, 126, 127, 128, 129, 130, 131, 190, 240, 248, 252]
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+def test_extreme_scale_codes(O, act):
+    """Every K block of W13 gets one extreme scale code; token t has activations only in block
+    t % 16, sized by 2^(124 - code) (kept >= 2^-106) so the layer stays finite.  Blocks a token
+    does not touch still meet zeros: a decode that overflowed would turn them into NaN."""
+    T, H, I, E, k = 32, 512, 256, 4, 2
+    L, _, lg, w = _layer_inputs(O, T, H, I, E, k, 77)
+    w13, s13, w2, s2 = (a.copy() for a in w)
+    s13[...] = np.array(EXTREME_CODES, np.uint8)
+    rng = np.random.default_rng(5)
+    xf = np.zeros((T, H), np.float32)
+    for t in range(T):
+        j = t % 16
+        xf[t, 32 * j:32 * j + 32] = rng.standard_normal(32) * 2.0 ** max(124 - EXTREME_CODES[j],
+                                                                         -106)
+    x = torch.from_numpy(xf).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_mxfp4_forward_ex(dev(x), dev(lg), dev(w13), dev(s13), dev(w2), dev(s2), T, H, I, E, k,
+                             y, act_mode=act)
+    assert moe.moe_mxfp4_get_status() == 0
+    yg = bf16_to_f64(host_bf16(y))
+    assert np.isfinite(yg).all()
+    mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_EXACT
+    _, yref, _ = O.moe_forward(x, lg, w13, s13, w2, s2, k, mode)
+    for t in range(T):                                      # per token: magnitudes differ widely
+        if act == moe.MOE_ACT_MXFP8:
+            assert rel_fro(yg[t], yref[t]) <= MXFP8_FRO
+            assert max_err_over_rms(yg[t], yref[t]) <= MXFP8_MAX
+        else:
+            assert rel_fro(yg[t], yref[t]) <= BF16_FRO

@@ -10,15 +10,18 @@
 //   producer (warp 0)   TMA of the two packed FP4 tiles (128 rows x 64 bytes,
 //                       64-byte swizzle) and of the bf16 activation tile (two
 //                       128-byte-swizzled halves of 64 elements)
-//   decoders (warps 4-11, one per tile and TMEM lane quarter; lane = weight row)
-//                       read their row's 64 packed bytes, decode the 128 values
-//                       exactly to bf16 and store them into TMEM with one
-//                       tcgen05.st (A in TMEM: row m on lane m, element k at
-//                       column k/2, even k in the low half — established by a
-//                       device probe)
-//   MMA (warp 2)        16 x tcgen05.mma.kind::f16 (K = 16) per stage, A from
+//   MMA (warp 1)        16 x tcgen05.mma.kind::f16 (K = 16) per stage, A from
 //                       TMEM, B from shared memory
-//   epilogue (12-15)    silu(gate) * up -> bf16 h (GEMM1) or fp32 rows (GEMM2)
+//   epilogue (4-7)      silu(gate) * up -> bf16 h (GEMM1) or fp32 rows (GEMM2)
+//   decoders (8-23)     one per tile, TMEM lane quarter and half of the stage's
+//                       K (lane = weight row): read the row's 32 packed bytes,
+//                       decode the 64 values exactly to bf16 and store them into
+//                       TMEM with one tcgen05.st (A in TMEM: row m on lane m,
+//                       element k at column k/2, even k in the low half —
+//                       established by a device probe).  Four decoder warps per
+//                       scheduler hide each other's shared-memory and TMEM
+//                       latencies; three decoded buffers let decode run ahead of
+//                       the MMA.
 // Decode: the bits (m << 6) | (sign << 15) of an E2M1 code with magnitude m
 // are, read as bf16, exactly e2m1 * 2^-126 (m = 1 lands on the subnormal
 // 2^-127 = 0.5 * 2^-126); one bf16 multiply by 2^(c-1) (two, by 2^126 and
@@ -34,13 +37,14 @@
 
 namespace moe {
 
-constexpr int kBfThreads = 512;        // 16 warps
+constexpr int kBfThreads = 768;        // 24 warps
+constexpr int kBfDecoders = 16;        // decoder warps (8..23)
 constexpr int kBfNMax = kChunkNarrow;  // tokens per item (bf16 mode uses narrow chunks)
 constexpr int kBfPackedTile = 128 * 64;                // 128 rows x 128 FP4 (packed)
 constexpr int kBfBHalf = kBfNMax * 128;                // kBfNMax rows x 64 bf16
 constexpr int kBfStageBytes = 2 * kBfPackedTile + 2 * kBfBHalf;
 constexpr int kBfStages = (232448 - 1024 - 256) / kBfStageBytes;
-constexpr int kBfDecBufs = 2;                          // decoded-A buffers in TMEM
+constexpr int kBfDecBufs = 3;                          // decoded-A buffers in TMEM
 constexpr int kBfAccCols = 2 * kBfNMax;                // gate|up (or lo|hi) accumulators
 constexpr int kBfDecCol0 = 2 * kBfAccCols;             // first TMEM column of decoded A
 constexpr int kBfDecCols = 2 * 64;                     // two tiles x 64 columns (128 bf16)
@@ -105,23 +109,27 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// One weight row's 128 values of a stage, decoded and stored to TMEM.
+// 64 values of one weight row (two E8M0 blocks), decoded and stored to TMEM.
 // Packed byte i holds elements 2i (low nibble) and 2i+1 (high nibble).  For a
 // 32-bit word of 8 codes, e / o hold the even / odd codes one per byte; the
 // permute puts code 2j in bits 0-3 and code 2j+1 in bits 16-19 with zero bytes
 // between, the multiply by 0x1040 copies each code to bits 6-9 and 12-15 (no
 // overlap, so no carries), and the mask keeps the magnitude at 6-8 and the
 // sign at 15: the bf16 bits of e2m1 * 2^-126.
-__device__ __forceinline__ void bf_decode_row(const uint4 (&packed)[4], uint32_t scale_word,
-                                              uint32_t taddr) {
-  uint32_t out[2][32];
+// kTwoStep: some code of the pair exceeds 128, where 2^(c-1) is not a bf16;
+// those blocks multiply by 2^126 and then by 2^(c-127) (exact: the first
+// product is the e2m1 value itself).
+template <bool kTwoStep>
+__device__ __forceinline__ void bf_decode_half(const uint4 (&packed)[2], uint32_t scale_pair,
+                                               uint32_t taddr) {
+  uint32_t out[32];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {  // 32 values per E8M0 block
-    const uint32_t c = (scale_word >> (8 * j)) & 0xFFu;
-    const bool one_step = c <= 128;  // 2^(c-1) is a normal bf16
+  for (int j = 0; j < 2; ++j) {  // 32 values per E8M0 block
+    const uint32_t c = (scale_pair >> (8 * j)) & 0xFFu;
+    const bool one_step = !kTwoStep || c <= 128;  // 2^(c-1) is a normal bf16
     const uint32_t e1 = one_step ? c + 126 : 253;  // 2^(c-1), or 2^126 then 2^(c-127)
     const uint32_t f1 = (e1 << 7) * 0x00010001u;
-    const uint32_t f2 = (c << 7) * 0x00010001u;
+    const uint32_t f2 = one_step ? 0x3F803F80u : (c << 7) * 0x00010001u;  // 1.0 or 2^(c-127)
     const uint32_t w[4] = {packed[j].x, packed[j].y, packed[j].z, packed[j].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -130,14 +138,12 @@ __device__ __forceinline__ void bf_decode_row(const uint4 (&packed)[4], uint32_t
       for (int b = 0; b < 4; ++b) {
         const uint32_t q = prmt(e, o, 0x8080u | (uint32_t)b | ((uint32_t)(4 + b) << 8));
         uint32_t v = bf16x2_mul((q * 0x1040u) & 0x81C081C0u, f1);
-        if (!one_step) v = bf16x2_mul(v, f2);
-        const int word = j * 16 + i * 4 + b;  // output column: elements 2*word, 2*word+1
-        out[word >> 5][word & 31] = v;
+        if (kTwoStep) v = bf16x2_mul(v, f2);
+        out[j * 16 + i * 4 + b] = v;  // column: elements 2*word, 2*word+1 of the half
       }
     }
   }
-  tmem_st_x32(taddr, out[0]);
-  tmem_st_x32(taddr + 32, out[1]);
+  tmem_st_x32(taddr, out);
 }
 
 template <bool kGated>
@@ -159,10 +165,10 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
   if (threadIdx.x == 0) {
     for (int s = 0; s < kBfStages; ++s) {
       ptx::mbar_init(&full[s], 1);       // TMA arrive.expect_tx
-      ptx::mbar_init(&empty[s], 1 + 8);  // MMA commit (B read) + 8 decoder warps (A read)
+      ptx::mbar_init(&empty[s], 1 + kBfDecoders);  // MMA commit (B read) + decoders (A read)
     }
     for (int d = 0; d < kBfDecBufs; ++d) {
-      ptx::mbar_init(&dec_full[d], 8);   // 8 decoder warps
+      ptx::mbar_init(&dec_full[d], kBfDecoders);
       ptx::mbar_init(&dec_empty[d], 1);  // MMA commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
-  if (warp == 2) {
+  if (warp == 1) {
     ptx::tmem_alloc(tmem_slot, 512);
     ptx::tmem_relinquish();
   }
@@ -194,9 +200,8 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
     set_status(p.status, code);
     *abort_flag = 1;
   };
-  auto deadline = [&]() { return ptx::globaltimer() + p.timeout_ns; };
   auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
+    return __all_sync(0xffffffffu, ptx::mbar_wait_for(bar, parity, p.timeout_ns, abort_flag));
   };
 
   if (warp == 0) {
@@ -230,7 +235,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
       }
     }
     grid_launch_dependents();
-  } else if (warp == 2) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     uint32_t fill = 0;
     bool ok = true;
@@ -278,56 +283,67 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
     }
     ptx::mma_commit_warp(drain);
     if (!wait_all(drain, 0) && lane == 0) fail(kStatusTimeout);
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp >= 8) {
     // ------------------------------------------------------------ decoders
-    const int t = (warp - 4) >> 2, q = warp & 3;
+    const int t = ((warp - 8) >> 2) & 1, q = warp & 3, kh = (warp - 8) >> 3;
     const int r = q * 32 + lane;  // row within the tile = TMEM lane
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const int sf_row = p.K / 32;
     // this CTA's stages: ksteps per item, items blockIdx.x, + gridDim.x, ...
     const int my_items = blockIdx.x < items ? (items - 1 - blockIdx.x) / gridDim.x + 1 : 0;
     const uint32_t n_fills = (uint32_t)my_items * (uint32_t)ksteps;
-    // scale words kRing fills ahead (one 32-bit word per row and stage)
+    // scale pairs kRing fills ahead (this row's two E8M0 codes of the stage
+    // half); the row pointer is found once per item and then advances 4 bytes
+    // a stage
     constexpr int kRing = 4;
     uint32_t sw[kRing];
-    int ld_item = blockIdx.x, ld_ks = 0;
+    int ld_item = blockIdx.x - (int)gridDim.x, ld_left = 0;
+    const uint16_t* ld_ptr = nullptr;
     auto load_sw = [&](uint32_t& dst) {
-      dst = 0;
-      if (ld_item < items) {
-        const int4 ch = p.chunks[ld_item / p.m_tiles];
-        const int64_t row = (int64_t)ch.x * p.R + (ld_item % p.m_tiles) * p.m_stride +
-                            t * p.half + r;
-        if (row < p.rows_total)
-          dst = __ldg(reinterpret_cast<const uint32_t*>(p.w_sf + row * sf_row + ld_ks * 4));
-        if (++ld_ks == ksteps) {
-          ld_ks = 0;
-          ld_item += gridDim.x;
+      if (ld_left == 0) {
+        ld_item += gridDim.x;
+        ld_left = ksteps;
+        ld_ptr = nullptr;
+        if (ld_item < items) {
+          const int4 ch = p.chunks[ld_item / p.m_tiles];
+          const int64_t row = (int64_t)ch.x * p.R + (ld_item % p.m_tiles) * p.m_stride +
+                              t * p.half + r;
+          if (row < p.rows_total)
+            ld_ptr = reinterpret_cast<const uint16_t*>(p.w_sf + row * sf_row + kh * 2);
         }
       }
+      dst = ld_ptr ? __ldg(ld_ptr) : 0u;
+      if (ld_ptr) ld_ptr += 2;
+      --ld_left;
     };
 #pragma unroll
     for (int i = 0; i < kRing; ++i) load_sw(sw[i]);
+    // per-lane constants: the row's two swizzled 16-byte chunks (64B swizzle:
+    // chunk c of a 64-byte row sits at c ^ ((r >> 1) & 3)) and its TMEM columns
+    const uint32_t off0 = t * kBfPackedTile + r * 64 + (((2 * kh) ^ ((r >> 1) & 3)) << 4);
+    const uint32_t off1 = t * kBfPackedTile + r * 64 + (((2 * kh + 1) ^ ((r >> 1) & 3)) << 4);
+    const uint32_t tcol0 = tbase + lane_off + kBfDecCol0 + t * 64 + kh * 32;
+    int s = 0, d = 0;
+    uint32_t full_par = 0, dec_par = 1;
     for (uint32_t fill = 0; fill < n_fills;) {
 #pragma unroll
       for (int i = 0; i < kRing; ++i, ++fill) {
         if (fill < n_fills) {
-          const int s = (int)(fill % kBfStages);
-          const uint32_t use = fill / kBfStages;
-          const int d = (int)(fill % kBfDecBufs);
-          const uint32_t duse = fill / kBfDecBufs;
-          if (!wait_all(&full[s], use & 1) || !wait_all(&dec_empty[d], (duse & 1) ^ 1)) {
+          if (!wait_all(&full[s], full_par) || !wait_all(&dec_empty[d], dec_par)) {
             if (lane == 0) fail(kStatusTimeout);
             fill = n_fills;
             break;
           }
           ptx::tc_fence_after();
-          // this row's 64 packed bytes: 16-byte chunk c at c ^ ((r >> 1) & 3) (64B swizzle)
-          const uint8_t* rowp = smem + s * kBfStageBytes + t * kBfPackedTile + r * 64;
-          uint4 pk[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            pk[c] = *reinterpret_cast<const uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4));
-          bf_decode_row(pk, sw[i], tbase + lane_off + kBfDecCol0 + d * kBfDecCols + t * 64);
+          const uint8_t* st = smem + s * kBfStageBytes;
+          uint4 pk[2];
+          pk[0] = *reinterpret_cast<const uint4*>(st + off0);
+          pk[1] = *reinterpret_cast<const uint4*>(st + off1);
+          const uint32_t taddr = tcol0 + d * kBfDecCols;
+          if (__all_sync(0xffffffffu, (sw[i] & 0xFFu) <= 128u && (sw[i] >> 8) <= 128u))
+            bf_decode_half<false>(pk, sw[i], taddr);
+          else
+            bf_decode_half<true>(pk, sw[i], taddr);
           ptx::tmem_st_wait();
           ptx::tc_fence_before();
           __syncwarp();
@@ -336,10 +352,18 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
             ptx::mbar_arrive(&empty[s]);
           }
           load_sw(sw[i]);
+          if (++s == kBfStages) {
+            s = 0;
+            full_par ^= 1;
+          }
+          if (++d == kBfDecBufs) {
+            d = 0;
+            dec_par ^= 1;
+          }
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
@@ -389,7 +413,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
-  if (warp == 2) ptx::tmem_dealloc(tbase, 512);
+  if (warp == 1) ptx::tmem_dealloc(tbase, 512);
 }
 
 }  // namespace moe

@@ -80,6 +80,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   return true;
 }
 
+// As mbar_wait, with the deadline taken `timeout_ns` after the first failed
+// try (no timer read when the phase has already completed).
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity,
+                                              unsigned long long timeout_ns,
+                                              const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait(bar, parity, globaltimer() + timeout_ns, abort);
+}
+
 // cp.async (4-byte, L1-allocating) with zero fill when src_bytes == 0
 __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gsrc, uint32_t src_bytes) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(smem_dst)),

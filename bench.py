@@ -6,6 +6,7 @@ layer (H=6144, I=2048, E=384, top-8), plus achieved HBM GB/s as a fraction of th
 B300 peak.  One JSON line on stdout (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--layer NAME]
+                  [--act mxfp8|bf16] [--path auto|multi|persistent]
 
 ours       K forward calls through the C ABI with all inputs resident in HBM (the 7.7 GB of
            packed weights exceed L2, so no L2 flush is needed), timed with CUDA events on the
@@ -178,9 +179,10 @@ class Events:
 
 # ------------------------------------------------------------------------- oracle leg
 
-def oracle_sample(L, n_tokens: int):
+def oracle_sample(L, n_tokens: int, act: str = "mxfp8"):
     """Prepare the oracle's inputs for the first n_tokens tokens (packing excluded from any
-    timing): returns a closure that runs the oracle on a list of token indices."""
+    timing): returns a closure that runs the oracle on a list of token indices (MXFP8
+    emulation for the mxfp8 mode, the exact fp64 layer for the bf16 mode)."""
     from oracle import oracle as O
     from synth import layers as LY
     x, lg = LY.host_x(L), LY.host_logits(L)
@@ -188,8 +190,10 @@ def oracle_sample(L, n_tokens: int):
     ridx, _ = O.route(lg[toks], L.k)
     w = LY.host_packed_weights(L, O.mxfp4_quantize, np.unique(ridx))
 
+    mode = O.ACT_MXFP8 if act == "mxfp8" else O.ACT_EXACT
+
     def run(tokens):
-        O.moe_forward(x, lg, *w, L.k, O.ACT_MXFP8, tokens=np.asarray(tokens, dtype=np.int64))
+        O.moe_forward(x, lg, *w, L.k, mode, tokens=np.asarray(tokens, dtype=np.int64))
     return run, int(np.unique(ridx).size)
 
 
@@ -205,7 +209,7 @@ def run_reference(args, L, rank):
         return
     n_tok = 8
     log(f"[reference] preparing oracle inputs for {n_tok} tokens of {L.name}")
-    run, n_exp = oracle_sample(L, n_tok)
+    run, n_exp = oracle_sample(L, n_tok, args.act)
     for i in range(args.warmup):
         run([i % n_tok])
     t0 = time.perf_counter()
@@ -215,13 +219,16 @@ def run_reference(args, L, rank):
     value = args.steps / dt
     cores = cpu_cores()
     sample = (f"one token per step (cycling through the first {n_tok} tokens of the layer, "
-              f"{n_exp} experts), fp64 oracle in MXFP8-emulation mode; MXFP4 packing excluded")
+              f"{n_exp} experts), fp64 oracle in "
+              f"{'MXFP8-emulation' if args.act == 'mxfp8' else 'exact'} mode; MXFP4 packing "
+              f"excluded")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{L.name}: {L.desc}", "parallelism": "host threads"},
+        "config": {"workload": f"{L.name}: {L.desc}", "parallelism": "host threads",
+                   "act_mode": args.act},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -255,6 +262,10 @@ def measure_config(L, steps, flush_buf):
 
     def fwd():
         moe.moe_mxfp4_forward(x, lg, *w, L.T, L.H, L.I, L.E, L.k, y)
+
+    def fwd_bf16():
+        moe.moe_mxfp4_forward_ex(x, lg, *w, L.T, L.H, L.I, L.E, L.k, y,
+                                 act_mode=moe.MOE_ACT_BF16)
     run, how = _replayable(fwd)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record()
@@ -264,6 +275,7 @@ def measure_config(L, steps, flush_buf):
     torch.cuda.synchronize()
     hot_us = a.elapsed_time(b) / steps * 1e3
     cold_us, _ = _time_cold(fwd, min(steps, 50), flush_buf)
+    bf16_us, _ = _time_cold(fwd_bf16, min(steps, 50), flush_buf)
     if moe.moe_mxfp4_get_status() != 0:
         raise RuntimeError(f"device status error in config {L.name}")
     del w
@@ -273,7 +285,8 @@ def measure_config(L, steps, flush_buf):
                                                                              L.k)],
             "us_hot": hot_us, "us_cold_l2_flushed": cold_us, "issued_as": how,
             "tokens_per_s_cold": L.T / (cold_us * 1e-6),
-            "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9}
+            "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9,
+            "bf16_mode_us_cold": bf16_us, "bf16_mode_hbm_gbs_cold": b_layer / (bf16_us * 1e-6) / 1e9}
 
 
 def _replayable(fn):
@@ -482,7 +495,8 @@ def run_ours(args, L, rank, world, local_rank):
     moe.moe_mxfp4_route(lg, L.T, L.E, L.k, tk[0], tk[1], cnt, *aux)
     touched, b_gemm1, b_gemm2, b_layer = layer_bytes(L, cnt.cpu().numpy())
 
-    path = PATHS[args.path] or moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E, L.k)
+    act = moe.MOE_ACT_BF16 if args.act == "bf16" else moe.MOE_ACT_MXFP8
+    path = PATHS[args.path] or moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E, L.k, act)
     names = STEP_NAMES[path]
     ev = Events()
     nsteps = len(names) + 1
@@ -490,7 +504,7 @@ def run_ours(args, L, rank, world, local_rank):
 
     def fwd(step_events=None):
         moe.moe_mxfp4_forward_ex(x, lg, w13, s13, w2, s2, L.T, L.H, L.I, L.E, L.k, y, stream,
-                                 path=path, step_events=step_events)
+                                 act_mode=act, path=path, step_events=step_events)
 
     for _ in range(args.warmup):
         fwd()
@@ -576,18 +590,20 @@ def run_ours(args, L, rank, world, local_rank):
     dominant = max((n for n in names if n in gemm_bytes), key=lambda n: step_ms[n])
     dom_bytes = gemm_bytes[dominant]
     achieved = dom_bytes / (step_ms[dominant] * 1e-3) / 1e9
-    traffic = read_traffic(dominant, L.name)
+    # the committed DRAM figures are those of the MXFP8-mode GEMM kernels
+    traffic = read_traffic(dominant, L.name) if args.act == "mxfp8" else None
     layer_gbs = b_layer / (ms * 1e-3) / 1e9
 
     out = {
         "metric": METRIC, "value": world * L.T / (ms * 1e-3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e2m1xe4m3->f32", "data": "synthetic",
+        "dtype": "e2m1xe4m3->f32" if args.act == "mxfp8" else "e2m1->bf16 x bf16->f32",
+        "data": "synthetic",
         "config": {"workload": f"{L.name}: {L.desc}", "global_batch": world * L.T,
                    "seq_len": 8, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (packed weights %.2f GB)" % (b_layer / 1e9),
-                   "touched_experts": touched, "act_mode": "mxfp8",
+                   "touched_experts": touched, "act_mode": args.act,
                    "path": {1: "multi", 2: "persistent"}[path]},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
@@ -625,7 +641,7 @@ def run_ours(args, L, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         log("[rank 0] timing the CPU oracle on a bounded sample")
         n_tok = min(args.cpu_tokens, L.T)
-        run, n_exp = oracle_sample(L, n_tok)
+        run, n_exp = oracle_sample(L, n_tok, args.act)
         reps, t0 = 0, time.perf_counter()
         while True:               # repeat the sample until at least --cpu-seconds of work
             run(list(range(n_tok)))
@@ -636,7 +652,8 @@ def run_ours(args, L, rank, world, local_rank):
         out["cpu_baseline"] = {
             "value": reps * n_tok / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"first {n_tok} of {L.T} tokens ({n_exp} experts) x {reps} repeats, fp64 "
-                      f"oracle in MXFP8-emulation mode, {dt:.1f} s; MXFP4 packing excluded"}
+                      f"oracle in {'MXFP8-emulation' if args.act == 'mxfp8' else 'exact'} mode, "
+                      f"{dt:.1f} s; MXFP4 packing excluded"}
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -650,6 +667,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--layer", default="full_t256")
     ap.add_argument("--path", choices=sorted(PATHS), default="auto")
+    ap.add_argument("--act", choices=["mxfp8", "bf16"], default="mxfp8",
+                    help="activation mode of the layer (the headline is mxfp8)")
     ap.add_argument("--row", choices=ROWS, default=None,
                     help="only run one call beside the layer (a profiling command)")
     ap.add_argument("--cpu-tokens", type=int, default=32)

@@ -352,6 +352,42 @@ int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
   return 0;
 }
 
+/* --------------------------------------------------- a chain of layers
+ *
+ * Several expert layers run back to back over the same block of tokens: the
+ * whole pipeline kept resident on the GPU rather than one operator at a time
+ * (dothoosh.com, section "TileRT"; techllm.github.io, "Xiaomi MiMo and TileRT
+ * ...", section "3. TileRT").  The pages give no formula for what flows
+ * between the layers; read plainly, layer l's output is layer l+1's input,
+ * optionally added to a residual stream before the one bf16 rounding:
+ *   x_0 = x,  x_{l+1} = bf16_RNE( y_l + r * x_l ),  output x_L,
+ * where y_l is layer l's fp64 output before its final rounding (each layer as
+ * oracle_moe_forward, with its own router logits and weights) and r is 0 or 1.
+ * With r = 0 each step is exactly oracle_moe_forward's bf16 output. */
+int oracle_moe_chain(int n_layers, const uint16_t* x_bf16, const float* const* router_logits,
+                     const uint8_t* const* w13_fp4, const uint8_t* const* w13_e8m0,
+                     const uint8_t* const* w2_fp4, const uint8_t* const* w2_e8m0, int64_t T,
+                     int64_t H, int64_t I, int64_t E, int k, int act_mode, int residual,
+                     uint16_t* y_bf16, int n_threads) {
+  if (n_layers < 1 || T < 0 || H <= 0 || (residual != 0 && residual != 1)) return -1;
+  uint16_t* cur = (uint16_t*)malloc(sizeof(uint16_t) * (size_t)(T * H + 1));
+  double* y = (double*)malloc(sizeof(double) * (size_t)(T * H + 1));
+  for (int64_t i = 0; i < T * H; ++i) cur[i] = x_bf16[i];
+  int rc = 0;
+  for (int l = 0; l < n_layers && rc == 0; ++l) {
+    rc = oracle_moe_forward(cur, router_logits[l], w13_fp4[l], w13_e8m0[l], w2_fp4[l],
+                            w2_e8m0[l], T, H, I, E, k, act_mode, NULL, T, y, NULL, NULL,
+                            n_threads);
+    for (int64_t i = 0; rc == 0 && i < T * H; ++i)
+      cur[i] = oracle_bf16_from_double(y[i] + (residual ? oracle_bf16_value(cur[i]) : 0.0));
+  }
+  if (rc == 0)
+    for (int64_t i = 0; i < T * H; ++i) y_bf16[i] = cur[i];
+  free(cur);
+  free(y);
+  return rc;
+}
+
 /* --------------------------------------------------- the router and a dense
  * FP8 projection (the steps beside the expert layer) */
 

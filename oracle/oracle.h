@@ -19,6 +19,9 @@
  * per 32 along the reduction dimension) in MXFP8-emulation mode, and bf16
  * rounding of the intermediate in bf16-emulation mode.
  *
+ * A chain of layers runs them back to back over one token block, each
+ * layer's output (optionally plus a residual) feeding the next.
+ *
  * Beside the layer: the router logits that feed its top-k (a linear layer
  * with bf16 weights), a dense projection with MXFP8 weights (a layer outside
  * the experts, kept at FP8), and the rejection-sampling verification of a
@@ -82,6 +85,16 @@ int oracle_moe_forward(const uint16_t* x_bf16, const float* router_logits,
                        int64_t I, int64_t E, int k, int act_mode, const int64_t* tokens,
                        int64_t n_tokens, double* y_f64, uint16_t* y_bf16, double* h_out,
                        int n_threads);
+
+/* A chain of n_layers layers over one token block: x_0 = x,
+ * x_{l+1} = bf16_RNE(y_l + residual * x_l) with y_l layer l's fp64 output
+ * (its own logits and weights, host arrays of n_layers pointers); writes x_L
+ * to y_bf16 [T, H].  Returns 0, or -1 on invalid arguments. */
+int oracle_moe_chain(int n_layers, const uint16_t* x_bf16, const float* const* router_logits,
+                     const uint8_t* const* w13_fp4, const uint8_t* const* w13_e8m0,
+                     const uint8_t* const* w2_fp4, const uint8_t* const* w2_e8m0, int64_t T,
+                     int64_t H, int64_t I, int64_t E, int k, int act_mode, int residual,
+                     uint16_t* y_bf16, int n_threads);
 
 /* router logits [T, E] = x [T, H] (bf16) times W_r^T (W_r [E, H] bf16), exact fp64 */
 void oracle_router_logits(const uint16_t* x_bf16, const uint16_t* w_bf16, int64_t T,

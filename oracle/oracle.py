@@ -56,6 +56,9 @@ def lib():
         L.oracle_moe_forward.restype = i32
         L.oracle_moe_forward.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
                                          vp, i64, vp, vp, vp, i32]
+        L.oracle_moe_chain.restype = i32
+        L.oracle_moe_chain.argtypes = [i32, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i32, i32,
+                                       i32, vp, i32]
         L.oracle_router_logits.restype = None
         L.oracle_router_logits.argtypes = [vp, vp, i64, i64, i64, vp]
         L.oracle_mxfp8_quantize.restype = None
@@ -140,6 +143,29 @@ def moe_forward(x_bf16, logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, k, act_mode=
     if rc != 0:
         raise ValueError(f"oracle_moe_forward rejected the arguments ({rc})")
     return y16, y64, h
+
+
+def moe_chain(x_bf16, logits_list, weights_list, k, act_mode=ACT_EXACT, residual=False,
+              n_threads=0):
+    """Layers back to back: x_{l+1} = bf16_RNE(y_l + residual * x_l); returns x_L (uint16
+    bf16 bits [T, H]).  logits_list[l] is [T, E] f32, weights_list[l] = (w13, s13, w2, s2)."""
+    x = np.ascontiguousarray(x_bf16, dtype=np.uint16)
+    T, H = x.shape
+    n = len(logits_list)
+    assert n == len(weights_list) and n >= 1
+    lg = [np.ascontiguousarray(a, dtype=np.float32) for a in logits_list]
+    ws = [[np.ascontiguousarray(a, dtype=np.uint8) for a in w] for w in weights_list]
+    E = lg[0].shape[1]
+    I = ws[0][2].shape[-1] * 2
+
+    def ptrs(arrs):
+        return (ctypes.c_void_p * n)(*[a.ctypes.data for a in arrs])
+    out = np.empty((T, H), dtype=np.uint16)
+    rc = lib().oracle_moe_chain(n, _p(x), ptrs(lg), *(ptrs([w[i] for w in ws]) for i in range(4)),
+                                T, H, I, E, k, act_mode, int(bool(residual)), _p(out), n_threads)
+    if rc != 0:
+        raise ValueError(f"oracle_moe_chain rejected the arguments ({rc})")
+    return out
 
 
 def router_logits(x_bf16: np.ndarray, w_bf16: np.ndarray) -> np.ndarray:

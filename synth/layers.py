@@ -43,6 +43,9 @@ LAYERS = {
     # full per-expert shape with 32 experts (0.64 GB of packed weights, larger than L2):
     # the case detailed ncu captures run on
     "full_e32_t64": Layer("full_e32_t64", 6144, 2048, 32, 8, 64, 5),
+    # the skewed 1024-token layer's regime (top experts near 1024 tokens each) on 32 experts:
+    # the case for detailed captures of the tensor-bound GEMMs
+    "zipf_e32_t1024": Layer("zipf_e32_t1024", 6144, 2048, 32, 8, 1024, 6, zipf=True),
 }
 
 

@@ -60,6 +60,7 @@ typedef enum {
 
 #define MOE_MAX_K 16     /* largest top-k */
 #define MOE_MAX_E 1024   /* largest expert count */
+#define MOE_MAX_CHAIN 256 /* most layers of one moe_mxfp4_forward_chain call */
 
 /* activation modes of moe_opts.act_mode */
 #define MOE_ACT_MXFP8 0  /* x and h quantized to MXFP8-E4M3 (blocks of 32) */
@@ -141,6 +142,44 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
                          const uint8_t* w13_e8m0, const uint8_t* w2_fp4, const uint8_t* w2_e8m0,
                          int T, int H, int I, int E, int k, void* y_bf16, cudaStream_t stream,
                          const moe_opts* opts);
+
+/*
+ * moe_mxfp4_forward_chain — n_layers expert layers back to back over one block
+ * of T tokens, the pipeline kept on the GPU instead of one call per layer
+ * (dothoosh.com, section "TileRT": the whole computational pipeline resident
+ * and prefetched; techllm.github.io, "Xiaomi MiMo and TileRT ...", section
+ * "3. TileRT").  The pages give no formula for the hand-off between layers;
+ * it is read as composition with an optional residual stream:
+ *
+ *   x_0 = x,  x_{l+1} = bf16_RNE( y_l + residual * x_l ),  y_bf16 = x_{n_layers}
+ *
+ * where y_l is layer l's gate-weighted sum (moe_mxfp4_forward before its
+ * final rounding, with layer l's own logits and weights; the residual is added
+ * in fp32 after the sum).  With residual = 0 the result is bit-identical to
+ * n_layers successive moe_mxfp4_forward_ex calls with the same options.
+ *
+ * All layers are routed first (routing reads only the given logits); each
+ * layer's combine then writes the next layer's activation rows directly.
+ *
+ * Arguments: router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0 are HOST
+ * arrays of n_layers device pointers, each as in moe_mxfp4_forward (one
+ * layer's tensors); the shape (T, H, I, E, k) is shared by all layers.
+ * 1 <= n_layers <= MOE_MAX_CHAIN; residual is 0 or 1; y_bf16 [T, H] may equal
+ * x_bf16.  opts as moe_mxfp4_forward_ex (act_mode, path, workspace of at least
+ * moe_mxfp4_workspace_size_chain bytes, debug flags); step markers follow the
+ * kernel order: route_topk, route_permute for each layer in turn, act_quant,
+ * then per layer its GEMM kernel(s) and combine.
+ * Returns MOE_OK or an moe_status error (host-detected errors launch nothing).
+ */
+int moe_mxfp4_forward_chain(int n_layers, const void* x_bf16, const float* const* router_logits,
+                            const uint8_t* const* w13_fp4, const uint8_t* const* w13_e8m0,
+                            const uint8_t* const* w2_fp4, const uint8_t* const* w2_e8m0, int T,
+                            int H, int I, int E, int k, int residual, void* y_bf16,
+                            cudaStream_t stream, const moe_opts* opts);
+
+/* scratch bytes moe_mxfp4_forward_chain needs (0 for an invalid shape) */
+size_t moe_mxfp4_workspace_size_chain(int n_layers, int T, int H, int I, int E, int k,
+                                      int act_mode);
 
 /*
  * moe_mxfp4_select_path — the path MOE_PATH_AUTO takes for this shape on the

@@ -21,7 +21,7 @@ MOE_PATH_AUTO, MOE_PATH_MULTI, MOE_PATH_PERSISTENT = 0, 1, 2
 MOE_DEBUG_SHORT_TIMEOUT = 1
 MOE_DEBUG_FORCE_DEP_TIMEOUT = 2
 MOE_ERR_DEVICE_TIMEOUT = -6
-MOE_MAX_K, MOE_MAX_E = 16, 1024
+MOE_MAX_K, MOE_MAX_E, MOE_MAX_CHAIN = 16, 1024, 256
 MOE_NOALLOC_SCRATCH_BYTES = 80 * 1024 * 1024
 
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID_ARG", -2: "MOE_ERR_UNSUPPORTED_SHAPE",
@@ -64,6 +64,11 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_forward_noalloc.restype = i
         L.moe_mxfp4_forward_routed.argtypes = fwd + [ctypes.POINTER(moe_opts)]
         L.moe_mxfp4_forward_routed.restype = i
+        L.moe_mxfp4_forward_chain.argtypes = [i, vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp,
+                                              vp, ctypes.POINTER(moe_opts)]
+        L.moe_mxfp4_forward_chain.restype = i
+        L.moe_mxfp4_workspace_size_chain.argtypes = [i, i, i, i, i, i, i]
+        L.moe_mxfp4_workspace_size_chain.restype = sz
         L.moe_mxfp4_workspace_size_routed.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_workspace_size_routed.restype = sz
         L.moe_router_topk.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, vp]
@@ -135,6 +140,31 @@ def moe_mxfp4_forward_ex(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8
                                              _ptr(w13_e8m0), _ptr(w2_fp4), _ptr(w2_e8m0), T, H, I,
                                              E, k, _ptr(y_bf16), _stream(stream),
                                              ctypes.byref(o)), "moe_mxfp4_forward_ex")
+
+
+def moe_mxfp4_forward_chain(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I,
+                            E, k, y_bf16, residual=False, stream=None, act_mode=MOE_ACT_MXFP8,
+                            path=MOE_PATH_AUTO, workspace=None, workspace_bytes=0,
+                            debug_flags=0, step_events=None):
+    """Layers back to back over one token block: router_logits and the four weight arguments
+    are sequences with one device tensor per layer; x_{l+1} = bf16(y_l + residual * x_l)."""
+    n = len(router_logits)
+    arrs = [router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0]
+    if any(len(a) != n for a in arrs):
+        raise ValueError("one logits tensor and one set of weights per layer")
+    ptrs = [(ctypes.c_void_p * max(n, 1))(*[_ptr(t) for t in a]) for a in arrs]
+    o = moe_opts(act_mode, path, _ptr(workspace), workspace_bytes, debug_flags)
+    if step_events is not None:
+        o.step_events = ctypes.cast(step_events, ctypes.POINTER(ctypes.c_void_p))
+        o.n_step_events = len(step_events)
+    return _check(lib().moe_mxfp4_forward_chain(n, _ptr(x_bf16), *ptrs, T, H, I, E, k,
+                                                int(bool(residual)), _ptr(y_bf16),
+                                                _stream(stream), ctypes.byref(o)),
+                  "moe_mxfp4_forward_chain")
+
+
+def moe_mxfp4_workspace_size_chain(n_layers, T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
+    return int(lib().moe_mxfp4_workspace_size_chain(n_layers, T, H, I, E, k, act_mode))
 
 
 def moe_mxfp4_forward_noalloc(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,

@@ -201,6 +201,9 @@ int device_state(DeviceState** out) {
     const int permute_smem = (35 * MOE_MAX_E + 35) * (int)sizeof(int);
     if (cudaFuncSetAttribute(route_permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              permute_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(route_permute_layers_kernel,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             permute_smem) != cudaSuccess ||
         !set_gemm_smem<kChunkNarrow>() || !set_gemm_smem<kChunkWide>() ||
         cudaFuncSetAttribute(dense_tc_kernel<kDenseBf16, kRouterNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -311,6 +314,46 @@ Work carve(void* base, const Layout& L) {
   w.part = reinterpret_cast<float*>(b + L.part);
   w.rlogits = reinterpret_cast<float*>(b + L.rlogits);
   w.max_chunks = L.max_chunks;
+  return w;
+}
+
+// A chain of n layers: n routing blocks one stride apart (a routing block is
+// the first regions of a layer's layout, topk_idx .. meta), then the rest of
+// one layer's layout (the activation buffers the layers share in turn), then
+// two bf16 [T, H] buffers that carry the residual stream between layers.
+struct ChainLayout {
+  Layout base;
+  size_t route_block, act_shift, xb[2], total;
+};
+
+ChainLayout chain_layout(int64_t n, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                         int act_mode) {
+  ChainLayout C{};
+  C.base = layout_for(T, H, I, E, k, act_mode);
+  C.route_block = C.base.xq;
+  C.act_shift = (size_t)(n - 1) * C.route_block;  // the base layout follows the last block
+  const size_t x_bytes = align256((size_t)(T * H * 2));
+  C.xb[0] = C.act_shift + C.base.total;
+  C.xb[1] = C.xb[0] + x_bytes;
+  C.total = C.xb[1] + x_bytes;
+  return C;
+}
+
+// layer l's view of a chain workspace: its own routing block, the shared rest
+Work carve_chain(void* base, const ChainLayout& C, int l) {
+  uint8_t* b = static_cast<uint8_t*>(base);
+  Work w = carve(b + C.act_shift, C.base);
+  uint8_t* r = b + (size_t)l * C.route_block;
+  const Layout& L = C.base;
+  w.topk_idx = reinterpret_cast<int32_t*>(r + L.topk_idx);
+  w.topk_w = reinterpret_cast<float*>(r + L.topk_w);
+  w.cnt = reinterpret_cast<int32_t*>(r + L.cnt);
+  w.off = reinterpret_cast<int32_t*>(r + L.off);
+  w.perm = reinterpret_cast<int32_t*>(r + L.perm);
+  w.pos = reinterpret_cast<int32_t*>(r + L.pos);
+  w.chunks = reinterpret_cast<int4*>(r + L.chunks);
+  w.done = reinterpret_cast<int32_t*>(r + L.done);
+  w.meta = reinterpret_cast<int32_t*>(r + L.meta);
   return w;
 }
 
@@ -426,6 +469,35 @@ int enqueue_route(const float* logits, bool first, int T, int E, int k, int chun
   return launch_status();
 }
 
+// Routing steps (1)-(4) of every layer of a chain in two launches (the first
+// an ordinary launch: it starts the call); layer l's routing block lies
+// l * stride bytes after layer 0's (w0)
+int enqueue_route_layers(const float* const* logits, int n, int T, int E, int k, int chunk_max,
+                         const Work& w0, int64_t stride, DeviceState* d, cudaStream_t s,
+                         Steps& st) {
+  LayerLogits lg{};
+  for (int l = 0; l < n; ++l) lg.p[l] = logits[l];
+  const dim3 grid(grid_for((int64_t)T * 32, 256, 1 << 30), n);
+  st.mark();
+  auto topk = [&](auto kernel) {
+    kernel<<<grid, 256, 0, s>>>(lg, T, E, k, w0.topk_idx, w0.topk_w, stride, d->status);
+    return cudaGetLastError();
+  };
+  const cudaError_t te = E <= 128   ? topk(route_topk_layers_kernel<4>)
+                         : E <= 384 ? topk(route_topk_layers_kernel<12>)
+                                    : topk(route_topk_layers_kernel<32>);
+  if (te != cudaSuccess) return MOE_ERR_CUDA;
+  st.launched();
+  st.mark();
+  const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
+  if (launch_pdl(route_permute_layers_kernel, dim3(n), dim3(1024), smem, s,
+                 (const int32_t*)w0.topk_idx, T, k, E, w0.cnt, w0.off, w0.perm, w0.pos, w0.chunks,
+                 w0.max_chunks, chunk_max, w0.meta, w0.done, stride, d->status) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  st.launched();
+  return launch_status();
+}
+
 // The path MOE_PATH_AUTO takes.  One launch removes the gap and the tail
 // between the two GEMMs, which pays when each SM gets a handful of work items;
 // with many items per SM the two specialised launches stream weights faster,
@@ -443,55 +515,11 @@ int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
              : MOE_PATH_MULTI;
 }
 
-// The layer.  Exactly one of `logits` (router logits [T, E]) and `w_router`
-// (router weights [E, H] bf16: the router GEMM runs in front of the top-k)
-// is given.
-int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
-                 const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
-                 void* y, cudaStream_t stream, const moe_opts* opts,
-                 const void* w_router = nullptr) {
-  if (!x_bf16 || (!logits == !w_router) || !w13 || !w13s || !w2 || !w2s || !y)
-    return MOE_ERR_INVALID_ARG;
-  int rc = validate_shape(T, H, I, E, k);
-  if (rc) return rc;
-  const bool routed = w_router != nullptr;
-  if (routed && !aligned(w_router, 16)) return MOE_ERR_ALIGNMENT;
-  const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
-  const int path = opts ? opts->path : MOE_PATH_AUTO;
-  if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
-  if (!aligned(w13, 32) || !aligned(w2, 32)) return MOE_ERR_ALIGNMENT;
-  if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
-      !aligned(y, 16))
-    return MOE_ERR_ALIGNMENT;
-  const Layout L = layout_for(T, H, I, E, k, act, routed);
-  if (opts && opts->workspace) {
-    if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
-    if (opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
-  }
-  if (T == 0) return MOE_OK;
-
-  DeviceState* d = nullptr;
-  if ((rc = device_state(&d))) return rc;
-  void* ws = opts ? opts->workspace : nullptr;
-  if (!ws && (rc = cached_workspace(d, L.total, &ws))) return rc;
-  const Work w = carve(ws, L);
+// step a4: gather x rows into slot order, MXFP8-quantised or copied as bf16
+int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, DeviceState* d,
+                cudaStream_t stream, Steps& st) {
   const int TK = T * k;
-
-  // Wide token chunks halve the MMA instructions per token when experts get
-  // many tokens (large T); narrow chunks keep the weight pipeline deepest.
-  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
-  const unsigned long long timeout_ns =
-      (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
-  Steps st{opts, stream};
-  if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
-                                     timeout_ns, st)))
-    return rc;
-  if ((rc = enqueue_route(routed ? w.rlogits : logits, !routed, T, E, k,
-                          wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
-    return rc;
   const int cap = d->sms * 8;
-  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   st.mark();
   const cudaError_t qe =
       act == MOE_ACT_MXFP8
@@ -504,6 +532,17 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
                        reinterpret_cast<uint16_t*>(w.xq), d->status);
   if (qe != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
+  return MOE_OK;
+}
+
+// steps a5-a7: the two grouped GEMMs (one persistent launch or two)
+int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                  const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
+                  DeviceState* d, cudaStream_t stream, unsigned long long timeout_ns,
+                  const moe_opts* opts, Steps& st) {
+  const int TK = T * k;
+  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
+  int rc = MOE_OK;
   if (act == MOE_ACT_MXFP8) {
     TcPhase g1{}, g2{};
     if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
@@ -623,12 +662,140 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
       return MOE_ERR_CUDA;
     st.launched();
   }
+  return MOE_OK;
+}
+
+// The layer.  Exactly one of `logits` (router logits [T, E]) and `w_router`
+// (router weights [E, H] bf16: the router GEMM runs in front of the top-k)
+// is given.
+int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, const uint8_t* w13s,
+                 const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
+                 void* y, cudaStream_t stream, const moe_opts* opts,
+                 const void* w_router = nullptr) {
+  if (!x_bf16 || (!logits == !w_router) || !w13 || !w13s || !w2 || !w2s || !y)
+    return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  const bool routed = w_router != nullptr;
+  if (routed && !aligned(w_router, 16)) return MOE_ERR_ALIGNMENT;
+  const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
+  const int path = opts ? opts->path : MOE_PATH_AUTO;
+  if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w13, 32) || !aligned(w2, 32)) return MOE_ERR_ALIGNMENT;
+  if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
+      !aligned(y, 16))
+    return MOE_ERR_ALIGNMENT;
+  const Layout L = layout_for(T, H, I, E, k, act, routed);
+  if (opts && opts->workspace) {
+    if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
+    if (opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
+  }
+  if (T == 0) return MOE_OK;
+
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  void* ws = opts ? opts->workspace : nullptr;
+  if (!ws && (rc = cached_workspace(d, L.total, &ws))) return rc;
+  const Work w = carve(ws, L);
+
+  // Wide token chunks halve the MMA instructions per token when experts get
+  // many tokens (large T); narrow chunks keep the weight pipeline deepest.
+  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
+  const unsigned long long timeout_ns =
+      (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
+  Steps st{opts, stream};
+  if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
+                                     timeout_ns, st)))
+    return rc;
+  if ((rc = enqueue_route(routed ? w.rlogits : logits, !routed, T, E, k,
+                          wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
+    return rc;
+  if ((rc = enqueue_act(act, static_cast<const uint16_t*>(x_bf16), w, T, H, k, d, stream, st)) ||
+      (rc = enqueue_gemms(act, path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream, timeout_ns,
+                          opts, st)))
+    return rc;
+  const int cap = d->sms * 8;
   st.mark();
-  if (launch_pdl(combine_kernel, dim3(grid_for((int64_t)T * H / 8, 256, cap)), dim3(256), 0,
+  if (launch_pdl(combine_kernel, dim3(grid_for((int64_t)T * H / 4, 256, cap)), dim3(256), 0,
                  stream, (const float*)w.yp, (const int32_t*)w.pos, (const float*)w.topk_w, T, H,
                  k, static_cast<uint16_t*>(y)) != cudaSuccess)
     return MOE_ERR_CUDA;
   st.launched();
+  st.mark();
+  return launch_status();
+}
+
+// A chain of layers over one token block: x_0 = x, x_{l+1} = bf16_RNE(y_l +
+// residual * x_l), y = x_n.  Routing depends only on each layer's logits, so
+// every layer is routed first, all layers at once (two launches); then per
+// layer the GEMMs run and the combine writes layer l+1's activation rows
+// directly (combine_next_kernel).
+int chain_impl(int n, const void* x_bf16, const float* const* logits,
+               const uint8_t* const* w13, const uint8_t* const* w13s, const uint8_t* const* w2,
+               const uint8_t* const* w2s, int T, int H, int I, int E, int k, int residual,
+               void* y, cudaStream_t stream, const moe_opts* opts) {
+  if (n < 1 || n > MOE_MAX_CHAIN || !x_bf16 || !logits || !w13 || !w13s || !w2 || !w2s || !y ||
+      (residual != 0 && residual != 1))
+    return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
+  const int path = opts ? opts->path : MOE_PATH_AUTO;
+  if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x_bf16, 16) || !aligned(y, 16)) return MOE_ERR_ALIGNMENT;
+  for (int l = 0; l < n; ++l) {
+    if (!logits[l] || !w13[l] || !w13s[l] || !w2[l] || !w2s[l]) return MOE_ERR_INVALID_ARG;
+    if (!aligned(logits[l], 16) || !aligned(w13[l], 32) || !aligned(w2[l], 32) ||
+        !aligned(w13s[l], 16) || !aligned(w2s[l], 16))
+      return MOE_ERR_ALIGNMENT;
+  }
+  const ChainLayout C = chain_layout(n, T, H, I, E, k, act);
+  if (opts && opts->workspace) {
+    if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
+    if (opts->workspace_bytes < C.total) return MOE_ERR_NO_MEMORY;
+  }
+  if (T == 0) return MOE_OK;
+
+  DeviceState* d = nullptr;
+  if ((rc = device_state(&d))) return rc;
+  void* ws = opts ? opts->workspace : nullptr;
+  if (!ws && (rc = cached_workspace(d, C.total, &ws))) return rc;
+  uint16_t* xb[2] = {reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + C.xb[0]),
+                     reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + C.xb[1])};
+  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
+  const unsigned long long timeout_ns =
+      (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
+  Steps st{opts, stream};
+  if ((rc = enqueue_route_layers(logits, n, T, E, k, wide ? kChunkWide : kChunkNarrow,
+                                 carve_chain(ws, C, 0), (int64_t)C.route_block, d, stream, st)))
+    return rc;
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  if ((rc = enqueue_act(act, x, carve_chain(ws, C, 0), T, H, k, d, stream, st))) return rc;
+  const int64_t threads = (int64_t)T * H / 4;
+  for (int l = 0; l < n; ++l) {
+    const Work w = carve_chain(ws, C, l);
+    if ((rc = enqueue_gemms(act, path, w13[l], w13s[l], w2[l], w2s[l], T, H, I, E, k, w, d,
+                            stream, timeout_ns, opts, st)))
+      return rc;
+    const bool last = l == n - 1;
+    const uint16_t* x_res = residual ? (l == 0 ? x : xb[l & 1]) : nullptr;
+    uint16_t* x_out = last ? static_cast<uint16_t*>(y) : residual ? xb[(l + 1) & 1] : nullptr;
+    const int32_t* pos_next = last ? nullptr : carve_chain(ws, C, l + 1).pos;
+    st.mark();
+    const dim3 grid(grid_for(threads, 256, d->sms * 8));
+    const cudaError_t e =
+        act == MOE_ACT_MXFP8
+            ? launch_pdl(combine_next_kernel<true>, grid, dim3(256), 0, stream,
+                         (const float*)w.yp, (const int32_t*)w.pos, (const float*)w.topk_w, T, H,
+                         k, x_res, x_out, pos_next, w.xq, w.xs, d->status)
+            : launch_pdl(combine_next_kernel<false>, grid, dim3(256), 0, stream,
+                         (const float*)w.yp, (const int32_t*)w.pos, (const float*)w.topk_w, T, H,
+                         k, x_res, x_out, pos_next, w.xq, w.xs, d->status);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    st.launched();
+  }
   st.mark();
   return launch_status();
 }
@@ -659,6 +826,23 @@ size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode)
   if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
   return layout_for(T, H, I, E, k, act_mode).total;
+}
+
+int moe_mxfp4_forward_chain(int n_layers, const void* x_bf16, const float* const* router_logits,
+                            const uint8_t* const* w13_fp4, const uint8_t* const* w13_e8m0,
+                            const uint8_t* const* w2_fp4, const uint8_t* const* w2_e8m0, int T,
+                            int H, int I, int E, int k, int residual, void* y_bf16,
+                            cudaStream_t stream, const moe_opts* opts) {
+  return chain_impl(n_layers, x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H, I,
+                    E, k, residual, y_bf16, stream, opts);
+}
+
+size_t moe_mxfp4_workspace_size_chain(int n_layers, int T, int H, int I, int E, int k,
+                                      int act_mode) {
+  if (n_layers < 1 || n_layers > MOE_MAX_CHAIN) return 0;
+  if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
+  return chain_layout(n_layers, T, H, I, E, k, act_mode).total;
 }
 
 int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode) {

@@ -15,16 +15,12 @@
 
 namespace moe {
 
-// One warp per token.  MAXPL logits per lane (E <= 32 * MAXPL).
+// Step (1) for token t, by one warp.  MAXPL logits per lane (E <= 32 * MAXPL).
 template <int MAXPL>
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int k, int32_t* __restrict__ idx,
-                                                         float* __restrict__ w, int* status) {
-  grid_dependency_wait();
-  grid_launch_dependents();
+__device__ __forceinline__ void route_topk_token(const float* __restrict__ logits, int t, int E,
+                                                 int k, int32_t* __restrict__ idx,
+                                                 float* __restrict__ w, int* status) {
   const int lane = threadIdx.x & 31;
-  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-  if (t >= T) return;
   const float* l = logits + (size_t)t * E;
   float v[MAXPL];
   uint32_t taken = 0;
@@ -75,6 +71,38 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+// one warp per token
+template <int MAXPL>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                         int E, int k, int32_t* __restrict__ idx,
+                                                         float* __restrict__ w, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  if (t < T) route_topk_token<MAXPL>(logits, t, E, k, idx, w, status);
+}
+
+// Router logits of the layers of a chain (host array copied into the launch)
+struct LayerLogits {
+  const float* p[MOE_MAX_CHAIN];
+};
+
+// step (1) of every layer of a chain in one launch: blockIdx.y = layer, whose
+// routing block starts `stride` bytes after the previous layer's
+template <int MAXPL>
+__global__ void __launch_bounds__(256) route_topk_layers_kernel(
+    const __grid_constant__ LayerLogits lg, int T, int E, int k, int32_t* __restrict__ idx0,
+    float* __restrict__ w0, int64_t stride, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int64_t off = (int64_t)blockIdx.y * stride;
+  if (t < T)
+    route_topk_token<MAXPL>(lg.p[blockIdx.y], t, E, k,
+                            reinterpret_cast<int32_t*>(reinterpret_cast<char*>(idx0) + off),
+                            reinterpret_cast<float*>(reinterpret_cast<char*>(w0) + off), status);
+}
+
 __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int x = v;
@@ -102,9 +130,9 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
   return r;
 }
 
-// Single CTA of 1024 threads: histogram, scan, stable permutation, chunk list.
-// Dynamic shared memory: (35 * E + 1 + 34) ints.
-__global__ void __launch_bounds__(1024) route_permute_kernel(
+// Steps (2)-(4) by one CTA of 1024 threads: histogram, scan, stable
+// permutation, chunk list.  Dynamic shared memory: (35 * E + 1 + 34) ints.
+__device__ __forceinline__ void route_permute_cta(
     const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ cnt_out,
     int32_t* __restrict__ off_out, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
     int4* __restrict__ chunks, int max_chunks, int chunk_max, int32_t* __restrict__ meta,
@@ -118,8 +146,6 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
   int* s_tot = s_warp + 32;   // 2
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int TK = T * k;
-  grid_dependency_wait();
-  grid_launch_dependents();
 
   for (int e = tid; e < E; e += 1024) {
     s_cnt[e] = 0;
@@ -200,6 +226,35 @@ __global__ void __launch_bounds__(1024) route_permute_kernel(
     meta[0] = min(s_tot[0], max_chunks);
     meta[1] = s_tot[1];
   }
+}
+
+__global__ void __launch_bounds__(1024) route_permute_kernel(
+    const int32_t* __restrict__ idx, int T, int k, int E, int32_t* __restrict__ cnt_out,
+    int32_t* __restrict__ off_out, int32_t* __restrict__ perm, int32_t* __restrict__ pos,
+    int4* __restrict__ chunks, int max_chunks, int chunk_max, int32_t* __restrict__ meta,
+    int32_t* __restrict__ done, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  route_permute_cta(idx, T, k, E, cnt_out, off_out, perm, pos, chunks, max_chunks, chunk_max,
+                    meta, done, status);
+}
+
+// steps (2)-(4) of every layer of a chain: one CTA per layer; each of the
+// layer's arrays starts `stride` bytes after the previous layer's
+__global__ void __launch_bounds__(1024) route_permute_layers_kernel(
+    const int32_t* idx0, int T, int k, int E, int32_t* cnt0, int32_t* off0, int32_t* perm0,
+    int32_t* pos0, int4* chunks0, int max_chunks, int chunk_max, int32_t* meta0, int32_t* done0,
+    int64_t stride, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t off = (int64_t)blockIdx.x * stride;
+  auto at = [off](auto* p) {
+    using P = decltype(p);
+    return reinterpret_cast<P>(reinterpret_cast<char*>(const_cast<void*>(
+                                   static_cast<const void*>(p))) + off);
+  };
+  route_permute_cta(at(idx0), T, k, E, at(cnt0), at(off0), at(perm0), at(pos0), at(chunks0),
+                    max_chunks, chunk_max, at(meta0), at(done0), status);
 }
 
 }  // namespace moe

@@ -140,3 +140,43 @@ def test_verify_validates_on_host(moe):
     assert L.moe_verify_block(256, 512, 768, 1024, 1284, 4, 7, 100, 1536, 1792, None) == -3
     assert L.moe_verify_block(*a, 0, 7, 100, 1536, 1792, None) == 0        # S = 0: no-op
     assert L.moe_verify_block(None, 512, 768, 1024, 1280, 4, 7, 100, 1536, 1792, None) == -1
+
+
+def _chain(moe, n=2, layer_ptrs=None, **kw):
+    """moe_mxfp4_forward_chain with fake, never-dereferenced addresses"""
+    import ctypes
+    a = dict(x=256, T=4, H=256, I=128, E=8, k=2, residual=0, y=16384, opts=None)
+    a.update(kw)
+    base = layer_ptrs or [(512, 1024, 2048, 4096, 8192)] * n
+    arrs = [(ctypes.c_void_p * max(n, 1))(*[p[i] for p in base]) for i in range(5)]
+    return moe.lib().moe_mxfp4_forward_chain(n, a["x"], *arrs, a["T"], a["H"], a["I"], a["E"],
+                                             a["k"], a["residual"], a["y"], None, a["opts"])
+
+
+def test_chain_validates_on_host(moe):
+    ok = (512, 1024, 2048, 4096, 8192)
+    assert _chain(moe, n=0) == -1
+    assert _chain(moe, n=moe.MOE_MAX_CHAIN + 1) == -1
+    assert _chain(moe, residual=2) == -1
+    assert _chain(moe, layer_ptrs=[ok, (512, None, 2048, 4096, 8192)]) == -1
+    assert _chain(moe, layer_ptrs=[ok, (512, 1040, 2048, 4096, 8192)]) == -3   # fp4 alignment
+    assert _chain(moe, layer_ptrs=[ok, (520, 1024, 2048, 4096, 8192)]) == -3   # logits
+    assert _chain(moe, H=200) == -2
+    assert _chain(moe, k=9) == -1
+    assert _chain(moe, y=16386) == -3
+    assert _chain(moe, T=0) == 0                 # no-op, nothing launched
+    import ctypes
+    o = moe.moe_opts(0, 0, 256 * 1024, 16, 0, None, 0)
+    assert _chain(moe, opts=ctypes.byref(o)) == -5   # workspace too small
+    o = moe.moe_opts(4, 0, None, 0, 0, None, 0)
+    assert _chain(moe, opts=ctypes.byref(o)) == -1   # bad act mode
+
+
+def test_chain_workspace_size(moe):
+    one = moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 2)
+    c1 = moe.moe_mxfp4_workspace_size_chain(1, 16, 256, 128, 8, 2)
+    c4 = moe.moe_mxfp4_workspace_size_chain(4, 16, 256, 128, 8, 2)
+    assert one < c1 < c4                          # residual buffers; a routing block per layer
+    assert moe.moe_mxfp4_workspace_size_chain(0, 16, 256, 128, 8, 2) == 0
+    assert moe.moe_mxfp4_workspace_size_chain(2, 16, 250, 128, 8, 2) == 0
+    assert moe.moe_mxfp4_workspace_size_chain(2, 16, 256, 128, 8, 2, 9) == 0

@@ -1,0 +1,138 @@
+"""GPU parity of the chain of layers (moe_mxfp4_forward_chain) through the C ABI.
+
+Without the residual the chain must equal successive single-layer calls bit for bit (the fused
+combine + next-layer activation step keeps the unfused arithmetic and order).  With the residual
+it is compared with the oracle's chain under the layer's own bars: MXFP8 mode against the
+MXFP8-emulation oracle (rel-Frobenius <= 1e-2, max|err| <= 4e-2 * rms), bf16 mode against the
+exact oracle (rel-Frobenius <= 5e-3).  Those cases raise every E8M0 scale by 2 (weights x 4,
+exactly) so that each layer's output is comparable to the residual stream it is added to (the
+stream's rms grows from 1 to between 1.2 and 4.6 over the layers).
+"""
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+import mxfp4_expert_layer_dflash_b300 as moe  # noqa: E402
+from gpu_util import bf16_to_f64, dev, host_bf16, max_err_over_rms, rel_fro  # noqa: E402
+from synth import layers as LY  # noqa: E402
+
+MXFP8_FRO, MXFP8_MAX, BF16_FRO = 1e-2, 4e-2, 5e-3
+
+
+def _layers(T, H, I, E, k, n, seed, device_weights=True):
+    Ls = [LY.Layer(f"chain{l}", H, I, E, k, T, seed + 7 * l) for l in range(n)]
+    lgs = [dev(LY.host_logits(L)) for L in Ls]
+    if device_weights:
+        ws = [LY.device_packed_weights(L, moe.mxfp4_quantize) for L in Ls]
+    else:
+        from oracle import oracle as O
+        ws = [tuple(dev(a) for a in LY.host_packed_weights(L, O.mxfp4_quantize)) for L in Ls]
+    return Ls, lgs, ws
+
+
+def _chain(x, lgs, ws, L, residual, act, path=moe.MOE_PATH_AUTO):
+    y = torch.full((L.T, L.H), float("nan"), dtype=torch.bfloat16, device="cuda")
+    moe.moe_mxfp4_forward_chain(x, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                [w[2] for w in ws], [w[3] for w in ws], L.T, L.H, L.I, L.E, L.k,
+                                y, residual=residual, act_mode=act, path=path)
+    assert moe.moe_mxfp4_get_status() == 0
+    return y
+
+
+def _successive(x, lgs, ws, L, act, path=moe.MOE_PATH_AUTO):
+    cur = x
+    for lg, w in zip(lgs, ws):
+        y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
+        moe.moe_mxfp4_forward_ex(cur, lg, *w, L.T, L.H, L.I, L.E, L.k, y, act_mode=act, path=path)
+        assert moe.moe_mxfp4_get_status() == 0
+        cur = y
+    return cur
+
+
+MODES = [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI), (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
+         (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)]
+
+
+@pytest.mark.parametrize("act,path", MODES)
+@pytest.mark.parametrize("T,H,I,E,k,n", [(16, 256, 128, 8, 2, 3), (1, 384, 128, 4, 4, 2),
+                                         (600, 256, 256, 6, 2, 2), (40, 2048, 1024, 64, 8, 4),
+                                         (9, 128, 128, 1, 1, 5)])
+def test_chain_without_residual_is_successive_calls(T, H, I, E, k, n, act, path):
+    Ls, lgs, ws = _layers(T, H, I, E, k, n, 100 + T)
+    x = dev(LY.host_x(Ls[0]))
+    yc = _chain(x, lgs, ws, Ls[0], False, act, path)
+    ys = _successive(x, lgs, ws, Ls[0], act, path)
+    assert torch.equal(yc.view(torch.int16), ys.view(torch.int16))
+
+
+def test_chain_full_shape_is_successive_calls():
+    Ls, lgs, ws = _layers(8, 6144, 2048, 384, 8, 2, 500)
+    x = dev(LY.host_x(Ls[0]))
+    yc = _chain(x, lgs, ws, Ls[0], False, moe.MOE_ACT_MXFP8)
+    ys = _successive(x, lgs, ws, Ls[0], moe.MOE_ACT_MXFP8)
+    assert torch.equal(yc.view(torch.int16), ys.view(torch.int16))
+    del ws
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+@pytest.mark.parametrize("T,H,I,E,k,n", [(16, 256, 128, 8, 2, 3), (5, 384, 256, 4, 2, 2)])
+def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act):
+    from oracle import oracle as O
+    Ls = [LY.Layer(f"res{l}", H, I, E, k, T, 300 + l) for l in range(n)]
+    xh = LY.host_x(Ls[0])
+    lgh = [LY.host_logits(L) for L in Ls]
+    wh = []
+    for L in Ls:
+        w13, s13, w2, s2 = LY.host_packed_weights(L, O.mxfp4_quantize)
+        wh.append((w13, s13 + 2, w2, s2 + 2))          # every weight x 4, exactly
+    y = _chain(dev(xh), [dev(a) for a in lgh], [tuple(dev(a) for a in w) for w in wh], Ls[0],
+               True, act)
+    yg = bf16_to_f64(host_bf16(y))
+    mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_EXACT
+    yref = bf16_to_f64(O.moe_chain(xh, lgh, wh, k, mode, residual=True))
+    delta = yref - bf16_to_f64(xh)
+    print(f"rms(x) {np.sqrt(np.mean(bf16_to_f64(xh) ** 2)):.3f} "
+          f"rms(sum of layer outputs) {np.sqrt(np.mean(delta ** 2)):.3f} "
+          f"fro {rel_fro(yg, yref):.2e} max/rms {max_err_over_rms(yg, yref):.2e}")
+    if act == moe.MOE_ACT_MXFP8:
+        assert rel_fro(yg, yref) <= MXFP8_FRO and max_err_over_rms(yg, yref) <= MXFP8_MAX
+    else:
+        assert rel_fro(yg, yref) <= BF16_FRO
+
+
+def test_chain_residual_with_zero_weights_returns_x():
+    Ls, lgs, ws = _layers(12, 256, 128, 8, 2, 3, 7)
+    zero = [tuple(torch.zeros_like(a) for a in w) for w in ws]
+    x = dev(LY.host_x(Ls[0]))
+    for act in (moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16):
+        y = _chain(x, lgs, zero, Ls[0], True, act)
+        assert torch.equal(y.view(torch.int16), x.view(torch.int16))
+
+
+def test_chain_output_may_alias_input():
+    Ls, lgs, ws = _layers(16, 256, 128, 8, 2, 2, 11)
+    x = dev(LY.host_x(Ls[0]))
+    want = _chain(x, lgs, ws, Ls[0], True, moe.MOE_ACT_MXFP8)
+    xa = x.clone()
+    moe.moe_mxfp4_forward_chain(xa, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                [w[2] for w in ws], [w[3] for w in ws], 16, 256, 128, 8, 2, xa,
+                                residual=True)
+    assert moe.moe_mxfp4_get_status() == 0
+    assert torch.equal(xa.view(torch.int16), want.view(torch.int16))
+
+
+def test_chain_with_caller_workspace_allocates_nothing():
+    Ls, lgs, ws = _layers(16, 256, 128, 8, 2, 3, 13)
+    x = dev(LY.host_x(Ls[0]))
+    nb = moe.moe_mxfp4_workspace_size_chain(3, 16, 256, 128, 8, 2)
+    wsp = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    y = torch.empty((16, 256), dtype=torch.bfloat16, device="cuda")
+    moe.moe_mxfp4_forward_chain(x, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                [w[2] for w in ws], [w[3] for w in ws], 16, 256, 128, 8, 2, y,
+                                workspace=wsp, workspace_bytes=nb)
+    assert moe.moe_mxfp4_get_status() == 0
+    assert torch.equal(y.view(torch.int16),
+                       _successive(x, lgs, ws, Ls[0], moe.MOE_ACT_MXFP8).view(torch.int16))

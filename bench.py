@@ -331,8 +331,9 @@ def _time_cold(fn, steps, flush_buf):
 
 def measure_next_rows(pk, flush_buf):
     """The steps beside the layer: the router (split-K bf16 GEMM + top-k), the layer with the
-    router in front, a dense MXFP8 projection (K = N = 6144) and the rejection-sampling
-    verification of the drafted block, each against its roofline."""
+    router in front, a dense MXFP8 projection (K = N = 6144), the rejection-sampling
+    verification of the drafted block, each against its roofline, and a chain of 4 layers in
+    one call against 4 successive calls."""
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
     from synth import layers as LY
@@ -408,14 +409,55 @@ def measure_next_rows(pk, flush_buf):
                          20, flush_buf)
     rep["routed_layer_t256"] = {"shape": L.desc + ", router in front", "us_cold": us_r,
                                 "us_cold_layer_on_given_logits": us_l, "issued_as": how}
-    if moe.moe_mxfp4_get_status() != 0:
-        raise RuntimeError("device status error in the next-rows report")
     del wts
     torch.cuda.empty_cache()
+    # a chain of 4 layers (distinct weights and logits) against 4 successive calls
+    for name in ("mid_t8", "full_t8"):
+        chain, succ, n, L = _chain_calls(LY.LAYERS[name], 4)
+        us_c, how = _time_cold(chain, 20, flush_buf)
+        us_s, _ = _time_cold(succ, 20, flush_buf)
+        rep[f"chain_{name}_x{n}"] = {
+            "shape": f"{n} layers of {L.desc.replace(f' seed={L.seed}', '')}, no residual",
+            "us_cold_per_layer_chain": us_c / n, "us_cold_per_layer_successive": us_s / n,
+            "speedup": us_s / us_c, "issued_as": how}
+        del chain, succ
+        torch.cuda.empty_cache()
+    if moe.moe_mxfp4_get_status() != 0:
+        raise RuntimeError("device status error in the next-rows report")
     return rep
 
 
-ROWS = ("router_t8", "router_t256", "dense_fp8_t8", "dense_fp8_t256", "verify_s32_g7")
+def _chain_calls(L0, n, residual=False):
+    """(chain call, n successive calls, n, layer) for n layers shaped like L0 (seeds L0.seed,
+    L0.seed + 1, ...), all inputs on the device"""
+    import torch
+    import mxfp4_expert_layer_dflash_b300 as moe
+    from synth import layers as LY
+    Ls = [LY.Layer(f"{L0.name}_l{l}", L0.H, L0.I, L0.E, L0.k, L0.T, L0.seed + l)
+          for l in range(n)]
+    x = torch.from_numpy(LY.host_x(Ls[0]).view(np.int16)).view(torch.bfloat16).cuda()
+    lgs = [torch.from_numpy(LY.host_logits(L)).cuda() for L in Ls]
+    ws = [LY.device_packed_weights(L, moe.mxfp4_quantize) for L in Ls]
+    y = torch.empty((L0.T, L0.H), dtype=torch.bfloat16, device="cuda")
+    tmp = [torch.empty_like(y) for _ in range(2)]
+    T, H, I, E, k = L0.T, L0.H, L0.I, L0.E, L0.k
+
+    def chain():
+        moe.moe_mxfp4_forward_chain(x, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                    [w[2] for w in ws], [w[3] for w in ws], T, H, I, E, k, y,
+                                    residual=residual)
+
+    def succ():
+        cur = x
+        for l in range(n):
+            out = y if l == n - 1 else tmp[l & 1]
+            moe.moe_mxfp4_forward(cur, lgs[l], *ws[l], T, H, I, E, k, out)
+            cur = out
+    return chain, succ, n, L0
+
+
+ROWS = ("router_t8", "router_t256", "dense_fp8_t8", "dense_fp8_t256", "verify_s32_g7",
+        "chain_mid_t8_x4")
 
 
 def run_row(args):
@@ -445,6 +487,9 @@ def run_row(args):
         del wf
         y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         fn = lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y)  # noqa: E731
+    elif name.startswith("chain"):
+        from synth import layers as LY
+        fn = _chain_calls(LY.LAYERS["mid_t8"], 4)[0]
     else:
         Sq, g, V = 32, 7, 152064
         pv, qv, dv, uv, Uv = S.verify_inputs(1, Sq, g, V)

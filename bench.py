@@ -48,6 +48,12 @@ KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f
 STEP_NAMES = {1: ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"],
               2: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2", "combine"]}
 PATHS = {"auto": 0, "multi": 1, "persistent": 2}
+SMALL_ROUTE_TOKENS = 32  # up to this T the first three steps are one kernel, route_act
+
+
+def step_names(path: int, T: int):
+    names = STEP_NAMES[path]
+    return ["route_act"] + names[3:] if T <= SMALL_ROUTE_TOKENS else names
 
 
 def log(*a):
@@ -542,7 +548,7 @@ def run_ours(args, L, rank, world, local_rank):
 
     act = moe.MOE_ACT_BF16 if args.act == "bf16" else moe.MOE_ACT_MXFP8
     path = PATHS[args.path] or moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E, L.k, act)
-    names = STEP_NAMES[path]
+    names = step_names(path, L.T)
     ev = Events()
     nsteps = len(names) + 1
     marks = [ev.create(nsteps) for _ in range(args.steps)]

@@ -117,8 +117,10 @@ typedef struct {
    * step_events[i] on `stream` just before the i-th kernel of the call and one
    * more after the last (i < n_step_events).  Kernel order: multi path —
    * route_topk, route_permute, act_quant, gemm1, gemm2, combine; persistent
-   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine.
-   * moe_mxfp4_forward_routed puts router_gemm, router_reduce first. */
+   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine.  For
+   * T <= 32 the first three are one kernel, route_act (unless
+   * MOE_DEBUG_SPLIT_ROUTING).  moe_mxfp4_forward_routed puts router_gemm,
+   * router_reduce first. */
   cudaEvent_t* step_events;
   int n_step_events;
 } moe_opts;
@@ -133,6 +135,10 @@ typedef struct {
  * y is unspecified.  Exercises the device timeout path without any fault;
  * ignored by the other paths. */
 #define MOE_DEBUG_FORCE_DEP_TIMEOUT 2u
+/* debug_flags: run routing and the activation step as three kernels even for
+ * T <= 32 (where they are normally one kernel); the results are identical —
+ * used by the tests to compare the two */
+#define MOE_DEBUG_SPLIT_ROUTING 4u
 
 /*
  * moe_mxfp4_forward_ex — moe_mxfp4_forward with options (NULL opts = defaults).

@@ -25,6 +25,7 @@
 #include "gemm_tc.cuh"
 #include "quant.cuh"
 #include "route.cuh"
+#include "route_small.cuh"
 #include "verify.cuh"
 
 namespace moe {
@@ -62,6 +63,27 @@ struct Steps {
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// the fused small-block routing kernel's largest shared memory (T = 32,
+// E = MOE_MAX_E, k = MOE_MAX_K), for every instantiation
+bool set_small_route_smem() {
+  const int tk = kSmallRouteTokens * MOE_MAX_K;
+  const int bytes = (int)small_route_smem(kSmallRouteTokens, MOE_MAX_E, MOE_MAX_K,
+                                          std::min(MOE_MAX_E, tk) + tk / kChunkNarrow + 1)
+                        .total;
+  bool ok = true;
+  auto set = [&](auto kernel) {
+    ok = ok && cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    bytes) == cudaSuccess;
+  };
+  set(route_act_small_kernel<4, true>);
+  set(route_act_small_kernel<12, true>);
+  set(route_act_small_kernel<32, true>);
+  set(route_act_small_kernel<4, false>);
+  set(route_act_small_kernel<12, false>);
+  set(route_act_small_kernel<32, false>);
+  return ok;
+}
 
 template <int kN>
 bool set_gemm_smem() {
@@ -204,6 +226,7 @@ int device_state(DeviceState** out) {
         cudaFuncSetAttribute(route_permute_layers_kernel,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              permute_smem) != cudaSuccess ||
+        !set_small_route_smem() ||
         !set_gemm_smem<kChunkNarrow>() || !set_gemm_smem<kChunkWide>() ||
         cudaFuncSetAttribute(dense_tc_kernel<kDenseBf16, kRouterNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -469,6 +492,40 @@ int enqueue_route(const float* logits, bool first, int T, int E, int k, int chun
   return launch_status();
 }
 
+// Steps a1-a4 in one launch for a block of T <= kSmallRouteTokens tokens
+// (route_act_small_kernel); `first`: the call's first kernel (ordinary launch)
+int enqueue_route_act_small(const float* logits, bool first, int act, const uint16_t* x, int T,
+                            int H, int E, int k, int chunk_max, const Work& w, DeviceState* d,
+                            cudaStream_t s, Steps& st) {
+  const int64_t units = (int64_t)T * k * ((H / 32 + 31) / 32);
+  const dim3 grid(grid_for(units, 32, d->sms));
+  const size_t smem = small_route_smem(T, E, k, w.max_chunks).total;
+  st.mark();
+  auto go = [&](auto kernel) {
+    if (first) {
+      kernel<<<grid, 1024, smem, s>>>(logits, x, T, H, E, k, w.max_chunks, chunk_max, w.topk_idx,
+                                      w.topk_w, w.cnt, w.off, w.perm, w.pos, w.chunks, w.meta,
+                                      w.done, w.xq, w.xs, d->status);
+      return cudaGetLastError();
+    }
+    return launch_pdl(kernel, grid, dim3(1024), smem, s, logits, x, T, H, E, k, w.max_chunks,
+                      chunk_max, w.topk_idx, w.topk_w, w.cnt, w.off, w.perm, w.pos, w.chunks,
+                      w.meta, w.done, w.xq, w.xs, d->status);
+  };
+  cudaError_t e;
+  if (act == MOE_ACT_MXFP8)
+    e = E <= 128 ? go(route_act_small_kernel<4, true>)
+        : E <= 384 ? go(route_act_small_kernel<12, true>)
+                   : go(route_act_small_kernel<32, true>);
+  else
+    e = E <= 128 ? go(route_act_small_kernel<4, false>)
+        : E <= 384 ? go(route_act_small_kernel<12, false>)
+                   : go(route_act_small_kernel<32, false>);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  st.launched();
+  return MOE_OK;
+}
+
 // Routing steps (1)-(4) of every layer of a chain in two launches (the first
 // an ordinary launch: it starts the call); layer l's routing block lies
 // l * stride bytes after layer 0's (w0)
@@ -708,11 +765,17 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
                                      timeout_ns, st)))
     return rc;
-  if ((rc = enqueue_route(routed ? w.rlogits : logits, !routed, T, E, k,
-                          wide ? kChunkWide : kChunkNarrow, w, d, stream, st)))
+  const float* lg = routed ? w.rlogits : logits;
+  const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  const int chunk = wide ? kChunkWide : kChunkNarrow;
+  if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
+    if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
+      return rc;
+  } else if ((rc = enqueue_route(lg, !routed, T, E, k, chunk, w, d, stream, st)) ||
+             (rc = enqueue_act(act, x, w, T, H, k, d, stream, st))) {
     return rc;
-  if ((rc = enqueue_act(act, static_cast<const uint16_t*>(x_bf16), w, T, H, k, d, stream, st)) ||
-      (rc = enqueue_gemms(act, path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream, timeout_ns,
+  }
+  if ((rc = enqueue_gemms(act, path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream, timeout_ns,
                           opts, st)))
     return rc;
   const int cap = d->sms * 8;

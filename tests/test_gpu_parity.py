@@ -318,3 +318,32 @@ def test_extreme_scale_codes(O, act):
             assert max_err_over_rms(yg[t], yref[t]) <= MXFP8_MAX
         else:
             assert rel_fro(yg[t], yref[t]) <= BF16_FRO
+
+
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+@pytest.mark.parametrize("T,E,k,ties", [(1, 8, 2, False), (5, 64, 8, False), (8, 384, 8, False),
+                                        (13, 5, 5, True), (16, 1000, 16, False),
+                                        (31, 384, 8, True), (32, 1, 1, False), (32, 64, 16, False)])
+def test_small_block_routing_matches_split_kernels(O, T, E, k, ties, act):
+    """For T <= 32 routing and the activation step run as one kernel; with
+    MOE_DEBUG_SPLIT_ROUTING they run as the three standalone kernels.  Same bits."""
+    H, I = 256, 128
+    L = LY.Layer("small", H, I, E, k, T, 900 + T + E)
+    lg = np.zeros((T, E), np.float32) if ties else LY.host_logits(L)
+    inp = (dev(LY.host_x(L)), dev(lg)) + tuple(LY.device_packed_weights(L, moe.mxfp4_quantize))
+    ys = []
+    for flags in (0, moe.MOE_DEBUG_SPLIT_ROUTING):
+        y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        moe.moe_mxfp4_forward_ex(*inp, T, H, I, E, k, y, act_mode=act, debug_flags=flags)
+        assert moe.moe_mxfp4_get_status() == 0
+        ys.append(y)
+    assert torch.equal(ys[0].view(torch.int16), ys[1].view(torch.int16))
+    if not ties and E <= 64:   # and against the oracle
+        w = _oracle_layer(O, L)
+        wd = tuple(dev(a) for a in w)
+        y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        moe.moe_mxfp4_forward_ex(inp[0], inp[1], *wd, T, H, I, E, k, y, act_mode=act)
+        yg = bf16_to_f64(host_bf16(y))
+        mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_EXACT
+        _, yref, _ = O.moe_forward(LY.host_x(L), lg, *w, k, mode)
+        assert rel_fro(yg, yref) <= (MXFP8_FRO if act == moe.MOE_ACT_MXFP8 else BF16_FRO)

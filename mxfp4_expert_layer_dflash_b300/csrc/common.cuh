@@ -90,6 +90,15 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// largest |v| over the warp in one instruction: non-negative floats order
+// like their bit patterns, so an unsigned max of |v|'s bits is the exact
+// float max for finite values (all 32 lanes must take part)
+__device__ __forceinline__ float warp_max_abs(float v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(__float_as_uint(fabsf(v))));
+  return __uint_as_float(r);
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);

@@ -599,25 +599,43 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ptx::tc_fence_after();
       const uint32_t acc0 = tbase + lane_off + b * C::kAccCols;
       const int row = mt * ph.m_stride + q * 32 + lane;  // output row within the expert
+      // eight tokens (accumulator columns) at a time, computed for all eight
+      // (columns past the chunk exist and are ignored) so their arithmetic
+      // and warp reductions interleave; only the stores are predicated
       for (int n0 = 0; n0 < ch.z; n0 += 8) {
         uint32_t v0[8], v1[8];
         ptx::tmem_ld_x8(acc0 + n0, v0);
         ptx::tmem_ld_x8(acc0 + kNMax + n0, v1);
         ptx::tmem_ld_wait();
+        const int nv = min(8, ch.z - n0);  // warp-uniform
+        const int64_t slot0 = ch.y + n0;
+        if (gated_phase(c.phase)) {
+          // h = silu(gate) * up, then MXFP8 along I: this warp's 32 rows are
+          // one block of 32 of token n0 + t
+          float h[8], amax[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) {
-          if (n0 + t < ch.z) {  // warp-uniform
-            const int64_t slot = ch.y + n0 + t;
-            if (gated_phase(c.phase)) {
-              const float g = __uint_as_float(v0[t]), up = __uint_as_float(v1[t]);
-              const float h = g / (1.0f + expf(-g)) * up;
-              const int code = block_scale_code(warp_max(fabsf(h)), 8);
-              p.hq[slot * ph.out_dim + row] = e4m3_encode_satfinite(h * exp2_exact(127 - code));
-              if (lane == 0) p.hs[slot * (ph.out_dim / 32) + row / 32] = (uint8_t)code;
-            } else {
-              p.yp[slot * ph.out_dim + row] = __uint_as_float(v0[t]);
+          for (int t = 0; t < 8; ++t) {
+            const float g = __uint_as_float(v0[t]);
+            h[t] = __fdividef(g, 1.0f + __expf(-g)) * __uint_as_float(v1[t]);
+          }
+#pragma unroll
+          for (int t = 0; t < 8; ++t) amax[t] = warp_max_abs(h[t]);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            if (t < nv) {
+              const int code = block_scale_code(amax[t], 8);
+              p.hq[(slot0 + t) * ph.out_dim + row] =
+                  e4m3_encode_satfinite(h[t] * exp2_exact(127 - code));
+              if (lane == 0) p.hs[(slot0 + t) * (ph.out_dim / 32) + row / 32] = (uint8_t)code;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            if (t < nv) {
+              p.yp[(slot0 + t) * ph.out_dim + row] = __uint_as_float(v0[t]);
               if (row + 128 < ph.out_dim)
-                p.yp[slot * ph.out_dim + row + 128] = __uint_as_float(v1[t]);
+                p.yp[(slot0 + t) * ph.out_dim + row + 128] = __uint_as_float(v1[t]);
             }
           }
         }

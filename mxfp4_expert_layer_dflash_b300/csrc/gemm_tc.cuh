@@ -75,6 +75,19 @@ struct TcPhase {
                    // for: 4 epilogue warps x tile pairs
 };
 
+// A chain of layers: the next layer's GEMM1, whose first weight tiles the
+// last GEMM launch of a layer prefetches into L2 once its own copies are
+// issued — the weight stream continues while the layer's tail, the hand-off
+// kernel and the next launch run (the pipeline kept in flight across
+// operators: dothoosh.com, section "TileRT").
+struct NextGemm1 {
+  CUtensorMap map_w;    // the next layer's w13, as TcPhase::map_w
+  const int4* chunks;   // the next layer's chunk list (routed before this launch)
+  const int32_t* meta;
+  int R, m_tiles, m_stride, half;
+  int stages;           // K steps of the CTA's first next-layer item to prefetch (0: off)
+};
+
 struct TcParams {
   TcPhase ph[2];  // [0] = the launch's (first) GEMM, [1] = GEMM2 of a persistent launch
   const int4* chunks;
@@ -85,6 +98,7 @@ struct TcParams {
   int* gemm1_done;      // [chunks] GEMM1 epilogue-warp publications per chunk (persistent path)
   int* status;
   unsigned long long timeout_ns;
+  NextGemm1 next;       // next.stages == 0 unless this is a chained layer's last GEMM launch
 };
 
 template <int kNMax>
@@ -348,6 +362,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           look = false;
         }
       }
+    }
+    // a chained layer: prefetch the first K steps of the item this CTA takes
+    // first in the next layer's GEMM1 (items are dealt round-robin over the
+    // same grid, so that is item blockIdx.x)
+    if (ok && p.next.stages > 0 && (int)blockIdx.x < p.next.meta[0] * p.next.m_tiles) {
+      const int4 ch = p.next.chunks[blockIdx.x / p.next.m_tiles];
+      const int row0 = ch.x * p.next.R + ((int)blockIdx.x % p.next.m_tiles) * p.next.m_stride;
+      if (ptx::elect_one()) {
+        for (int ks = 0; ks < p.next.stages; ++ks) {
+          ptx::tma_prefetch_2d(&p.next.map_w, ks * kBlockK, row0);
+          ptx::tma_prefetch_2d(&p.next.map_w, ks * kBlockK, row0 + p.next.half);
+        }
+      }
+      __syncwarp();
     }
     // every copy of this CTA is issued: the next kernel may be scheduled
     grid_launch_dependents();

@@ -340,6 +340,10 @@ Work carve(void* base, const Layout& L) {
   return w;
 }
 
+// K steps of the next layer's first GEMM1 item each CTA prefetches into L2
+// (2 x 8 KB of packed weights per step; 148 CTAs x 8 steps ~ 19 MB)
+constexpr int kChainPrefetchStages = 8;
+
 // A chain of n layers: n routing blocks one stride apart (a routing block is
 // the first regions of a layer's layout, topk_idx .. meta), then the rest of
 // one layer's layout (the activation buffers the layers share in turn), then
@@ -593,10 +597,12 @@ int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, 
 }
 
 // steps a5-a7: the two grouped GEMMs (one persistent launch or two)
+// `next` (a chained layer, MXFP8 mode): the last GEMM launch prefetches the
+// next layer's first GEMM1 weight tiles into L2
 int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                   const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
                   DeviceState* d, cudaStream_t stream, unsigned long long timeout_ns,
-                  const moe_opts* opts, Steps& st) {
+                  const moe_opts* opts, Steps& st, const NextGemm1* next = nullptr) {
   const int TK = T * k;
   const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
   int rc = MOE_OK;
@@ -651,6 +657,7 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       p.gemm1_done = w.done;
       p.ph[0] = g1;
       p.ph[1] = g2;
+      if (next) p.next = *next;
       st.mark();
       const cudaError_t e = launch(kModeBoth, p);
       if (e == cudaErrorCooperativeLaunchTooLarge) {
@@ -666,9 +673,11 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       p.gemm1_done = nullptr;
       p.ph[1] = TcPhase{};
       p.ph[0] = g1;
+      p.next = NextGemm1{};  // only the layer's last launch prefetches
       st.mark();
       if (launch(kModeGemm1, p) != cudaSuccess) return MOE_ERR_CUDA;
       p.ph[0] = g2;
+      p.next = next ? *next : NextGemm1{};
       st.mark();
       if (launch(kModeGemm2, p) != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -839,8 +848,22 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
   const int64_t threads = (int64_t)T * H / 4;
   for (int l = 0; l < n; ++l) {
     const Work w = carve_chain(ws, C, l);
+    NextGemm1 nx{};
+    if (l + 1 < n) {  // the next layer's first GEMM1 weight tiles, prefetched into L2
+      const Work wn = carve_chain(ws, C, l + 1);
+      if ((rc = make_map(&nx.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13[l + 1], H,
+                         (uint64_t)E * 2 * I, H / 2, 128, 128)))
+        return rc;
+      nx.chunks = wn.chunks;
+      nx.meta = wn.meta;
+      nx.R = 2 * I;
+      nx.m_tiles = I / 128;
+      nx.m_stride = 128;
+      nx.half = I;
+      nx.stages = std::min(kChainPrefetchStages, H / 128);
+    }
     if ((rc = enqueue_gemms(act, path, w13[l], w13s[l], w2[l], w2s[l], T, H, I, E, k, w, d,
-                            stream, timeout_ns, opts, st)))
+                            stream, timeout_ns, opts, st, l + 1 < n ? &nx : nullptr)))
       return rc;
     const bool last = l == n - 1;
     const uint16_t* x_res = residual ? (l == 0 ? x : xb[l & 1]) : nullptr;

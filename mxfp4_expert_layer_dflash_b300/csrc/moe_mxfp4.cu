@@ -576,21 +576,19 @@ int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
              : MOE_PATH_MULTI;
 }
 
-// step a4: gather x rows into slot order, MXFP8-quantised or copied as bf16
+// step a4: x rows into slot order, MXFP8-quantised or copied as bf16; each
+// token's row is read once and written to its k slots (pos from the routing)
 int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, DeviceState* d,
                 cudaStream_t stream, Steps& st) {
-  const int TK = T * k;
-  const int cap = d->sms * 8;
+  const int64_t units = (int64_t)T * ((H / 32 + 31) / 32);
+  const dim3 grid(grid_for(units, 8, d->sms * 8));
   st.mark();
   const cudaError_t qe =
       act == MOE_ACT_MXFP8
-          ? launch_pdl(mxfp8_rows_kernel, dim3(grid_for((int64_t)TK * ((H / 32 + 31) / 32), 8, cap)),
-                       dim3(256), 0, stream, x,
-                       (const int32_t*)w.perm, (int64_t)TK, (int64_t)H, (int64_t)T, w.xq, w.xs,
-                       d->status)
-          : launch_pdl(gather_bf16_rows_kernel, dim3(grid_for(TK, 8, cap)), dim3(256), 0, stream,
-                       x, (const int32_t*)w.perm, (int64_t)TK, (int64_t)H, (int64_t)T,
-                       reinterpret_cast<uint16_t*>(w.xq), d->status);
+          ? launch_pdl(act_tokens_kernel<true>, grid, dim3(256), 0, stream, x,
+                       (const int32_t*)w.pos, T, k, (int64_t)H, w.xq, w.xs, d->status)
+          : launch_pdl(act_tokens_kernel<false>, grid, dim3(256), 0, stream, x,
+                       (const int32_t*)w.pos, T, k, (int64_t)H, w.xq, w.xs, d->status);
   if (qe != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
   return MOE_OK;

@@ -135,27 +135,52 @@ __global__ void __launch_bounds__(256) mxfp8_rows_f32_kernel(const float* __rest
   }
 }
 
-// bf16 mode of a4: gather rows unchanged
-__global__ void __launch_bounds__(256) gather_bf16_rows_kernel(const uint16_t* __restrict__ x,
-                                                               const int32_t* __restrict__ row_map,
-                                                               int64_t rows, int64_t K,
-                                                               int64_t src_rows,
-                                                               uint16_t* __restrict__ out,
-                                                               int* status) {
+// Step a4 per token: a warp per (token, run of 32 blocks of 32), a block per
+// lane; each token's row is quantised (MXFP8) or read (bf16) once and written
+// to its k slot rows pos[t*k + j] — the same bytes as the per-slot kernels
+// with k times fewer loads.
+template <bool kMxfp8>
+__global__ void __launch_bounds__(256) act_tokens_kernel(const uint16_t* __restrict__ x,
+                                                         const int32_t* __restrict__ pos, int T,
+                                                         int k, int64_t K, uint8_t* __restrict__ q,
+                                                         uint8_t* __restrict__ s, int* status) {
   grid_dependency_wait();
   grid_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows;
-       r += warps) {
-    int64_t src = row_map[r];
-    if (src < 0 || src >= src_rows) {
-      if (lane == 0) set_status(status, kStatusFault);
-      src = 0;
+  const int64_t nb = K / 32, segs = (nb + 31) / 32, slots = (int64_t)T * k;
+  for (int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+       u < (int64_t)T * segs; u += warps) {
+    const int64_t t = u / segs;
+    const int64_t b = (u - t * segs) * 32 + lane;
+    if (b >= nb) continue;
+    uint8_t c[32];
+    int code = 0;
+    uint4 raw[4];
+    if (kMxfp8) {
+      float v[32];
+      load_bf16x32(x + t * K + b * 32, v);
+      code = mxfp8_block(v, c);
+    } else {
+      const uint4* a = reinterpret_cast<const uint4*>(x + t * K + b * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) raw[i] = a[i];
     }
-    const uint4* a = reinterpret_cast<const uint4*>(x + src * K);
-    uint4* o = reinterpret_cast<uint4*>(out + r * K);
-    for (int64_t i = lane; i < K / 8; i += 32) o[i] = a[i];
+    for (int j = 0; j < k; ++j) {
+      const int64_t slot = pos[t * k + j];
+      if (slot < 0 || slot >= slots) {
+        set_status(status, kStatusFault);
+        continue;
+      }
+      if (kMxfp8) {
+        store_u8x32(q + slot * K + b * 32, c);
+        s[slot * nb + b] = (uint8_t)code;
+      } else {
+        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + slot * K + b * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o[i] = raw[i];
+      }
+    }
   }
 }
 

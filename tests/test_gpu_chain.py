@@ -136,3 +136,31 @@ def test_chain_with_caller_workspace_allocates_nothing():
     assert moe.moe_mxfp4_get_status() == 0
     assert torch.equal(y.view(torch.int16),
                        _successive(x, lgs, ws, Ls[0], moe.MOE_ACT_MXFP8).view(torch.int16))
+
+
+def test_chain_of_the_most_layers():
+    """MOE_MAX_CHAIN layers: every layer's logits pointer travels in the routing launch's
+    parameters and every routing block sits one stride further into the workspace.  Bitwise
+    against successive calls; then, with zero weights in every layer but the last and the
+    residual on, the block reaches the last layer unchanged, so the result depends on the last
+    layer's routing block and logits: checked against the oracle's chain."""
+    from oracle import oracle as O
+    n = moe.MOE_MAX_CHAIN
+    Ls, lgs, ws = _layers(6, 128, 128, 4, 2, n, 4000)
+    x = dev(LY.host_x(Ls[0]))
+    for act in (moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16):
+        yc = _chain(x, lgs, ws, Ls[0], False, act)
+        ys = _successive(x, lgs, ws, Ls[0], act)
+        assert torch.equal(yc.view(torch.int16), ys.view(torch.int16))
+    lgh = [LY.host_logits(L) for L in Ls]
+    last = LY.host_packed_weights(Ls[-1], O.mxfp4_quantize)
+    last = (last[0], last[1] + 2, last[2], last[3] + 2)      # x 4: comparable to the stream
+    zero = tuple(np.zeros_like(a) for a in last)
+    wh = [zero] * (n - 1) + [last]
+    wd = [tuple(torch.zeros_like(a) for a in ws[0])] * (n - 1) + [tuple(dev(a) for a in last)]
+    y = _chain(x, [dev(a) for a in lgh], wd, Ls[0], True, moe.MOE_ACT_MXFP8)
+    xh = LY.host_x(Ls[0])
+    yref = bf16_to_f64(O.moe_chain(xh, lgh, wh, 2, O.ACT_MXFP8, residual=True))
+    yg = bf16_to_f64(host_bf16(y))
+    assert float(np.abs(yref - bf16_to_f64(xh)).max()) > 0.1   # the last layer does move it
+    assert rel_fro(yg, yref) <= MXFP8_FRO and max_err_over_rms(yg, yref) <= MXFP8_MAX

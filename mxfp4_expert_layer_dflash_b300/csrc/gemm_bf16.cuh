@@ -39,20 +39,25 @@ namespace moe {
 
 constexpr int kBfThreads = 768;        // 24 warps
 constexpr int kBfDecoders = 16;        // decoder warps (8..23)
-constexpr int kBfNMax = kChunkNarrow;  // tokens per item (bf16 mode uses narrow chunks)
-constexpr int kBfPackedTile = 128 * 64;                // 128 rows x 128 FP4 (packed)
-constexpr int kBfBHalf = kBfNMax * 128;                // kBfNMax rows x 64 bf16
-constexpr int kBfStageBytes = 2 * kBfPackedTile + 2 * kBfBHalf;
-constexpr int kBfStages = (232448 - 1024 - 256) / kBfStageBytes;
-constexpr int kBfDecBufs = 3;                          // decoded-A buffers in TMEM
-constexpr int kBfAccCols = 2 * kBfNMax;                // gate|up (or lo|hi) accumulators
-constexpr int kBfDecCol0 = 2 * kBfAccCols;             // first TMEM column of decoded A
-constexpr int kBfDecCols = 2 * 64;                     // two tiles x 64 columns (128 bf16)
-constexpr size_t kBfSmem = 1024 + (size_t)kBfStages * kBfStageBytes + 256;
-static_assert(kBfStageBytes % 1024 == 0, "stage alignment");
-static_assert(kBfDecCol0 + kBfDecBufs * kBfDecCols <= 512, "TMEM budget");
-static_assert(kBfSmem <= 232448, "shared memory budget");
-static_assert(kBfNMax % 16 == 0 && kBfNMax <= 64, "token block");
+// Per token-chunk width kNMax (32, or 64 for large token counts: fewer
+// chunks per expert, so each expert's weights are decoded fewer times).
+template <int kNMax>
+struct BfCfg {
+  static constexpr int kPackedTile = 128 * 64;                  // 128 rows x 128 FP4 (packed)
+  static constexpr int kBHalf = kNMax * 128;                    // kNMax rows x 64 bf16
+  static constexpr int kStageBytes = 2 * kPackedTile + 2 * kBHalf;
+  static constexpr int kStages = (232448 - 1024 - 256) / kStageBytes;
+  static constexpr int kAccCols = 2 * kNMax;                    // gate|up (or lo|hi) accumulators
+  static constexpr int kDecCol0 = 2 * kAccCols;                 // first TMEM column of decoded A
+  static constexpr int kDecCols = 2 * 64;                       // two tiles x 64 columns
+  static constexpr int kDecBufs = (512 - kDecCol0) / kDecCols;  // decoded-A buffers: 3 or 2
+  static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
+  static_assert(kStageBytes % 1024 == 0, "stage alignment");
+  static_assert(kDecBufs >= 2 && kDecCol0 + kDecBufs * kDecCols <= 512, "TMEM budget");
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kNMax % 16 == 0 && kNMax <= 64, "token block");
+  static_assert(8 * (2 * kStages + 2 * kDecBufs + 5) + 8 <= 256, "barrier area");
+};
 
 struct BfParams {
   CUtensorMap map_w;    // packed FP4 weights [E*R rows, K/2 bytes], u8 box {64, 128}, 64B swizzle
@@ -146,16 +151,17 @@ __device__ __forceinline__ void bf_decode_half(const uint4 (&packed)[2], uint32_
   tmem_st_x32(taddr, out);
 }
 
-template <bool kGated>
+template <int kNMax, bool kGated>
 __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_constant__ BfParams p) {
+  using C = BfCfg<kNMax>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kBfStages * kBfStageBytes);
-  uint64_t* empty = full + kBfStages;
-  uint64_t* dec_full = empty + kBfStages;
-  uint64_t* dec_empty = dec_full + kBfDecBufs;
-  uint64_t* acc_full = dec_empty + kBfDecBufs;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
+  uint64_t* empty = full + C::kStages;
+  uint64_t* dec_full = empty + C::kStages;
+  uint64_t* dec_empty = dec_full + C::kDecBufs;
+  uint64_t* acc_full = dec_empty + C::kDecBufs;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -163,11 +169,11 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kBfStages; ++s) {
+    for (int s = 0; s < C::kStages; ++s) {
       ptx::mbar_init(&full[s], 1);       // TMA arrive.expect_tx
       ptx::mbar_init(&empty[s], 1 + kBfDecoders);  // MMA commit (B read) + decoders (A read)
     }
-    for (int d = 0; d < kBfDecBufs; ++d) {
+    for (int d = 0; d < C::kDecBufs; ++d) {
       ptx::mbar_init(&dec_full[d], kBfDecoders);
       ptx::mbar_init(&dec_empty[d], 1);  // MMA commit
     }
@@ -214,23 +220,23 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
       const int mt = item % p.m_tiles;
       const int nrows = (ch.z + 15) & ~15;
       const int row0 = ch.x * p.R + mt * p.m_stride;
-      const uint32_t tx = 2u * kBfPackedTile + 2u * (uint32_t)nrows * 128u;
+      const uint32_t tx = 2u * C::kPackedTile + 2u * (uint32_t)nrows * 128u;
       for (int ks = 0; ks < ksteps; ++ks, ++fill) {
-        const int s = (int)(fill % kBfStages);
-        const uint32_t use = fill / kBfStages;
+        const int s = (int)(fill % C::kStages);
+        const uint32_t use = fill / C::kStages;
         if (!wait_all(&empty[s], (use & 1) ^ 1)) {
           if (lane == 0) fail(kStatusTimeout);
           ok = false;
           break;
         }
-        uint8_t* st = smem + s * kBfStageBytes;
+        uint8_t* st = smem + s * C::kStageBytes;
         ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
         ptx::tma_load_2d_warp(st, &p.map_w, &full[s], ks * 64, row0, pol_w);
-        ptx::tma_load_2d_warp(st + kBfPackedTile, &p.map_w, &full[s], ks * 64, row0 + p.half,
+        ptx::tma_load_2d_warp(st + C::kPackedTile, &p.map_w, &full[s], ks * 64, row0 + p.half,
                               pol_w);
         for (int h = 0; h < 2; ++h)
           for (int r = 0; r < nrows; r += 16)
-            ptx::tma_load_2d_warp(st + 2 * kBfPackedTile + h * kBfBHalf + r * 128, &p.map_x,
+            ptx::tma_load_2d_warp(st + 2 * C::kPackedTile + h * C::kBHalf + r * 128, &p.map_x,
                                   &full[s], ks * 128 + h * 64, ch.y + r, pol_x);
       }
     }
@@ -251,27 +257,27 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t acc = tbase + b * kBfAccCols;
+      const uint32_t acc = tbase + b * C::kAccCols;
       for (int ks = 0; ks < ksteps; ++ks, ++fill) {
-        const int s = (int)(fill % kBfStages);
-        const uint32_t use = fill / kBfStages;
-        const int d = (int)(fill % kBfDecBufs);
-        const uint32_t duse = fill / kBfDecBufs;
+        const int s = (int)(fill % C::kStages);
+        const uint32_t use = fill / C::kStages;
+        const int d = (int)(fill % C::kDecBufs);
+        const uint32_t duse = fill / C::kDecBufs;
         if (!wait_all(&full[s], use & 1) || !wait_all(&dec_full[d], duse & 1)) {
           if (lane == 0) fail(kStatusTimeout);
           ok = false;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t sb = ptx::smem_u32(smem + s * kBfStageBytes + 2 * kBfPackedTile);
-        const uint32_t a0 = tbase + kBfDecCol0 + d * kBfDecCols;
+        const uint32_t sb = ptx::smem_u32(smem + s * C::kStageBytes + 2 * C::kPackedTile);
+        const uint32_t a0 = tbase + C::kDecCol0 + d * C::kDecCols;
 #pragma unroll
         for (int t = 0; t < 2; ++t) {
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t accum = (ks | kk) ? 1u : 0u;
-            mma_bf16_tmem_a_warp(acc + t * kBfNMax, a0 + t * 64 + kk * 8,
-                                 ptx::desc_kmajor_sw128(sb + (kk >> 2) * kBfBHalf + 32 * (kk & 3)),
+            mma_bf16_tmem_a_warp(acc + t * kNMax, a0 + t * 64 + kk * 8,
+                                 ptx::desc_kmajor_sw128(sb + (kk >> 2) * C::kBHalf + 32 * (kk & 3)),
                                  idesc, accum);
           }
         }
@@ -320,9 +326,9 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
     for (int i = 0; i < kRing; ++i) load_sw(sw[i]);
     // per-lane constants: the row's two swizzled 16-byte chunks (64B swizzle:
     // chunk c of a 64-byte row sits at c ^ ((r >> 1) & 3)) and its TMEM columns
-    const uint32_t off0 = t * kBfPackedTile + r * 64 + (((2 * kh) ^ ((r >> 1) & 3)) << 4);
-    const uint32_t off1 = t * kBfPackedTile + r * 64 + (((2 * kh + 1) ^ ((r >> 1) & 3)) << 4);
-    const uint32_t tcol0 = tbase + lane_off + kBfDecCol0 + t * 64 + kh * 32;
+    const uint32_t off0 = t * C::kPackedTile + r * 64 + (((2 * kh) ^ ((r >> 1) & 3)) << 4);
+    const uint32_t off1 = t * C::kPackedTile + r * 64 + (((2 * kh + 1) ^ ((r >> 1) & 3)) << 4);
+    const uint32_t tcol0 = tbase + lane_off + C::kDecCol0 + t * 64 + kh * 32;
     int s = 0, d = 0;
     uint32_t full_par = 0, dec_par = 1;
     for (uint32_t fill = 0; fill < n_fills;) {
@@ -335,11 +341,11 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
             break;
           }
           ptx::tc_fence_after();
-          const uint8_t* st = smem + s * kBfStageBytes;
+          const uint8_t* st = smem + s * C::kStageBytes;
           uint4 pk[2];
           pk[0] = *reinterpret_cast<const uint4*>(st + off0);
           pk[1] = *reinterpret_cast<const uint4*>(st + off1);
-          const uint32_t taddr = tcol0 + d * kBfDecCols;
+          const uint32_t taddr = tcol0 + d * C::kDecCols;
           if (__all_sync(0xffffffffu, (sw[i] & 0xFFu) <= 128u && (sw[i] >> 8) <= 128u))
             bf_decode_half<false>(pk, sw[i], taddr);
           else
@@ -352,11 +358,11 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
             ptx::mbar_arrive(&empty[s]);
           }
           load_sw(sw[i]);
-          if (++s == kBfStages) {
+          if (++s == C::kStages) {
             s = 0;
             full_par ^= 1;
           }
-          if (++d == kBfDecBufs) {
+          if (++d == C::kDecBufs) {
             d = 0;
             dec_par ^= 1;
           }
@@ -378,12 +384,12 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
         break;
       }
       ptx::tc_fence_after();
-      const uint32_t acc0 = tbase + lane_off + b * kBfAccCols;
+      const uint32_t acc0 = tbase + lane_off + b * C::kAccCols;
       const int row = mt * p.m_stride + q * 32 + lane;  // output row within the expert
       for (int n0 = 0; n0 < ch.z; n0 += 8) {
         uint32_t v0[8], v1[8];
         ptx::tmem_ld_x8(acc0 + n0, v0);
-        ptx::tmem_ld_x8(acc0 + kBfNMax + n0, v1);
+        ptx::tmem_ld_x8(acc0 + kNMax + n0, v1);
         ptx::tmem_ld_wait();
 #pragma unroll
         for (int tt = 0; tt < 8; ++tt) {

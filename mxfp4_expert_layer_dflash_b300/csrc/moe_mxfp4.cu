@@ -64,6 +64,24 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
+template <int kN>
+bool set_bf16_smem() {
+  const int bytes = (int)BfCfg<kN>::kSmem;
+  return cudaFuncSetAttribute(gemm_bf16_kernel<kN, true>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_bf16_kernel<kN, false>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+// Token-chunk width (slots per GEMM work item): narrow chunks keep the weight
+// pipeline deepest; from kWideMinTokens tokens on, experts get many tokens and
+// wide chunks cut the MMA instructions per token (MXFP8 mode) or the decodes
+// of each expert's weights (bf16 mode).
+int chunk_for(int act, int T) {
+  if (T < kWideMinTokens) return kChunkNarrow;
+  return act == MOE_ACT_MXFP8 ? kChunkWide : kChunkBf16Wide;
+}
+
 // the fused small-block routing kernel's largest shared memory (T = 32,
 // E = MOE_MAX_E, k = MOE_MAX_K), for every instantiation
 bool set_small_route_smem() {
@@ -234,10 +252,7 @@ int device_state(DeviceState** out) {
         cudaFuncSetAttribute(dense_tc_kernel<kDenseMxf8, kDenseNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DenseCfg<kDenseMxf8, kDenseNMax>::kSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_bf16_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kBfSmem) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm_bf16_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kBfSmem) != cudaSuccess)
+        !set_bf16_smem<kChunkNarrow>() || !set_bf16_smem<kChunkBf16Wide>())
       return MOE_ERR_CUDA;
     d.ready = true;
   }
@@ -603,6 +618,7 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
                   const moe_opts* opts, Steps& st, const NextGemm1* next = nullptr) {
   const int TK = T * k;
   const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
+  const bool bf_wide = chunk_for(act, T) == kChunkBf16Wide;
   int rc = MOE_OK;
   if (act == MOE_ACT_MXFP8) {
     TcPhase g1{}, g2{};
@@ -716,12 +732,18 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
     b2.out_dim = H;
     b2.rows_total = E * H;
     st.mark();
-    if (launch_pdl(gemm_bf16_kernel<true>, dim3(d->sms), dim3(kBfThreads), kBfSmem, stream, b1) !=
+    if ((bf_wide ? launch_pdl(gemm_bf16_kernel<kChunkBf16Wide, true>, dim3(d->sms),
+                              dim3(kBfThreads), BfCfg<kChunkBf16Wide>::kSmem, stream, b1)
+                 : launch_pdl(gemm_bf16_kernel<kChunkNarrow, true>, dim3(d->sms),
+                              dim3(kBfThreads), BfCfg<kChunkNarrow>::kSmem, stream, b1)) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     st.launched();
     st.mark();
-    if (launch_pdl(gemm_bf16_kernel<false>, dim3(d->sms), dim3(kBfThreads), kBfSmem, stream, b2) !=
+    if ((bf_wide ? launch_pdl(gemm_bf16_kernel<kChunkBf16Wide, false>, dim3(d->sms),
+                              dim3(kBfThreads), BfCfg<kChunkBf16Wide>::kSmem, stream, b2)
+                 : launch_pdl(gemm_bf16_kernel<kChunkNarrow, false>, dim3(d->sms),
+                              dim3(kBfThreads), BfCfg<kChunkNarrow>::kSmem, stream, b2)) !=
         cudaSuccess)
       return MOE_ERR_CUDA;
     st.launched();
@@ -765,7 +787,6 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
 
   // Wide token chunks halve the MMA instructions per token when experts get
   // many tokens (large T); narrow chunks keep the weight pipeline deepest.
-  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
   const unsigned long long timeout_ns =
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
@@ -774,7 +795,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     return rc;
   const float* lg = routed ? w.rlogits : logits;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
-  const int chunk = wide ? kChunkWide : kChunkNarrow;
+  const int chunk = chunk_for(act, T);
   if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
     if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
       return rc;
@@ -834,11 +855,10 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
   if (!ws && (rc = cached_workspace(d, C.total, &ws))) return rc;
   uint16_t* xb[2] = {reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + C.xb[0]),
                      reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + C.xb[1])};
-  const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
   const unsigned long long timeout_ns =
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
-  if ((rc = enqueue_route_layers(logits, n, T, E, k, wide ? kChunkWide : kChunkNarrow,
+  if ((rc = enqueue_route_layers(logits, n, T, E, k, chunk_for(act, T),
                                  carve_chain(ws, C, 0), (int64_t)C.route_block, d, stream, st)))
     return rc;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);

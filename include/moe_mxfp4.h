@@ -139,6 +139,11 @@ typedef struct {
  * T <= 32 (where they are normally one kernel); the results are identical —
  * used by the tests to compare the two */
 #define MOE_DEBUG_SPLIT_ROUTING 4u
+/* debug_flags: in the bf16 mode, GEMM1's MMA warp never hands decoded weight
+ * buffers back to the decoders, so their bounded wait runs out (~1 ms with
+ * MOE_DEBUG_SHORT_TIMEOUT): the call reports MOE_ERR_DEVICE_TIMEOUT and y is
+ * unspecified.  Exercises that kernel's timeout path without any fault. */
+#define MOE_DEBUG_STALL_DECODE 8u
 
 /*
  * moe_mxfp4_forward_ex — moe_mxfp4_forward with options (NULL opts = defaults).

@@ -21,6 +21,7 @@ MOE_PATH_AUTO, MOE_PATH_MULTI, MOE_PATH_PERSISTENT = 0, 1, 2
 MOE_DEBUG_SHORT_TIMEOUT = 1
 MOE_DEBUG_FORCE_DEP_TIMEOUT = 2
 MOE_DEBUG_SPLIT_ROUTING = 4
+MOE_DEBUG_STALL_DECODE = 8
 MOE_ERR_DEVICE_TIMEOUT = -6
 MOE_MAX_K, MOE_MAX_E, MOE_MAX_CHAIN = 16, 1024, 256
 MOE_NOALLOC_SCRATCH_BYTES = 80 * 1024 * 1024

@@ -70,6 +70,7 @@ struct BfParams {
   int K, R, m_tiles, m_stride, half, out_dim, rows_total;
   int* status;
   unsigned long long timeout_ns;
+  int stall_decode;  // debug: decoded buffers are never handed back (the wait runs out)
 };
 
 // D[tmem] (+)= A[tmem] x B[smem]^T, bf16, fp32 accumulation; warp-collective
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kBfThreads, 1) gemm_bf16_kernel(const __grid_c
           }
         }
         ptx::mma_commit_warp(&empty[s]);      // the activation tile is read
-        ptx::mma_commit_warp(&dec_empty[d]);  // the decoded weights are read
+        if (!p.stall_decode) ptx::mma_commit_warp(&dec_empty[d]);  // the decoded weights are read
       }
       if (!ok) break;
       ptx::mma_commit_warp(&acc_full[b]);

@@ -714,6 +714,7 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       b->timeout_ns = timeout_ns;
     }
     b1.w_sf = w13s;
+    b1.stall_decode = opts && (opts->debug_flags & MOE_DEBUG_STALL_DECODE) ? 1 : 0;
     b1.hq = reinterpret_cast<uint16_t*>(w.hq);
     b1.K = H;
     b1.R = 2 * I;

@@ -61,3 +61,25 @@ def test_flag_is_ignored_by_the_two_launch_path():
     ref = gpu_forward(L, inp, path=moe.MOE_PATH_MULTI)
     assert torch.equal(y.view(torch.int16), ref.view(torch.int16))
     assert np.isfinite(bf16_to_f64(host_bf16(y))).all()
+
+
+def test_bf16_decode_wait_times_out_and_context_survives(O):
+    """The bf16 mode's GEMM: decoders whose buffers are never handed back give up after the
+    short timeout; every role sees the abort flag, the status reads MOE_ERR_DEVICE_TIMEOUT,
+    and the next normal call is correct."""
+    L = LY.LAYERS["mid_t8"]                  # 16 K steps per item: the decoders need a buffer back
+    inp = device_layer(L)
+    y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
+    assert moe.moe_mxfp4_get_status() == 0
+    moe.moe_mxfp4_forward_ex(*inp, L.T, L.H, L.I, L.E, L.k, y, act_mode=moe.MOE_ACT_BF16,
+                             debug_flags=moe.MOE_DEBUG_SHORT_TIMEOUT | moe.MOE_DEBUG_STALL_DECODE)
+    assert moe.moe_mxfp4_get_status() == moe.MOE_ERR_DEVICE_TIMEOUT
+    assert moe.moe_mxfp4_get_status() == 0
+    yb = gpu_forward(L, inp, act_mode=moe.MOE_ACT_BF16)
+    toks = [0, 3, 7]
+    w = LY.host_packed_weights(L, O.mxfp4_quantize, None)
+    _, yref, _ = O.moe_forward(LY.host_x(L), LY.host_logits(L), *w, L.k, O.ACT_EXACT,
+                               tokens=np.array(toks))
+    assert rel_fro(bf16_to_f64(host_bf16(yb))[toks], yref) <= 5e-3
+    del inp
+    torch.cuda.empty_cache()

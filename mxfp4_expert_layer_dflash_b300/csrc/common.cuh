@@ -22,7 +22,6 @@ constexpr int kChunkNarrow = MOE_CHUNK_NARROW;
 #define MOE_CHUNK_WIDE 96
 #endif
 constexpr int kChunkWide = MOE_CHUNK_WIDE;
-constexpr int kChunkBf16Wide = 64;  // wide chunks of the bf16 mode (its TMEM holds 2 x 2 x 64)
 // layers with at least this many tokens use wide chunks (MXFP8 mode)
 #ifndef MOE_WIDE_MIN_TOKENS
 #define MOE_WIDE_MIN_TOKENS 512

@@ -37,6 +37,7 @@
 
 namespace moe {
 
+constexpr int kChunkBf16Wide = 64;     // wide chunks of this mode (its TMEM holds 2 x 2 x 64)
 constexpr int kBfThreads = 768;        // 24 warps
 constexpr int kBfDecoders = 16;        // decoder warps (8..23)
 // Per token-chunk width kNMax (32, or 64 for large token counts: fewer

@@ -113,8 +113,9 @@ __global__ void __launch_bounds__(256) combine_next_kernel(
 #pragma unroll
       for (int q = 0; q < 4; ++q) codes |= (uint32_t)e4m3_encode_satfinite(v[q] * inv) << (8 * q);
     }
+    const int my_slot = lane < k ? pos_next[t * k + lane] : 0;  // one round trip for k slots
     for (int j = 0; j < k; ++j) {
-      const int64_t slot = pos_next[t * k + j];
+      const int64_t slot = __shfl_sync(0xffffffffu, my_slot, j);
       if (slot < 0 || slot >= slots) {
         set_status(status, kStatusFault);
         continue;

@@ -153,21 +153,26 @@ __global__ void __launch_bounds__(256) act_tokens_kernel(const uint16_t* __restr
        u < (int64_t)T * segs; u += warps) {
     const int64_t t = u / segs;
     const int64_t b = (u - t * segs) * 32 + lane;
-    if (b >= nb) continue;
+    const bool live = b < nb;  // lanes past the row still take part in the shuffles
+    // the token's k slots in one round trip: lane j loads slot j
+    const int my_slot = lane < k ? pos[t * k + lane] : 0;
     uint8_t c[32];
     int code = 0;
     uint4 raw[4];
-    if (kMxfp8) {
-      float v[32];
-      load_bf16x32(x + t * K + b * 32, v);
-      code = mxfp8_block(v, c);
-    } else {
-      const uint4* a = reinterpret_cast<const uint4*>(x + t * K + b * 32);
+    if (live) {
+      if (kMxfp8) {
+        float v[32];
+        load_bf16x32(x + t * K + b * 32, v);
+        code = mxfp8_block(v, c);
+      } else {
+        const uint4* a = reinterpret_cast<const uint4*>(x + t * K + b * 32);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) raw[i] = a[i];
+        for (int i = 0; i < 4; ++i) raw[i] = a[i];
+      }
     }
     for (int j = 0; j < k; ++j) {
-      const int64_t slot = pos[t * k + j];
+      const int64_t slot = __shfl_sync(0xffffffffu, my_slot, j);
+      if (!live) continue;
       if (slot < 0 || slot >= slots) {
         set_status(status, kStatusFault);
         continue;

@@ -126,3 +126,60 @@ def test_rejects_bad_arguments(synth_mod, oracle_mod):
     x, lg, w13, s13, w2, s2 = make_layer(synth_mod, oracle_mod, 2, 64, 32, 2, 1)
     with pytest.raises(ValueError):
         oracle_mod.moe_forward(x, lg, w13, s13, w2, s2, 3)
+
+
+def test_literal_nested_loops_equal_the_oracle_bit_for_bit(synth_mod, oracle_mod):
+    """The layer written out as plain Python loops over tokens, slots, rows and the reduction
+    index — weights decoded from the E2M1 grid and 2^(s - 127), top-k by a linear scan (the
+    first of equal logits kept), softmax of the selected logits, sums in the same index order
+    — gives the oracle's fp64 output exactly (no fused multiply-adds on either side)."""
+    import math
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    T, H, I, E, k = 3, 64, 32, 4, 2
+    x, lg, w13, s13, w2, s2 = make_layer(synth_mod, oracle_mod, T, H, I, E, 77)
+    _, y64, _ = oracle_mod.moe_forward(x, lg, w13, s13, w2, s2, k)
+
+    def wv(fp4, sc, e, r, c):
+        byte = int(fp4[e, r, c // 2])
+        nib = (byte >> 4) if c % 2 else (byte & 0xF)
+        mag = grid[nib & 7] * (-1.0 if nib & 8 else 1.0)
+        return mag * 2.0 ** (int(sc[e, r, c // 32]) - 127)
+
+    want = np.zeros((T, H))
+    for t in range(T):
+        a = [float(R.bf16_to_f64(x[t:t + 1, h:h + 1])[0, 0]) for h in range(H)]
+        taken, sel = set(), []
+        for _ in range(k):
+            best = -1
+            for e in range(E):
+                if e not in taken and (best < 0 or float(lg[t, e]) > float(lg[t, best])):
+                    best = e
+            taken.add(best)
+            sel.append(best)
+        m = float(lg[t, sel[0]])
+        s = 0.0
+        for e in sel:
+            s += math.exp(float(lg[t, e]) - m)
+        g = [math.exp(float(lg[t, e]) - m) / s for e in sel]
+        d = []
+        for e in sel:
+            hv = []
+            for i in range(I):
+                gate = up = 0.0
+                for h in range(H):
+                    gate += wv(w13, s13, e, i, h) * a[h]
+                    up += wv(w13, s13, e, I + i, h) * a[h]
+                hv.append(gate / (1.0 + math.exp(-gate)) * up)
+            row = []
+            for o in range(H):
+                acc = 0.0
+                for i in range(I):
+                    acc += wv(w2, s2, e, o, i) * hv[i]
+                row.append(acc)
+            d.append(row)
+        for o in range(H):
+            acc = 0.0
+            for j in range(k):
+                acc += g[j] * d[j][o]
+            want[t, o] = acc
+    assert (y64 == want).all()

@@ -4,8 +4,12 @@
 // host code validates arguments before any CUDA call, lays out the per-call
 // scratch, and enqueues the steps of the layer on the caller's stream:
 //   route_topk -> route_permute -> act quant/gather -> GEMM1 -> GEMM2 -> combine
-// MXFP8 mode runs the GEMMs on tcgen05 block-scaled MMA fed by TMA; bf16 mode
-// runs them on CUDA cores.
+// (for T <= 32 the first three are one kernel; GEMM1 and GEMM2 are one
+// cooperative launch on layers with a handful of work items per SM).  MXFP8
+// mode runs the GEMMs on tcgen05 block-scaled MMA fed by TMA; bf16 mode
+// decodes the weights to bf16 in tensor memory and runs tcgen05 kind::f16.
+// Beside the layer: the router GEMM, a dense MXFP8 projection, the
+// verification of a drafted block, and a chain of layers in one call.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>

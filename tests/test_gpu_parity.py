@@ -182,6 +182,27 @@ def test_forward_full_size_sampled(O, name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("T,E,seed", [(4096, 384, 8), (256, 1024, 9)])
+def test_forward_extreme_sizes_sampled(O, T, E, seed):
+    """The full per-expert shape at the edges of the supported range: 4096 tokens (32768
+    assignments: the permutation's many passes, wide chunks at scale) and the largest expert
+    count (E = 1024, 20 GB of packed weights).  Sampled tokens against the oracle."""
+    L = LY.Layer(f"edge_t{T}_e{E}", 6144, 2048, E, 8, T, seed)
+    inp = device_layer(L)
+    y = host_bf16(gpu_forward(L, inp))
+    x, lg = LY.host_x(L), LY.host_logits(L)
+    toks = _sample_tokens(T)
+    ridx, _ = O.route(lg[toks], L.k)
+    w = _oracle_layer(O, L, np.unique(ridx))
+    _, yref, _ = O.moe_forward(x, lg, *w, L.k, O.ACT_MXFP8, tokens=toks)
+    yt = bf16_to_f64(y[toks])
+    f, m = rel_fro(yt, yref), max_err_over_rms(yt, yref)
+    print(f"T={T} E={E}: mxfp8 fro={f:.3e} max/rms={m:.3e}")
+    assert f <= MXFP8_FRO and m <= MXFP8_MAX
+    del inp
+    torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------ edge cases and invariants
 
 def _layer_inputs(O, T, H, I, E, k, seed, logits=None):

@@ -693,6 +693,13 @@ def run_ours(args, L, rank, world, local_rank):
             r["tflops_cold"] = flops / (r["us_cold_l2_flushed"] * 1e-6) / 1e12
             # the block-scaled FP4 x FP8 MMA runs at the FP8 rate: 2 x the bf16 peak
             r["tensor_frac_cold"] = r["tflops_cold"] / (2.0 * float(pk["bf16_tflops"]))
+            if not args.no_cpu_baseline:  # the oracle on the first 4 tokens (packing untimed)
+                n_tok = min(4, Lc.T)
+                run, _ = oracle_sample(Lc, n_tok)
+                t0 = time.perf_counter()
+                run(list(range(n_tok)))
+                r["cpu_oracle_tokens_per_s"] = n_tok / (time.perf_counter() - t0)
+                r["cpu_oracle_sample"] = f"first {n_tok} tokens, fp64, MXFP8 emulation, {cpu_cores()} cores"
             rep[tag] = r
         out["configs_report_peaks"] = {
             "hbm_gbs": hbm, "fp8_tflops": 2.0 * float(pk["bf16_tflops"]),

@@ -88,6 +88,8 @@ int chunk_for(int act, int T) {
 
 // the fused small-block routing kernel's largest shared memory (T = 32,
 // E = MOE_MAX_E, k = MOE_MAX_K), for every instantiation
+static_assert(kSmallRouteTokens * MOE_MAX_K <= 1024,
+              "the small-block routing ranks one assignment per thread");
 bool set_small_route_smem() {
   const int tk = kSmallRouteTokens * MOE_MAX_K;
   const int bytes = (int)small_route_smem(kSmallRouteTokens, MOE_MAX_E, MOE_MAX_K,

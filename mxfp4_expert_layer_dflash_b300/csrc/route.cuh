@@ -130,6 +130,34 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
   return r;
 }
 
+// Chunk list of a routed block, by one 1024-thread CTA whose thread e < E
+// holds expert e's count c and first slot excl: touched experts in ascending
+// order, each split into ceil(n / chunk_max) chunks of near-equal size;
+// meta[0] = chunks, meta[1] = touched experts.
+__device__ __forceinline__ void route_chunk_list(int c, int excl, int E, int chunk_max,
+                                                 int4* __restrict__ chunks, int max_chunks,
+                                                 int32_t* __restrict__ meta, int* s_warp,
+                                                 int* s_tot, int* status) {
+  const int tid = threadIdx.x;
+  const int nch = c > 0 ? (c + chunk_max - 1) / chunk_max : 0;
+  const int cbase = block_exclusive_scan_1024(nch, s_warp, &s_tot[0]);
+  const int touched = block_exclusive_scan_1024(c > 0 ? 1 : 0, s_warp, &s_tot[1]);
+  (void)touched;
+  if (tid < E && nch > 0) {
+    const int q = (c + nch - 1) / nch;
+    for (int i = 0; i < nch; ++i) {
+      const int b = cbase + i;
+      const int n = min(q, c - i * q);
+      if (b < max_chunks) chunks[b] = make_int4(tid, excl + i * q, n, 0);
+      else set_status(status, kStatusFault);
+    }
+  }
+  if (tid == 0) {
+    meta[0] = min(s_tot[0], max_chunks);
+    meta[1] = s_tot[1];
+  }
+}
+
 // Steps (2)-(4) by one CTA of 1024 threads: histogram, scan, stable
 // permutation, chunk list.  Dynamic shared memory: (35 * E + 1 + 34) ints.
 __device__ __forceinline__ void route_permute_cta(
@@ -207,25 +235,7 @@ __device__ __forceinline__ void route_permute_cta(
     __syncthreads();
   }
 
-  // chunk list: touched experts in ascending order, each split into
-  // ceil(n / chunk_max) chunks of near-equal size
-  const int nch = c > 0 ? (c + chunk_max - 1) / chunk_max : 0;
-  const int cbase = block_exclusive_scan_1024(nch, s_warp, &s_tot[0]);
-  const int touched = block_exclusive_scan_1024(c > 0 ? 1 : 0, s_warp, &s_tot[1]);
-  (void)touched;
-  if (tid < E && nch > 0) {
-    const int q = (c + nch - 1) / nch;
-    for (int i = 0; i < nch; ++i) {
-      const int b = cbase + i;
-      const int n = min(q, c - i * q);
-      if (b < max_chunks) chunks[b] = make_int4(tid, excl + i * q, n, 0);
-      else set_status(status, kStatusFault);
-    }
-  }
-  if (tid == 0) {
-    meta[0] = min(s_tot[0], max_chunks);
-    meta[1] = s_tot[1];
-  }
+  route_chunk_list(c, excl, E, chunk_max, chunks, max_chunks, meta, s_warp, s_tot, status);
 }
 
 __global__ void __launch_bounds__(1024) route_permute_kernel(

@@ -4,11 +4,13 @@
 // dothoosh.com, section "TileRT").
 //
 // Every CTA recomputes the whole routing of the block in its own shared
-// memory (at most 32 tokens: one warp per token for the top-k, then one CTA's
-// histogram / scan / stable permutation / chunk list — the same device code
-// as the three-kernel path, so the results are identical), CTA 0 publishes
-// the routing arrays, and every CTA then gathers and quantises its share of
-// the slot rows (MXFP8, blocks of 32 along H) or copies them (bf16 mode).
+// memory (at most 32 tokens: one warp per token for the top-k — the
+// three-kernel path's device code — then histogram, scan, stable permutation
+// and chunk list for at most 512 assignments, where each assignment's rank
+// within its expert is a direct count of the earlier equal ones: the same
+// arrays as the general permutation, bit for bit), CTA 0 publishes the
+// routing arrays, and every CTA then gathers and quantises its share of the
+// slot rows (MXFP8, blocks of 32 along H) or copies them (bf16 mode).
 // Redundant routing costs a few microseconds of L2 reads of the [T, E]
 // logits per CTA; it removes two launches and their dependency waits.
 #pragma once
@@ -21,9 +23,8 @@ namespace moe {
 
 constexpr int kSmallRouteTokens = 32;  // one warp per token in a 1024-thread CTA
 
-// Shared memory of route_act_small_kernel: the permutation's own region
-// ((35 E + 35) ints at offset 0, see route_permute_cta), then this block's
-// routing arrays.
+// Shared memory of route_act_small_kernel: the block scans' scratch (64 ints
+// at offset 0), then this block's routing arrays.
 struct SmallRouteSmem {
   size_t idx, gate, cnt, off, perm, pos, chunks, meta, total;
 };
@@ -31,7 +32,7 @@ struct SmallRouteSmem {
 __host__ __device__ inline SmallRouteSmem small_route_smem(int T, int E, int k, int max_chunks) {
   auto up16 = [](size_t b) { return (b + 15) & ~size_t(15); };
   SmallRouteSmem L{};
-  size_t o = up16((size_t)(35 * E + 35) * sizeof(int));
+  size_t o = 64 * sizeof(int);
   const size_t tk = (size_t)T * k;
   L.idx = o;
   o = up16(o + tk * 4);
@@ -76,11 +77,39 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   grid_launch_dependents();
 
   // (1) top-k + softmax: warp t takes token t
+  int* s_warp = reinterpret_cast<int*>(sm);  // 32 + 2 ints of block-scan scratch
+  int* s_tot = s_warp + 32;
   if (warp < T) route_topk_token<MAXPL>(logits, warp, E, k, s_idx, s_gate, status);
+  for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
+  if (blockIdx.x == 0 && done)
+    for (int i = tid; i < max_chunks; i += 1024) done[i] = 0;  // per-call completion counters
   __syncthreads();
-  // (2)-(4): histogram, scan, stable permutation, chunk list, into shared memory
-  route_permute_cta(s_idx, T, k, E, s_cnt, s_off, s_perm, s_pos, s_chunks, max_chunks, chunk_max,
-                    s_meta, blockIdx.x == 0 ? done : nullptr, status);
+  // (2)-(4) for at most 32 * 16 assignments: counts, offsets, each assignment's
+  // rank among the earlier ones of its expert (a direct count: at most 511
+  // broadcast reads), chunk list — route_permute_kernel's results exactly
+  for (int f = tid; f < TK; f += 1024) {
+    if ((unsigned)s_idx[f] >= (unsigned)E) {  // never from the top-k; kept as a guard
+      set_status(status, kStatusFault);
+      s_idx[f] = 0;
+    }
+  }
+  __syncthreads();
+  for (int f = tid; f < TK; f += 1024) atomicAdd(&s_cnt[s_idx[f]], 1);
+  __syncthreads();
+  const int c = tid < E ? s_cnt[tid] : 0;
+  const int excl = block_exclusive_scan_1024(c, s_warp, &s_tot[0]);
+  if (tid < E) s_off[tid] = excl;
+  if (tid == 0) s_off[E] = TK;
+  __syncthreads();
+  if (tid < TK) {
+    const int e = s_idx[tid];
+    int r = 0;
+    for (int g = 0; g < tid; ++g) r += s_idx[g] == e;
+    const int slot = s_off[e] + r;
+    s_pos[tid] = slot;
+    s_perm[slot] = tid / k;
+  }
+  route_chunk_list(c, excl, E, chunk_max, s_chunks, max_chunks, s_meta, s_warp, s_tot, status);
   __syncthreads();
   if (blockIdx.x == 0) {  // publish the routing arrays
     for (int i = tid; i < TK; i += 1024) {

@@ -133,16 +133,23 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* s_warp, int
 // Chunk list of a routed block, by one 1024-thread CTA whose thread e < E
 // holds expert e's count c and first slot excl: touched experts in ascending
 // order, each split into ceil(n / chunk_max) chunks of near-equal size;
-// meta[0] = chunks, meta[1] = touched experts.
+// meta[0] = chunks, meta[1] = touched experts.  kPacked: both prefix sums in
+// one scan of (chunks | touched << 16) — exact while the block has fewer than
+// 65536 chunks (the small-block kernel: at most 512 assignments).
+template <bool kPacked = false>
 __device__ __forceinline__ void route_chunk_list(int c, int excl, int E, int chunk_max,
                                                  int4* __restrict__ chunks, int max_chunks,
                                                  int32_t* __restrict__ meta, int* s_warp,
                                                  int* s_tot, int* status) {
   const int tid = threadIdx.x;
   const int nch = c > 0 ? (c + chunk_max - 1) / chunk_max : 0;
-  const int cbase = block_exclusive_scan_1024(nch, s_warp, &s_tot[0]);
-  const int touched = block_exclusive_scan_1024(c > 0 ? 1 : 0, s_warp, &s_tot[1]);
-  (void)touched;
+  int cbase;
+  if (kPacked) {
+    cbase = block_exclusive_scan_1024(nch | (c > 0 ? 1 << 16 : 0), s_warp, &s_tot[0]) & 0xFFFF;
+  } else {
+    cbase = block_exclusive_scan_1024(nch, s_warp, &s_tot[0]);
+    block_exclusive_scan_1024(c > 0 ? 1 : 0, s_warp, &s_tot[1]);
+  }
   if (tid < E && nch > 0) {
     const int q = (c + nch - 1) / nch;
     for (int i = 0; i < nch; ++i) {
@@ -153,8 +160,8 @@ __device__ __forceinline__ void route_chunk_list(int c, int excl, int E, int chu
     }
   }
   if (tid == 0) {
-    meta[0] = min(s_tot[0], max_chunks);
-    meta[1] = s_tot[1];
+    meta[0] = min(kPacked ? s_tot[0] & 0xFFFF : s_tot[0], max_chunks);
+    meta[1] = kPacked ? s_tot[0] >> 16 : s_tot[1];
   }
 }
 

@@ -9,8 +9,10 @@
 // and chunk list for at most 512 assignments, where each assignment's rank
 // within its expert is a direct count of the earlier equal ones: the same
 // arrays as the general permutation, bit for bit), CTA 0 publishes the
-// routing arrays, and every CTA then gathers and quantises its share of the
-// slot rows (MXFP8, blocks of 32 along H) or copies them (bf16 mode).
+// routing arrays.  Step a4 runs token-major: the warps that the top-k leaves
+// idle read and quantise (MXFP8, blocks of 32 along H) or read (bf16 mode)
+// their share of the token rows while the routing runs, and write each to
+// the token's k slot rows once the slots are known.
 // Redundant routing costs a few microseconds of L2 reads of the [T, E]
 // logits per CTA; it removes two launches and their dependency waits.
 #pragma once
@@ -54,6 +56,63 @@ __host__ __device__ inline SmallRouteSmem small_route_smem(int T, int E, int k, 
   return L;
 }
 
+// One token-major unit of step a4: token t's run of 32 blocks of 32 along H
+// (a block per lane), read and quantised (MXFP8) or read (bf16) into
+// registers, then written to each of the token's k slot rows.
+template <bool kMxfp8>
+struct SmallActUnit {
+  uint32_t w[kMxfp8 ? 8 : 16];
+  int code;
+  int64_t t, b;
+  bool live;
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ x, int64_t u, int64_t segs,
+                                       int64_t H) {
+    const int lane = threadIdx.x & 31;
+    t = u / segs;
+    b = (u - t * segs) * 32 + lane;
+    live = b < H / 32;
+    if (!live) return;
+    if (kMxfp8) {
+      float v[32];
+      uint8_t c[32];
+      load_bf16x32(x + t * H + b * 32, v);
+      code = mxfp8_block(v, c);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        w[i] = (uint32_t)c[4 * i] | ((uint32_t)c[4 * i + 1] << 8) |
+               ((uint32_t)c[4 * i + 2] << 16) | ((uint32_t)c[4 * i + 3] << 24);
+    } else {
+      const uint4* a = reinterpret_cast<const uint4*>(x + t * H + b * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint4 q = a[i];
+        w[4 * i] = q.x;
+        w[4 * i + 1] = q.y;
+        w[4 * i + 2] = q.z;
+        w[4 * i + 3] = q.w;
+      }
+    }
+  }
+  __device__ __forceinline__ void store(const int32_t* s_pos, int k, int TK, int64_t H,
+                                        uint8_t* __restrict__ q, uint8_t* __restrict__ s,
+                                        int* status) const {
+    if (!live) return;
+    const int64_t nb = H / 32;
+    for (int j = 0; j < k; ++j) {
+      const int64_t slot = s_pos[t * k + j];
+      if (slot < 0 || slot >= TK) {
+        set_status(status, kStatusFault);
+        continue;
+      }
+      uint4* o = reinterpret_cast<uint4*>(q + (slot * H + b * 32) * (kMxfp8 ? 1 : 2));
+#pragma unroll
+      for (int i = 0; i < (kMxfp8 ? 2 : 4); ++i)
+        o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      if (kMxfp8) s[slot * nb + b] = (uint8_t)code;
+    }
+  }
+};
+
 template <int MAXPL, bool kMxfp8>
 __global__ void __launch_bounds__(1024) route_act_small_kernel(
     const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int k,
@@ -63,6 +122,8 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
     int32_t* __restrict__ done, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int* status) {
   extern __shared__ __align__(16) uint8_t sm[];
   const SmallRouteSmem L = small_route_smem(T, E, k, max_chunks);
+  int* s_warp = reinterpret_cast<int*>(sm);  // 32 + 2 ints of block-scan scratch
+  int* s_tot = s_warp + 32;
   int32_t* s_idx = reinterpret_cast<int32_t*>(sm + L.idx);
   float* s_gate = reinterpret_cast<float*>(sm + L.gate);
   int32_t* s_cnt = reinterpret_cast<int32_t*>(sm + L.cnt);
@@ -71,30 +132,40 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   int32_t* s_pos = reinterpret_cast<int32_t*>(sm + L.pos);
   int4* s_chunks = reinterpret_cast<int4*>(sm + L.chunks);
   int32_t* s_meta = reinterpret_cast<int32_t*>(sm + L.meta);
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int TK = T * k;
+  const int64_t segs = (H / 32 + 31) / 32, units = (int64_t)T * segs;
+  // warps T..31 of every CTA take the first token-major units of a4 while
+  // warps 0..T-1 route; the rest of the units follow the routing
+  const int64_t early = (int64_t)gridDim.x * (32 - T);
   grid_dependency_wait();
   grid_launch_dependents();
 
-  // (1) top-k + softmax: warp t takes token t
-  int* s_warp = reinterpret_cast<int*>(sm);  // 32 + 2 ints of block-scan scratch
-  int* s_tot = s_warp + 32;
-  if (warp < T) route_topk_token<MAXPL>(logits, warp, E, k, s_idx, s_gate, status);
+  SmallActUnit<kMxfp8> held;
+  held.live = false;
+  if (warp < T) {
+    // (1) top-k + softmax: warp t takes token t
+    route_topk_token<MAXPL>(logits, warp, E, k, s_idx, s_gate, status);
+  } else {
+    const int64_t u = blockIdx.x + (int64_t)gridDim.x * (warp - T);
+    if (u < units) held.load(x, u, segs, H);
+  }
   for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
   if (blockIdx.x == 0 && done)
     for (int i = tid; i < max_chunks; i += 1024) done[i] = 0;  // per-call completion counters
   __syncthreads();
   // (2)-(4) for at most 32 * 16 assignments: counts, offsets, each assignment's
-  // rank among the earlier ones of its expert (a direct count: at most 511
-  // broadcast reads), chunk list — route_permute_kernel's results exactly
+  // rank among the earlier ones of its expert (a direct count), chunk list —
+  // route_permute_kernel's results exactly
   for (int f = tid; f < TK; f += 1024) {
-    if ((unsigned)s_idx[f] >= (unsigned)E) {  // never from the top-k; kept as a guard
+    int e = s_idx[f];
+    if ((unsigned)e >= (unsigned)E) {  // never from the top-k; kept as a guard
       set_status(status, kStatusFault);
+      e = 0;
       s_idx[f] = 0;
     }
+    atomicAdd(&s_cnt[e], 1);
   }
-  __syncthreads();
-  for (int f = tid; f < TK; f += 1024) atomicAdd(&s_cnt[s_idx[f]], 1);
   __syncthreads();
   const int c = tid < E ? s_cnt[tid] : 0;
   const int excl = block_exclusive_scan_1024(c, s_warp, &s_tot[0]);
@@ -103,13 +174,20 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   __syncthreads();
   if (tid < TK) {
     const int e = s_idx[tid];
+    const int4* v4 = reinterpret_cast<const int4*>(s_idx);
     int r = 0;
-    for (int g = 0; g < tid; ++g) r += s_idx[g] == e;
+#pragma unroll 4
+    for (int g = 0; g < (tid >> 2); ++g) {
+      const int4 v = v4[g];
+      r += (v.x == e) + (v.y == e) + (v.z == e) + (v.w == e);
+    }
+    for (int g = tid & ~3; g < tid; ++g) r += s_idx[g] == e;
     const int slot = s_off[e] + r;
     s_pos[tid] = slot;
     s_perm[slot] = tid / k;
   }
-  route_chunk_list(c, excl, E, chunk_max, s_chunks, max_chunks, s_meta, s_warp, s_tot, status);
+  route_chunk_list<true>(c, excl, E, chunk_max, s_chunks, max_chunks, s_meta, s_warp, s_tot,
+                         status);
   __syncthreads();
   if (blockIdx.x == 0) {  // publish the routing arrays
     for (int i = tid; i < TK; i += 1024) {
@@ -126,32 +204,13 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
     if (tid < 2) meta[tid] = s_meta[tid];
   }
 
-  // a4: this CTA's share of the slot rows; a warp per (slot, run of 32
-  // blocks of 32), a block per lane (the standalone kernels' arithmetic)
-  const int64_t nb = H / 32, segs = (nb + 31) / 32;
-  const int64_t warps = (int64_t)gridDim.x * 32;
-  for (int64_t u = (int64_t)blockIdx.x * 32 + warp; u < (int64_t)TK * segs; u += warps) {
-    const int64_t r = u / segs;
-    const int64_t b = (u - r * segs) * 32 + lane;
-    int64_t src = s_perm[r];
-    if (src < 0 || src >= T) {
-      if (lane == 0) set_status(status, kStatusFault);
-      src = 0;
-    }
-    if (b >= nb) continue;
-    if (kMxfp8) {
-      float v[32];
-      uint8_t c[32];
-      load_bf16x32(x + src * H + b * 32, v);
-      const int code = mxfp8_block(v, c);
-      store_u8x32(q + r * H + b * 32, c);
-      s[r * nb + b] = (uint8_t)code;
-    } else {
-      const uint4* a = reinterpret_cast<const uint4*>(x + src * H + b * 32);
-      uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(q) + r * H + b * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = a[i];
-    }
+  // a4: the held unit, then the units past the early ones (a warp each)
+  held.store(s_pos, k, TK, H, q, s, status);
+  for (int64_t u = early + (int64_t)blockIdx.x * 32 + warp; u < units;
+       u += (int64_t)gridDim.x * 32) {
+    SmallActUnit<kMxfp8> a;
+    a.load(x, u, segs, H);
+    a.store(s_pos, k, TK, H, q, s, status);
   }
 }
 

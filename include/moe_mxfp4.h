@@ -187,8 +187,10 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
  * 1 <= n_layers <= MOE_MAX_CHAIN; residual is 0 or 1; y_bf16 [T, H] may equal
  * x_bf16.  opts as moe_mxfp4_forward_ex (act_mode, path, workspace of at least
  * moe_mxfp4_workspace_size_chain bytes, debug flags); step markers follow the
- * kernel order: route_topk, route_permute for each layer in turn, act_quant,
- * then per layer its GEMM kernel(s) and combine.
+ * kernel order: route_topk (every layer), route_permute (every layer),
+ * act_quant (layer 0), then per layer its GEMM kernel(s) and combine; for
+ * T <= 32 the first three are one kernel, route_act (unless
+ * MOE_DEBUG_SPLIT_ROUTING), with the same results.
  * Returns MOE_OK or an moe_status error (host-detected errors launch nothing).
  */
 int moe_mxfp4_forward_chain(int n_layers, const void* x_bf16, const float* const* router_logits,

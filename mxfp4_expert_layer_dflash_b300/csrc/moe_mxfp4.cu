@@ -106,6 +106,12 @@ bool set_small_route_smem() {
   set(route_act_small_kernel<4, false>);
   set(route_act_small_kernel<12, false>);
   set(route_act_small_kernel<32, false>);
+  set(route_act_small_layers_kernel<4, true>);
+  set(route_act_small_layers_kernel<12, true>);
+  set(route_act_small_layers_kernel<32, true>);
+  set(route_act_small_layers_kernel<4, false>);
+  set(route_act_small_layers_kernel<12, false>);
+  set(route_act_small_layers_kernel<32, false>);
   return ok;
 }
 
@@ -580,6 +586,39 @@ int enqueue_route_layers(const float* const* logits, int n, int T, int E, int k,
   return launch_status();
 }
 
+// Routing of every layer of a chain over a block of T <= kSmallRouteTokens
+// tokens, and layer 0's step a4, in one ordinary launch (the call's first):
+// route_act_small_layers_kernel; layer l's routing block lies l * stride
+// bytes after layer 0's (w0)
+int enqueue_route_act_small_layers(const float* const* logits, int n, int act, const uint16_t* x,
+                                   int T, int H, int E, int k, int chunk_max, const Work& w0,
+                                   int64_t stride, DeviceState* d, cudaStream_t s, Steps& st) {
+  LayerLogits lg{};
+  for (int l = 0; l < n; ++l) lg.p[l] = logits[l];
+  const int64_t units = (int64_t)T * k * ((H / 32 + 31) / 32);
+  const dim3 grid(grid_for(units, 32, d->sms), n);
+  const size_t smem = small_route_smem(T, E, k, w0.max_chunks).total;
+  st.mark();
+  auto go = [&](auto kernel) {
+    kernel<<<grid, 1024, smem, s>>>(lg, x, T, H, E, k, w0.max_chunks, chunk_max, w0.topk_idx,
+                                    w0.topk_w, w0.cnt, w0.off, w0.perm, w0.pos, w0.chunks,
+                                    w0.meta, w0.done, w0.xq, w0.xs, stride, d->status);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if (act == MOE_ACT_MXFP8)
+    e = E <= 128 ? go(route_act_small_layers_kernel<4, true>)
+        : E <= 384 ? go(route_act_small_layers_kernel<12, true>)
+                   : go(route_act_small_layers_kernel<32, true>);
+  else
+    e = E <= 128 ? go(route_act_small_layers_kernel<4, false>)
+        : E <= 384 ? go(route_act_small_layers_kernel<12, false>)
+                   : go(route_act_small_layers_kernel<32, false>);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  st.launched();
+  return MOE_OK;
+}
+
 // The path MOE_PATH_AUTO takes.  One launch removes the gap and the tail
 // between the two GEMMs, which pays when each SM gets a handful of work items;
 // with many items per SM the two specialised launches stream weights faster,
@@ -865,11 +904,19 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
   const unsigned long long timeout_ns =
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
-  if ((rc = enqueue_route_layers(logits, n, T, E, k, chunk_for(act, T),
-                                 carve_chain(ws, C, 0), (int64_t)C.route_block, d, stream, st)))
-    return rc;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
-  if ((rc = enqueue_act(act, x, carve_chain(ws, C, 0), T, H, k, d, stream, st))) return rc;
+  if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
+    if ((rc = enqueue_route_act_small_layers(logits, n, act, x, T, H, E, k, chunk_for(act, T),
+                                             carve_chain(ws, C, 0), (int64_t)C.route_block, d,
+                                             stream, st)))
+      return rc;
+  } else {
+    if ((rc = enqueue_route_layers(logits, n, T, E, k, chunk_for(act, T),
+                                   carve_chain(ws, C, 0), (int64_t)C.route_block, d, stream,
+                                   st)))
+      return rc;
+    if ((rc = enqueue_act(act, x, carve_chain(ws, C, 0), T, H, k, d, stream, st))) return rc;
+  }
   const int64_t threads = (int64_t)T * H / 4;
   for (int l = 0; l < n; ++l) {
     const Work w = carve_chain(ws, C, l);

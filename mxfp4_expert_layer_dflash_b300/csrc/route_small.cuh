@@ -113,13 +113,17 @@ struct SmallActUnit {
   }
 };
 
+// The routing of one block of T <= 32 tokens by one CTA (every CTA of the
+// grid's x dimension that calls it computes the same arrays); `publish`: this
+// CTA writes them out.  x == nullptr: no step a4.
 template <int MAXPL, bool kMxfp8>
-__global__ void __launch_bounds__(1024) route_act_small_kernel(
+__device__ __forceinline__ void route_small_block(
     const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int k,
-    int max_chunks, int chunk_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
-    int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ perm,
-    int32_t* __restrict__ pos, int4* __restrict__ chunks, int32_t* __restrict__ meta,
-    int32_t* __restrict__ done, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int* status) {
+    int max_chunks, int chunk_max, bool publish, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* __restrict__ cnt, int32_t* __restrict__ off,
+    int32_t* __restrict__ perm, int32_t* __restrict__ pos, int4* __restrict__ chunks,
+    int32_t* __restrict__ meta, int32_t* __restrict__ done, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ s, int* status) {
   extern __shared__ __align__(16) uint8_t sm[];
   const SmallRouteSmem L = small_route_smem(T, E, k, max_chunks);
   int* s_warp = reinterpret_cast<int*>(sm);  // 32 + 2 ints of block-scan scratch
@@ -138,20 +142,18 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   // warps T..31 of every CTA take the first token-major units of a4 while
   // warps 0..T-1 route; the rest of the units follow the routing
   const int64_t early = (int64_t)gridDim.x * (32 - T);
-  grid_dependency_wait();
-  grid_launch_dependents();
 
   SmallActUnit<kMxfp8> held;
   held.live = false;
   if (warp < T) {
     // (1) top-k + softmax: warp t takes token t
     route_topk_token<MAXPL>(logits, warp, E, k, s_idx, s_gate, status);
-  } else {
+  } else if (x) {
     const int64_t u = blockIdx.x + (int64_t)gridDim.x * (warp - T);
     if (u < units) held.load(x, u, segs, H);
   }
   for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
-  if (blockIdx.x == 0 && done)
+  if (publish && done)
     for (int i = tid; i < max_chunks; i += 1024) done[i] = 0;  // per-call completion counters
   __syncthreads();
   // (2)-(4) for at most 32 * 16 assignments: counts, offsets, each assignment's
@@ -189,7 +191,7 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   route_chunk_list<true>(c, excl, E, chunk_max, s_chunks, max_chunks, s_meta, s_warp, s_tot,
                          status);
   __syncthreads();
-  if (blockIdx.x == 0) {  // publish the routing arrays
+  if (publish) {
     for (int i = tid; i < TK; i += 1024) {
       topk_idx[i] = s_idx[i];
       topk_w[i] = s_gate[i];
@@ -204,6 +206,7 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
     if (tid < 2) meta[tid] = s_meta[tid];
   }
 
+  if (!x) return;
   // a4: the held unit, then the units past the early ones (a warp each)
   held.store(s_pos, k, TK, H, q, s, status);
   for (int64_t u = early + (int64_t)blockIdx.x * 32 + warp; u < units;
@@ -212,6 +215,47 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
     a.load(x, u, segs, H);
     a.store(s_pos, k, TK, H, q, s, status);
   }
+}
+
+// Steps a1-a4 of one layer: every CTA routes, CTA 0 publishes, all quantise
+template <int MAXPL, bool kMxfp8>
+__global__ void __launch_bounds__(1024) route_act_small_kernel(
+    const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int k,
+    int max_chunks, int chunk_max, int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int32_t* __restrict__ cnt, int32_t* __restrict__ off, int32_t* __restrict__ perm,
+    int32_t* __restrict__ pos, int4* __restrict__ chunks, int32_t* __restrict__ meta,
+    int32_t* __restrict__ done, uint8_t* __restrict__ q, uint8_t* __restrict__ s, int* status) {
+  grid_dependency_wait();
+  grid_launch_dependents();
+  route_small_block<MAXPL, kMxfp8>(logits, x, T, H, E, k, max_chunks, chunk_max,
+                                   blockIdx.x == 0, topk_idx, topk_w, cnt, off, perm, pos,
+                                   chunks, meta, done, q, s, status);
+}
+
+// A chain of layers over one small block: blockIdx.y = layer, whose routing
+// arrays start `stride` bytes after the previous layer's.  Layer 0 as in
+// route_act_small_kernel (every CTA routes it, CTA 0 publishes, all CTAs run
+// its step a4 into q / s); every later layer is routed and published by its
+// CTA x = 0 alone (its activation rows come from the previous layer's combine).
+template <int MAXPL, bool kMxfp8>
+__global__ void __launch_bounds__(1024) route_act_small_layers_kernel(
+    const __grid_constant__ LayerLogits lg, const uint16_t* __restrict__ x, int T, int H, int E,
+    int k, int max_chunks, int chunk_max, int32_t* topk_idx0, float* topk_w0, int32_t* cnt0,
+    int32_t* off0, int32_t* perm0, int32_t* pos0, int4* chunks0, int32_t* meta0, int32_t* done0,
+    uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t stride, int* status) {
+  const int l = blockIdx.y;
+  if (l > 0 && blockIdx.x > 0) return;
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t o = (int64_t)l * stride;
+  auto at = [o](auto* p) {
+    using P = decltype(p);
+    return reinterpret_cast<P>(reinterpret_cast<char*>(p) + o);
+  };
+  route_small_block<MAXPL, kMxfp8>(lg.p[l], l == 0 ? x : nullptr, T, H, E, k, max_chunks,
+                                   chunk_max, blockIdx.x == 0, at(topk_idx0), at(topk_w0),
+                                   at(cnt0), at(off0), at(perm0), at(pos0), at(chunks0), at(meta0),
+                                   done0 ? at(done0) : nullptr, q, s, status);
 }
 
 }  // namespace moe

@@ -103,6 +103,31 @@ def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act):
         assert rel_fro(yg, yref) <= BF16_FRO
 
 
+@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+@pytest.mark.parametrize("T,H,I,E,k,n", [(32, 1024, 256, 40, 16, 3), (30, 6144, 128, 16, 2, 2),
+                                         (7, 2048, 256, 200, 8, 3), (5, 384, 128, 600, 4, 2)])
+def test_chain_small_block_routing_matches_split_kernels(T, H, I, E, k, n, act):
+    """At T <= 32 the chain routes every layer, and runs layer 0's activation step, in one
+    launch; MOE_DEBUG_SPLIT_ROUTING makes it use the general routing kernels instead.  Both must
+    give the same routing and slot rows, so the outputs are equal bit for bit.  The residual is
+    on so that x itself reaches the output too.  The shapes cover 512 assignments (T = 32,
+    k = 16: no warp is free during the top-k, so all of step a4 follows the routing), a mix of
+    early and late activation units (T = 30, H = 6144), and all three top-k widths (E up to
+    128, up to 384, above 384)."""
+    Ls, lgs, ws = _layers(T, H, I, E, k, n, 700 + T)
+    x = dev(LY.host_x(Ls[0]))
+    outs = []
+    for flags in (0, moe.MOE_DEBUG_SPLIT_ROUTING):
+        y = torch.full((T, H), float("nan"), dtype=torch.bfloat16, device="cuda")
+        moe.moe_mxfp4_forward_chain(x, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                    [w[2] for w in ws], [w[3] for w in ws], T, H, I, E, k, y,
+                                    residual=True, act_mode=act, debug_flags=flags)
+        assert moe.moe_mxfp4_get_status() == 0
+        outs.append(y)
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert not torch.isnan(outs[0].float()).any()
+
+
 def test_chain_residual_with_zero_weights_returns_x():
     Ls, lgs, ws = _layers(12, 256, 128, 8, 2, 3, 7)
     zero = [tuple(torch.zeros_like(a) for a in w) for w in ws]

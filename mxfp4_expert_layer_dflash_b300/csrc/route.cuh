@@ -15,51 +15,73 @@
 
 namespace moe {
 
+// Order-preserving key of a logit: a larger value has a larger key, equal
+// values (+0 and -0 included) have equal keys.  Non-finite logits are outside
+// the supported inputs.
+__device__ __forceinline__ uint32_t topk_key(float v) {
+  uint32_t u = __float_as_uint(v);
+  if ((u << 1) == 0) u = 0;  // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float topk_key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+__device__ __forceinline__ uint32_t warp_redux_max(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t warp_redux_min(uint32_t v) {
+  uint32_t r;
+  asm volatile("redux.sync.min.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(v));
+  return r;
+}
+
 // Step (1) for token t, by one warp.  MAXPL logits per lane (E <= 32 * MAXPL).
+// Round j picks the largest remaining logit, the lowest expert index among
+// equal ones: the warp's largest key (one reduction), then the lowest index
+// among the lanes whose own best has that key (a second one).
 template <int MAXPL>
 __device__ __forceinline__ void route_topk_token(const float* __restrict__ logits, int t, int E,
                                                  int k, int32_t* __restrict__ idx,
                                                  float* __restrict__ w, int* status) {
   const int lane = threadIdx.x & 31;
   const float* l = logits + (size_t)t * E;
-  float v[MAXPL];
-  uint32_t taken = 0;
+  uint32_t key[MAXPL];
 #pragma unroll
   for (int i = 0; i < MAXPL; ++i) {
-    int e = lane + 32 * i;
-    v[i] = e < E ? l[e] : -FLT_MAX;
-    if (e >= E) taken |= 1u << i;
+    const int e = lane + 32 * i;
+    key[i] = e < E ? topk_key(l[e]) : 0u;  // 0: below every finite logit's key
   }
   float my_v = 0.0f;
   int my_e = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int be = 0x7FFFFFFF;
+    uint32_t bk = 0;
+    int bi = -1;
 #pragma unroll
-    for (int i = 0; i < MAXPL; ++i) {
-      int e = lane + 32 * i;
-      if (!((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < be))) {
-        bv = v[i];
-        be = e;
+    for (int i = 0; i < MAXPL; ++i) {  // strict >: the lowest i (index) among equal keys
+      if (key[i] > bk) {
+        bk = key[i];
+        bi = i;
       }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if (be >= E) {  // only possible with non-finite logits
+    const uint32_t wk = warp_redux_max(bk);
+    uint32_t be = warp_redux_min(bi >= 0 && bk == wk ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+    if (be >= (uint32_t)E) {  // only possible with non-finite logits
       if (lane == 0) set_status(status, kStatusFault);
       be = 0;
     }
-    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if ((int)(be & 31) == lane) {
+#pragma unroll
+      for (int i = 0; i < MAXPL; ++i)
+        if (i == (int)(be >> 5)) key[i] = 0u;  // taken
+    }
     if (lane == j) {
-      my_v = bv;
-      my_e = be;
+      my_v = topk_key_value(wk);
+      my_e = (int)be;
     }
   }
   const float m = __shfl_sync(0xffffffffu, my_v, 0);  // first pick is the largest

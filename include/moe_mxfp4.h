@@ -136,8 +136,8 @@ typedef struct {
  * ignored by the other paths. */
 #define MOE_DEBUG_FORCE_DEP_TIMEOUT 2u
 /* debug_flags: run routing and the activation step as three kernels even for
- * T <= 32 (where they are normally one kernel); the results are identical —
- * used by the tests to compare the two */
+ * T <= 32 (where they are normally one kernel, for one layer and for a chain);
+ * the results are identical — used by the tests to compare the two */
 #define MOE_DEBUG_SPLIT_ROUTING 4u
 /* debug_flags: in the bf16 mode, GEMM1's MMA warp never hands decoded weight
  * buffers back to the decoders, so their bounded wait runs out (~1 ms with

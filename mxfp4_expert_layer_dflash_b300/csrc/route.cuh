@@ -9,8 +9,6 @@
 // techllm.github.io, "Xiaomi MiMo and TileRT ...", section "3. TileRT".
 #pragma once
 
-#include <float.h>
-
 #include "common.cuh"
 
 namespace moe {

@@ -101,6 +101,15 @@ typedef enum {
  * Other pointers must be 16-byte aligned.  Scratch space comes from a
  * library-owned per-device cache that grows on first use of a larger shape
  * (a cudaMalloc outside any stream capture).
+ * Sharing: every call on a device that is not given its own workspace
+ * (moe_mxfp4_forward, and the other entry points that say they use the
+ * library's scratch) uses that one cache.  Such calls must be ordered on the
+ * GPU (one stream, or events between streams) — calls that overlap there race
+ * on the scratch and give wrong results — and must not run at the same time
+ * on the host either: growing the cache frees the previous buffer, which a
+ * call on another host thread may still be enqueueing work on.  Callers that
+ * run layers concurrently give each stream its own workspace through
+ * moe_mxfp4_forward_ex (or moe_mxfp4_forward_chain's options).
  * Returns MOE_OK or an moe_status error (host-detected errors launch nothing).
  */
 int moe_mxfp4_forward(const void* x_bf16, const float* router_logits, const uint8_t* w13_fp4,
@@ -239,7 +248,9 @@ int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4,
  *  router_logits [T, E] fp32 device;  outputs (device):
  *  topk_idx [T, k] int32, topk_w [T, k] fp32, cnt [E] int32, off [E+1] int32,
  *  perm [T*k] int32 (slot -> token), pos [T*k] int32 ((t*k + j) -> slot).
- * Slots are expert-major; within an expert, ascending t*k + j.
+ * Slots are expert-major; within an expert, ascending t*k + j.  Scratch (the
+ * chunk list) from the library-owned cache (shared: see the ordering rules
+ * under moe_mxfp4_forward).
  */
 int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* topk_idx,
                     float* topk_w, int32_t* cnt, int32_t* off, int32_t* perm, int32_t* pos,
@@ -308,7 +319,8 @@ int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
  * 1 <= k <= min(E, MOE_MAX_K)); pointers 16-byte aligned.  The logits are
  * fp32 sums of exact bf16 products, accumulated on the tensor cores in K
  * ranges whose partial sums are added in a fixed order: deterministic run to
- * run.  Scratch from the library-owned cache.  Returns MOE_OK or an error.
+ * run.  Scratch from the library-owned cache (shared: see the ordering
+ * rules under moe_mxfp4_forward).  Returns MOE_OK or an error.
  * No counterpart in the papers beyond the routing step itself.
  */
 int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H, int E, int k,
@@ -359,7 +371,8 @@ int mxfp8_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_e4m3, u
  * K a multiple of 128, N a multiple of 4, T >= 0 (0 = no-op); pointers
  * 16-byte aligned.  The MMA accumulates in fp32 over K ranges whose partial
  * sums are added in a fixed order (deterministic).  Scratch from the
- * library-owned cache.  Returns MOE_OK or an error (host-detected errors
+ * library-owned cache (shared: see the ordering rules under
+ * moe_mxfp4_forward).  Returns MOE_OK or an error (host-detected errors
  * launch nothing).
  */
 int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8_t* w_e8m0,
@@ -389,7 +402,8 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
  *                      then -1
  * All device pointers, 4-byte aligned (U 8-byte); 1 <= g <= MOE_VERIFY_MAX_DRAFT,
  * 1 <= V <= 2^21 (MOE_ERR_UNSUPPORTED_SHAPE above), S >= 0 (0 = no-op).
- * Scratch from the library-owned cache.
+ * Scratch from the library-owned cache (shared: see the ordering rules under
+ * moe_mxfp4_forward).
  * The random numbers are inputs: the call is deterministic.
  */
 #define MOE_VERIFY_MAX_DRAFT 64

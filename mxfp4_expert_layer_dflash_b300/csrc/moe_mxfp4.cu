@@ -831,8 +831,6 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   if (!ws && (rc = cached_workspace(d, L.total, &ws))) return rc;
   const Work w = carve(ws, L);
 
-  // Wide token chunks halve the MMA instructions per token when experts get
-  // many tokens (large T); narrow chunks keep the weight pipeline deepest.
   const unsigned long long timeout_ns =
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
@@ -841,6 +839,8 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     return rc;
   const float* lg = routed ? w.rlogits : logits;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
+  // wide token chunks cut the MMA instructions per token when experts get
+  // many tokens (large T); narrow chunks keep the weight pipeline deepest
   const int chunk = chunk_for(act, T);
   if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
     if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
@@ -865,7 +865,8 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
 
 // A chain of layers over one token block: x_0 = x, x_{l+1} = bf16_RNE(y_l +
 // residual * x_l), y = x_n.  Routing depends only on each layer's logits, so
-// every layer is routed first, all layers at once (two launches); then per
+// every layer is routed first, all layers at once (two launches, or at T <= 32
+// one that also runs layer 0's activation step); then per
 // layer the GEMMs run and the combine writes layer l+1's activation rows
 // directly (combine_next_kernel).
 int chain_impl(int n, const void* x_bf16, const float* const* logits,

@@ -104,27 +104,81 @@ def layer_bytes(L, cnt):
 # ------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while active."""
+    """SM clocks, power and clock-event (throttle) reasons of one GPU, read through NVML by a
+    background thread every `period_s` while active, each sample time-stamped, so that the
+    samples inside a timed region of a few tens of milliseconds can be picked out
+    (`mark_start` / `mark_stop` around it).  Reads only; changes no setting.  Falls back to
+    `nvidia-smi -lms 50` when NVML is unavailable."""
+    REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, cuda_index: int, period_s: float = 0.002):
+        self.cuda_index = cuda_index
+        self.period = period_s
+        self.samples = []          # (time, sm_mhz, max_mhz, reasons bitmask)
+        self.window = None
+        self.source = None
+
+    def _handle(self):
+        import pynvml
+        import torch
+        pynvml.nvmlInit()
+        uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+        for u in (uuid, "GPU-" + uuid):
+            try:
+                return pynvml.nvmlDeviceGetHandleByUUID(u)
+            except Exception:  # noqa: BLE001 - try the other spelling, then the index
+                pass
+        return pynvml.nvmlDeviceGetHandleByIndex(self.cuda_index)
+
+    def _run_nvml(self, h):
+        import pynvml
+        mx = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+        while not self._stop.is_set():
+            try:
+                sm = float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
+                rs = int(pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))
+                self.samples.append((time.perf_counter(), sm, mx, rs))
+            except Exception:  # noqa: BLE001 - a failed read is skipped
+                pass
+            self._stop.wait(self.period)
 
     def __enter__(self):
+        import threading
+        self._stop = threading.Event()
+        self.proc = None
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-i", str(self.gpu), "-lms", "200"], stdout=subprocess.PIPE,
-                stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
+            h = self._handle()
+            self.thread = threading.Thread(target=self._run_nvml, args=(h,), daemon=True)
+            self.thread.start()
+            self.source = f"NVML every {self.period * 1e3:.0f} ms"
+        except Exception:  # noqa: BLE001 - no NVML: nvidia-smi at its fastest period
+            self.thread = None
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                     "-i", str(self.cuda_index), "-lms", "50"], stdout=subprocess.PIPE,
+                    stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi every 50 ms"
+            except OSError:
+                self.proc = None
+        self.t_enter = time.perf_counter()
         return self
 
+    def mark_start(self):
+        self.window = [time.perf_counter(), None]
+
+    def mark_stop(self):
+        if self.window:
+            self.window[1] = time.perf_counter()
+
     def __exit__(self, *exc):
-        self.lines = []
+        self._stop.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -132,25 +186,34 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
                 out, _ = self.proc.communicate()
-            self.lines = [l for l in out.splitlines() if l.strip()]
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for l in out.splitlines():
+                f = [x.strip() for x in l.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm, mx = float(f[1]), float(f[2])
+                except ValueError:
+                    continue
+                rs = 0
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        rs |= self.REASONS[n]
+                self.samples.append((None, sm, mx, rs))
 
     def summary(self):
-        sm, mx, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
-            f = [x.strip() for x in l.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx = max(mx, float(f[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
+        """Samples inside the marked timed region (all samples since warm-up began when no
+        sample fell inside it, e.g. with the coarse nvidia-smi fallback)."""
+        inside = [s for s in self.samples if s[0] is not None and self.window and
+                  self.window[0] <= s[0] <= (self.window[1] or s[0])]
+        use = inside or self.samples
+        sm = [s[1] for s in use]
+        mx = max((s[2] for s in use), default=0.0)
+        reasons = sorted({n for s in use for n, b in self.REASONS.items() if s[3] & b})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": reasons, "samples": len(sm),
+                "window": "timed region" if inside else "warm-up and timed region",
+                "source": self.source}
 
 
 # ------------------------------------------------------------------------- events
@@ -185,6 +248,27 @@ class Events:
 
 # ------------------------------------------------------------------------- oracle leg
 
+def _host_packed_weights_parallel(L, quantize, experts):
+    """LY.host_packed_weights for `experts`, one host thread per expert at a time (the
+    generator and the packing are C calls that release the GIL); same arrays."""
+    from concurrent.futures import ThreadPoolExecutor
+    from synth import synth as S
+    E, H, I = L.E, L.H, L.I
+    w13 = np.zeros((E, 2 * I, H // 2), np.uint8)
+    s13 = np.zeros((E, 2 * I, H // 32), np.uint8)
+    w2 = np.zeros((E, H, I // 2), np.uint8)
+    s2 = np.zeros((E, H, I // 32), np.uint8)
+
+    def one(e):
+        a = S.normal_f32(L.seed, S.ID_W13, e * 2 * I * H, 2 * I * H, S.W_SIGMA).reshape(2 * I, H)
+        w13[e], s13[e] = quantize(a)
+        b = S.normal_f32(L.seed, S.ID_W2, e * H * I, H * I, S.W_SIGMA).reshape(H, I)
+        w2[e], s2[e] = quantize(b)
+    with ThreadPoolExecutor(max_workers=min(16, cpu_cores())) as ex:
+        list(ex.map(one, sorted(set(int(v) for v in experts))))
+    return w13, s13, w2, s2
+
+
 def oracle_sample(L, n_tokens: int, act: str = "mxfp8"):
     """Prepare the oracle's inputs for the first n_tokens tokens (packing excluded from any
     timing): returns a closure that runs the oracle on a list of token indices (MXFP8
@@ -194,7 +278,7 @@ def oracle_sample(L, n_tokens: int, act: str = "mxfp8"):
     x, lg = LY.host_x(L), LY.host_logits(L)
     toks = np.arange(min(n_tokens, L.T))
     ridx, _ = O.route(lg[toks], L.k)
-    w = LY.host_packed_weights(L, O.mxfp4_quantize, np.unique(ridx))
+    w = _host_packed_weights_parallel(L, O.mxfp4_quantize, np.unique(ridx))
 
     mode = O.ACT_MXFP8 if act == "mxfp8" else O.ACT_EXACT
 
@@ -210,24 +294,31 @@ def cpu_cores() -> int:
         return os.cpu_count() or 1
 
 
+def oracle_layer_sample(L, act, n_tokens):
+    """(run, description): the oracle over the first n_tokens tokens of layer L, one call per
+    step — the same sample in both arms (the whole layer by default)."""
+    n = min(n_tokens, L.T)
+    run, n_exp = oracle_sample(L, n, act)
+    toks = list(range(n))
+    mode = "MXFP8-emulation" if act == "mxfp8" else "exact"
+    what = "the whole layer" if n == L.T else f"the first {n} of {L.T} tokens"
+    return (lambda: run(toks)), n, (f"{what} ({n} tokens, {n_exp} experts) per step, fp64 "
+                                    f"oracle in {mode} mode; MXFP4 packing excluded")
+
+
 def run_reference(args, L, rank):
     if rank != 0:
         return
-    n_tok = 8
-    log(f"[reference] preparing oracle inputs for {n_tok} tokens of {L.name}")
-    run, n_exp = oracle_sample(L, n_tok, args.act)
+    log(f"[reference] preparing oracle inputs for {L.name}")
+    run, n_tok, sample = oracle_layer_sample(L, args.act, args.cpu_tokens)
     for i in range(args.warmup):
-        run([i % n_tok])
+        run()
     t0 = time.perf_counter()
     for i in range(args.steps):
-        run([i % n_tok])
+        run()
     dt = time.perf_counter() - t0
-    value = args.steps / dt
+    value = args.steps * n_tok / dt
     cores = cpu_cores()
-    sample = (f"one token per step (cycling through the first {n_tok} tokens of the layer, "
-              f"{n_exp} experts), fp64 oracle in "
-              f"{'MXFP8-emulation' if args.act == 'mxfp8' else 'exact'} mode; MXFP4 packing "
-              f"excluded")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -571,24 +662,27 @@ def run_ours(args, L, rank, world, local_rank):
         moe.moe_mxfp4_forward_ex(x, lg, w13, s13, w2, s2, L.T, L.H, L.I, L.E, L.k, y, stream,
                                  act_mode=act, path=path, step_events=step_events)
 
-    for _ in range(args.warmup):
-        fwd()
-    if moe.moe_mxfp4_get_status() != 0:
-        raise RuntimeError("device status error during warm-up")
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    clk = ClockSampler(local_rank)
+    with clk:       # clocks sampled from the warm-up on; the summary keeps the timed region
+        for _ in range(args.warmup):
+            fwd()
+        if moe.moe_mxfp4_get_status() != 0:
+            raise RuntimeError("device status error during warm-up")
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
 
-    # timed region: plain forward calls (event records between kernels cost about a
-    # microsecond each, so the per-kernel split comes from a second, marked pass)
-    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    launches0 = moe.moe_mxfp4_launch_count()
-    with ClockSampler(local_rank) as clk:
+        # timed region: plain forward calls (event records between kernels cost about a
+        # microsecond each, so the per-kernel split comes from a second, marked pass)
+        start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        launches0 = moe.moe_mxfp4_launch_count()
+        clk.mark_start()
         start.record(stream)
         for i in range(args.steps):
             fwd()
         stop.record(stream)
         torch.cuda.synchronize()
+        clk.mark_stop()
     launches = moe.moe_mxfp4_launch_count() - launches0
     if dist:
         dist.barrier()
@@ -709,21 +803,14 @@ def run_ours(args, L, rank, world, local_rank):
         out["next_rows"] = measure_next_rows(pk, flush)
         del flush
     if world == 1 and not args.no_cpu_baseline:
-        log("[rank 0] timing the CPU oracle on a bounded sample")
-        n_tok = min(args.cpu_tokens, L.T)
-        run, n_exp = oracle_sample(L, n_tok, args.act)
-        reps, t0 = 0, time.perf_counter()
-        while True:               # repeat the sample until at least --cpu-seconds of work
-            run(list(range(n_tok)))
-            reps += 1
-            dt = time.perf_counter() - t0
-            if dt >= args.cpu_seconds:
-                break
+        log("[rank 0] timing the CPU oracle over the layer")
+        run, n_tok, sample = oracle_layer_sample(L, args.act, args.cpu_tokens)
+        t0 = time.perf_counter()
+        run()                     # one step: the same sample the reference arm times per step
+        dt = time.perf_counter() - t0
         out["cpu_baseline"] = {
-            "value": reps * n_tok / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"first {n_tok} of {L.T} tokens ({n_exp} experts) x {reps} repeats, fp64 "
-                      f"oracle in {'MXFP8-emulation' if args.act == 'mxfp8' else 'exact'} mode, "
-                      f"{dt:.1f} s; MXFP4 packing excluded"}
+            "value": n_tok / dt, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{sample}; one step, {dt:.1f} s"}
     print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
@@ -741,8 +828,8 @@ def main():
                     help="activation mode of the layer (the headline is mxfp8)")
     ap.add_argument("--row", choices=ROWS, default=None,
                     help="only run one call beside the layer (a profiling command)")
-    ap.add_argument("--cpu-tokens", type=int, default=32)
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-tokens", type=int, default=1 << 30,
+                    help="tokens of the layer the CPU oracle runs per step (default: all)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-config-sweep", action="store_true",
                     help="skip the per-config µs/layer report")

@@ -229,6 +229,54 @@ int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode);
 size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode);
 
 /*
+ * moe_mxfp4_workspace_layout — where a forward leaves its intermediate arrays
+ * inside a caller workspace (moe_opts.workspace of moe_mxfp4_forward_ex), so
+ * that the routing, the permutation and the quantised activations the layer
+ * actually used can be read back and checked after the call (the routing
+ * arrays must equal the routing rule's bit for bit).  Byte offsets from the
+ * workspace's start; after a call on that workspace completes:
+ *  topk_idx [T, k] int32 and topk_w [T, k] fp32   step (1)
+ *  cnt [E] int32, off [E+1] int32                 steps (2)-(3)
+ *  perm [T*k] int32 (slot -> token),
+ *  pos [T*k] int32 ((t*k + j) -> slot)            step (4): expert-major
+ *                                                 slots, ascending t*k + j
+ *                                                 within an expert
+ *  xq [T*k, H], xs [T*k, H/32]                    act1(x) in slot order: E4M3
+ *                                                 codes + E8M0 scales (MXFP8
+ *                                                 mode) or bf16 copies (xs
+ *                                                 unused)
+ *  hq [T*k, I], hs [T*k, I/32]                    act2(h) in slot order, same
+ *                                                 forms
+ *  yp [T*k, H] fp32                               W2 act2(h) per slot
+ *  x_stream[2] [T, H] bf16                        SIZE_MAX here (chain only)
+ *  total                                          moe_mxfp4_workspace_size
+ * The layout depends only on the arguments.  Returns MOE_OK or an error for
+ * invalid arguments.  No counterpart in the papers: a support call for
+ * checking the layer's steps one by one.
+ */
+typedef struct {
+  size_t topk_idx, topk_w, cnt, off, perm, pos;
+  size_t xq, xs, hq, hs, yp;
+  size_t x_stream[2];
+  size_t total;
+} moe_workspace_layout;
+int moe_mxfp4_workspace_layout(int T, int H, int I, int E, int k, int act_mode,
+                               moe_workspace_layout* out);
+
+/*
+ * moe_mxfp4_workspace_layout_chain — the same for layer `layer` (0 <= layer <
+ * n_layers) of a moe_mxfp4_forward_chain workspace.  Every layer keeps its own
+ * routing arrays (topk_idx .. pos, all valid after the call).  xq/xs, hq/hs
+ * and yp are shared by the layers in turn: after the call xq/xs hold the last
+ * layer's act1 input (written by the previous layer's combine, or by the
+ * activation step when n_layers = 1), hq/hs and yp the last layer's.  With
+ * residual = 1, x_stream[(n_layers - 1) & 1] holds x_{n_layers-1}, the last
+ * layer's bf16 input (n_layers >= 2).
+ */
+int moe_mxfp4_workspace_layout_chain(int n_layers, int layer, int T, int H, int I, int E, int k,
+                                     int act_mode, moe_workspace_layout* out);
+
+/*
  * mxfp4_quantize — pack fp32 weights to MXFP4 with the layer's rule (offline).
  *  w        [rows, K] fp32 device, K a multiple of 32, 16-byte aligned
  *  out_fp4  [rows, K/2] packed E2M1 (element 2i in the low nibble of byte i)
@@ -248,9 +296,11 @@ int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4,
  *  router_logits [T, E] fp32 device;  outputs (device):
  *  topk_idx [T, k] int32, topk_w [T, k] fp32, cnt [E] int32, off [E+1] int32,
  *  perm [T*k] int32 (slot -> token), pos [T*k] int32 ((t*k + j) -> slot).
- * Slots are expert-major; within an expert, ascending t*k + j.  Scratch (the
- * chunk list) from the library-owned cache (shared: see the ordering rules
- * under moe_mxfp4_forward).
+ * Slots are expert-major; within an expert, ascending t*k + j.  The kernels
+ * are those the forward runs for the same T: one launch of the small-block
+ * routing kernel for T <= 32, the top-k and permutation kernels above.
+ * Scratch (the chunk list) from the library-owned cache (shared: see the
+ * ordering rules under moe_mxfp4_forward).
  */
 int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* topk_idx,
                     float* topk_w, int32_t* cnt, int32_t* off, int32_t* perm, int32_t* pos,
@@ -421,6 +471,11 @@ int moe_mxfp4_get_status(cudaStream_t stream);
 /* number of kernels this library has launched in this process (all devices,
  * all entry points); a diagnostic for counting launches in a timed region */
 uint64_t moe_mxfp4_launch_count(void);
+
+/* number of device allocations (cudaMalloc) this library has made in this
+ * process (all devices): its scratch cache growing.  A diagnostic: a call
+ * that must not allocate leaves it unchanged. */
+uint64_t moe_mxfp4_alloc_count(void);
 
 /* human-readable name of an moe_status value (static string) */
 const char* moe_status_string(int status);

@@ -45,6 +45,13 @@ class moe_opts(ctypes.Structure):
                 ("n_step_events", ctypes.c_int)]
 
 
+class moe_workspace_layout(ctypes.Structure):
+    """Byte offsets of a forward's intermediate arrays inside a caller workspace."""
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("topk_idx", "topk_w", "cnt", "off", "perm", "pos", "xq", "xs", "hq", "hs",
+                 "yp")] + [("x_stream", ctypes.c_size_t * 2), ("total", ctypes.c_size_t)]
+
+
 _lib = None
 
 
@@ -95,6 +102,14 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_get_status.restype = i
         L.moe_mxfp4_launch_count.argtypes = []
         L.moe_mxfp4_launch_count.restype = ctypes.c_uint64
+        L.moe_mxfp4_alloc_count.argtypes = []
+        L.moe_mxfp4_alloc_count.restype = ctypes.c_uint64
+        L.moe_mxfp4_workspace_layout.argtypes = [i, i, i, i, i, i,
+                                                 ctypes.POINTER(moe_workspace_layout)]
+        L.moe_mxfp4_workspace_layout.restype = i
+        L.moe_mxfp4_workspace_layout_chain.argtypes = [i, i, i, i, i, i, i, i,
+                                                       ctypes.POINTER(moe_workspace_layout)]
+        L.moe_mxfp4_workspace_layout_chain.restype = i
         L.moe_status_string.argtypes = [i]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -259,6 +274,26 @@ def moe_mxfp4_get_status(stream=None) -> int:
 
 def moe_mxfp4_launch_count() -> int:
     return int(lib().moe_mxfp4_launch_count())
+
+
+def moe_mxfp4_alloc_count() -> int:
+    return int(lib().moe_mxfp4_alloc_count())
+
+
+def moe_mxfp4_workspace_layout(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> moe_workspace_layout:
+    out = moe_workspace_layout()
+    _check(lib().moe_mxfp4_workspace_layout(T, H, I, E, k, act_mode, ctypes.byref(out)),
+           "moe_mxfp4_workspace_layout")
+    return out
+
+
+def moe_mxfp4_workspace_layout_chain(n_layers, layer, T, H, I, E, k,
+                                     act_mode=MOE_ACT_MXFP8) -> moe_workspace_layout:
+    out = moe_workspace_layout()
+    _check(lib().moe_mxfp4_workspace_layout_chain(n_layers, layer, T, H, I, E, k, act_mode,
+                                                  ctypes.byref(out)),
+           "moe_mxfp4_workspace_layout_chain")
+    return out
 
 
 def moe_status_string(status: int) -> str:

@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <climits>
+#include <cstdint>
 #include <atomic>
 #include <cstring>
 #include <mutex>
@@ -51,6 +52,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 std::atomic<uint64_t> g_launches{0};
+std::atomic<uint64_t> g_allocs{0};  // device allocations of the scratch cache
 
 // records the step markers of moe_opts around the kernels of one call
 struct Steps {
@@ -411,6 +413,25 @@ Work carve_chain(void* base, const ChainLayout& C, int l) {
   return w;
 }
 
+// the public form of a layout: routing arrays `route_shift` bytes and the
+// activation buffers `act_shift` bytes after the layout's own offsets
+moe_workspace_layout public_layout(const Layout& L, size_t route_shift, size_t act_shift) {
+  moe_workspace_layout o{};
+  o.topk_idx = route_shift + L.topk_idx;
+  o.topk_w = route_shift + L.topk_w;
+  o.cnt = route_shift + L.cnt;
+  o.off = route_shift + L.off;
+  o.perm = route_shift + L.perm;
+  o.pos = route_shift + L.pos;
+  o.xq = act_shift + L.xq;
+  o.xs = act_shift + L.xs;
+  o.hq = act_shift + L.hq;
+  o.hs = act_shift + L.hs;
+  o.yp = act_shift + L.yp;
+  o.x_stream[0] = o.x_stream[1] = SIZE_MAX;
+  return o;
+}
+
 // library-owned scratch of at least `bytes` on this device
 int cached_workspace(DeviceState* d, size_t bytes, void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
@@ -422,6 +443,7 @@ int cached_workspace(DeviceState* d, size_t bytes, void** out) {
       cudaGetLastError();
       return MOE_ERR_NO_MEMORY;
     }
+    g_allocs.fetch_add(1, std::memory_order_relaxed);
     d->ws_bytes = bytes;
   }
   *out = d->ws;
@@ -523,13 +545,24 @@ int enqueue_route(const float* logits, bool first, int T, int E, int k, int chun
   return launch_status();
 }
 
+// CTAs of the small-block routing kernel: step a4 has T * ceil(H / 1024)
+// token-major warp units; each CTA's warps T..31 take one unit while warps
+// 0..T-1 run the top-k (all 32 warps take units after the routing when
+// T = 32), so this many CTAs cover the units in one round.  One CTA when there
+// is no a4 (routing alone).
+int small_route_grid(int T_act, int H, int sms) {
+  const int64_t units = (int64_t)T_act * ((H / 32 + 31) / 32);
+  const int per = T_act < kSmallRouteTokens ? kSmallRouteTokens - T_act : kSmallRouteTokens;
+  return grid_for(units, per, sms);
+}
+
 // Steps a1-a4 in one launch for a block of T <= kSmallRouteTokens tokens
-// (route_act_small_kernel); `first`: the call's first kernel (ordinary launch)
+// (route_act_small_kernel); `first`: the call's first kernel (ordinary launch);
+// x == nullptr: routing alone (no a4)
 int enqueue_route_act_small(const float* logits, bool first, int act, const uint16_t* x, int T,
                             int H, int E, int k, int chunk_max, const Work& w, DeviceState* d,
                             cudaStream_t s, Steps& st) {
-  const int64_t units = (int64_t)T * k * ((H / 32 + 31) / 32);
-  const dim3 grid(grid_for(units, 32, d->sms));
+  const dim3 grid(small_route_grid(x ? T : 0, H, d->sms));
   const size_t smem = small_route_smem(T, E, k, w.max_chunks).total;
   st.mark();
   auto go = [&](auto kernel) {
@@ -595,8 +628,7 @@ int enqueue_route_act_small_layers(const float* const* logits, int n, int act, c
                                    int64_t stride, DeviceState* d, cudaStream_t s, Steps& st) {
   LayerLogits lg{};
   for (int l = 0; l < n; ++l) lg.p[l] = logits[l];
-  const int64_t units = (int64_t)T * k * ((H / 32 + 31) / 32);
-  const dim3 grid(grid_for(units, 32, d->sms), n);
+  const dim3 grid(small_route_grid(T, H, d->sms), n);
   const size_t smem = small_route_smem(T, E, k, w0.max_chunks).total;
   st.mark();
   auto go = [&](auto kernel) {
@@ -1050,6 +1082,13 @@ int moe_mxfp4_route(const float* router_logits, int T, int E, int k, int32_t* to
   w.perm = perm;
   w.pos = pos;
   Steps st{nullptr, stream};
+  // the kernels the forward runs for this T
+  if (T <= kSmallRouteTokens) {
+    if ((rc = enqueue_route_act_small(router_logits, true, MOE_ACT_MXFP8, nullptr, T, 128, E, k,
+                                      kChunkNarrow, w, d, stream, st)))
+      return rc;
+    return launch_status();
+  }
   return enqueue_route(router_logits, true, T, E, k, kChunkNarrow, w, d, stream, st);
 }
 
@@ -1241,6 +1280,35 @@ int moe_mxfp4_get_status(cudaStream_t stream) {
 
 uint64_t moe_mxfp4_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+uint64_t moe_mxfp4_alloc_count(void) { return g_allocs.load(std::memory_order_relaxed); }
+
+int moe_mxfp4_workspace_layout(int T, int H, int I, int E, int k, int act_mode,
+                               moe_workspace_layout* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_for(T, H, I, E, k, act_mode);
+  *out = public_layout(L, 0, 0);
+  out->total = L.total;
+  return MOE_OK;
+}
+
+int moe_mxfp4_workspace_layout_chain(int n_layers, int layer, int T, int H, int I, int E, int k,
+                                     int act_mode, moe_workspace_layout* out) {
+  if (!out || n_layers < 1 || n_layers > MOE_MAX_CHAIN || layer < 0 || layer >= n_layers)
+    return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  const ChainLayout C = chain_layout(n_layers, T, H, I, E, k, act_mode);
+  *out = public_layout(C.base, (size_t)layer * C.route_block, C.act_shift);
+  out->x_stream[0] = C.xb[0];
+  out->x_stream[1] = C.xb[1];
+  out->total = C.total;
+  return MOE_OK;
+}
+
 // ---------------------------------------------------------------- no-alloc entry point
 //
 // Scratch for moe_mxfp4_forward_noalloc: a fixed-size array in the module's
@@ -1279,8 +1347,16 @@ int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
                               const uint8_t* w13_fp4, const uint8_t* w13_e8m0,
                               const uint8_t* w2_fp4, const uint8_t* w2_e8m0, int T, int H, int I,
                               int E, int k, void* y_bf16, cudaStream_t stream) {
+  // argument errors first, in moe_mxfp4_forward's order (pointers, shape,
+  // alignment), then the scratch size
+  if (!x_bf16 || !router_logits || !w13_fp4 || !w13_e8m0 || !w2_fp4 || !w2_e8m0 || !y_bf16)
+    return MOE_ERR_INVALID_ARG;
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
+  if (!aligned(w13_fp4, 32) || !aligned(w2_fp4, 32) || !aligned(x_bf16, 16) ||
+      !aligned(router_logits, 16) || !aligned(w13_e8m0, 16) || !aligned(w2_e8m0, 16) ||
+      !aligned(y_bf16, 16))
+    return MOE_ERR_ALIGNMENT;
   if (layout_for(T, H, I, E, k, MOE_ACT_MXFP8).total > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
     return MOE_ERR_NO_MEMORY;  // needs more scratch than the static array holds
   if (T == 0) return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,

@@ -180,3 +180,77 @@ def test_chain_workspace_size(moe):
     assert moe.moe_mxfp4_workspace_size_chain(0, 16, 256, 128, 8, 2) == 0
     assert moe.moe_mxfp4_workspace_size_chain(2, 16, 250, 128, 8, 2) == 0
     assert moe.moe_mxfp4_workspace_size_chain(2, 16, 256, 128, 8, 2, 9) == 0
+
+
+def _regions(lay, T, H, I, E, k, act):
+    """(name, offset, bytes) of every array a layout names"""
+    ab = 2 if act == 1 else 1
+    return [("topk_idx", lay.topk_idx, T * k * 4), ("topk_w", lay.topk_w, T * k * 4),
+            ("cnt", lay.cnt, E * 4), ("off", lay.off, (E + 1) * 4),
+            ("perm", lay.perm, T * k * 4), ("pos", lay.pos, T * k * 4),
+            ("xq", lay.xq, T * k * H * ab), ("xs", lay.xs, T * k * H // 32),
+            ("hq", lay.hq, T * k * I * ab), ("hs", lay.hs, T * k * I // 32),
+            ("yp", lay.yp, T * k * H * 4)]
+
+
+@pytest.mark.parametrize("act", [0, 1])
+@pytest.mark.parametrize("T,H,I,E,k", [(16, 256, 128, 8, 2), (8, 6144, 2048, 384, 8),
+                                       (1, 128, 128, 1, 1)])
+def test_workspace_layout_is_disjoint_and_aligned(moe, T, H, I, E, k, act):
+    lay = moe.moe_mxfp4_workspace_layout(T, H, I, E, k, act)
+    assert lay.total == moe.moe_mxfp4_workspace_size(T, H, I, E, k, act)
+    assert lay.x_stream[0] == lay.x_stream[1] == 2**64 - 1     # SIZE_MAX: single layer
+    regs = sorted(_regions(lay, T, H, I, E, k, act), key=lambda r: r[1])
+    for (n0, o0, b0), (n1, o1, b1) in zip(regs, regs[1:]):
+        assert o0 + b0 <= o1, (n0, n1)
+    for n, o, b in regs:
+        assert o % 256 == 0 and o + b <= lay.total, n
+
+
+def test_chain_workspace_layout(moe):
+    n, T, H, I, E, k = 3, 8, 256, 128, 8, 2
+    lays = [moe.moe_mxfp4_workspace_layout_chain(n, l, T, H, I, E, k) for l in range(n)]
+    total = moe.moe_mxfp4_workspace_size_chain(n, T, H, I, E, k)
+    route = ("topk_idx", "topk_w", "cnt", "off", "perm", "pos")
+    for lay in lays:
+        assert lay.total == total
+        for name, o, b in _regions(lay, T, H, I, E, k, 0):
+            assert o % 256 == 0 and o + b <= total, name
+        for s in lay.x_stream:
+            assert s % 256 == 0 and s + T * H * 2 <= total
+    # every layer has its own routing arrays; the activation buffers are shared
+    for name in route:
+        assert len({getattr(l, name) for l in lays}) == n, name
+    for name in ("xq", "xs", "hq", "hs", "yp"):
+        assert len({getattr(l, name) for l in lays}) == 1, name
+    spans = [(o, o + b) for lay in lays for nm, o, b in _regions(lay, T, H, I, E, k, 0)
+             if nm in route]
+    spans += [(o, o + b) for nm, o, b in _regions(lays[0], T, H, I, E, k, 0) if nm not in route]
+    spans += [(s, s + T * H * 2) for s in lays[0].x_stream]
+    spans.sort()
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0
+    L = moe.lib()
+    lay = moe.moe_workspace_layout()
+    import ctypes
+    assert L.moe_mxfp4_workspace_layout_chain(3, 3, T, H, I, E, k, 0, ctypes.byref(lay)) == -1
+    assert L.moe_mxfp4_workspace_layout_chain(3, 0, T, 250, I, E, k, 0, ctypes.byref(lay)) == -2
+    assert L.moe_mxfp4_workspace_layout(T, H, I, E, k, 0, None) == -1
+
+
+def test_noalloc_checks_arguments_before_its_scratch_limit(moe):
+    """A null or misaligned pointer is reported as such even when the shape would also be
+    too large for the fixed scratch array (the forward's order: arguments, then size)."""
+    L = moe.lib()
+    big_T = 4096                                    # far past the array at the full shape
+    args = [256, 512, 1024, 2048, 4096, 8192]
+    assert L.moe_mxfp4_forward_noalloc(None, *args[1:], big_T, 6144, 2048, 384, 8, 16384,
+                                       None) == -1
+    assert L.moe_mxfp4_forward_noalloc(*args[:2], 1040, *args[3:], big_T, 6144, 2048, 384, 8,
+                                       16384, None) == -3
+    assert L.moe_mxfp4_forward_noalloc(*args, big_T, 6144, 2048, 384, 8, 16384, None) == -5
+    assert L.moe_mxfp4_forward_noalloc(*args, 4, 250, 128, 8, 2, 16384, None) == -2
+
+
+def test_alloc_counter_is_exported(moe):
+    assert moe.moe_mxfp4_alloc_count() >= 0

@@ -183,3 +183,33 @@ def test_literal_nested_loops_equal_the_oracle_bit_for_bit(synth_mod, oracle_mod
                 acc += g[j] * d[j][o]
             want[t, o] = acc
     assert (y64 == want).all()
+
+
+def test_bf16_mode_rounds_h_to_the_nearest_bf16(synth_mod, oracle_mod):
+    """bf16-emulation mode (act1 the identity on the bf16 x, act2 = round h to bf16), pinned
+    against numpy and torch: with one expert, the oracle's h must be bf16 values (torch's own
+    bf16 cast leaves them unchanged), each within half a bf16 step of the exact fp64 h that
+    numpy computes from independently decoded weights, equal to torch's rounding of that h
+    almost everywhere (torch may round fp64 -> fp32 -> bf16 twice), and y must be that
+    rounded h times W2 — not the exact layer's y, so a skipped act2 fails."""
+    import torch
+    T, H, I = 6, 96, 64
+    x, lg, w13, s13, w2, s2 = make_layer(synth_mod, oracle_mod, T, H, I, 1, 31)
+    _, y64, h = oracle_mod.moe_forward(x, lg, w13, s13, w2, s2, 1, 2, want_h=True)
+    _, yex, _ = oracle_mod.moe_forward(x, lg, w13, s13, w2, s2, 1, 0)
+    W13 = R.dequant(w13, s13)[0]
+    W2 = R.dequant(w2, s2)[0]
+    xf = R.bf16_to_f64(x)
+    hr = R.silu(xf @ W13[:I].T) * (xf @ W13[I:].T)
+    hg = h[:, 0, :]
+    as_bf16 = torch.from_numpy(hg).to(torch.bfloat16).to(torch.float64).numpy()
+    assert (as_bf16 == hg).all()
+    step = np.ldexp(1.0, np.floor(np.log2(np.abs(hr))).astype(np.int64) - 7)
+    assert (np.abs(hg - hr) <= 0.5 * step * (1 + 1e-9)).all()
+    tb = torch.from_numpy(hr).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.mean(tb == hg) > 0.99
+    np.testing.assert_allclose(y64, hg @ W2.T, rtol=1e-11, atol=1e-15)
+    assert not np.allclose(y64, yex, rtol=1e-5, atol=0)
+    # act1 is the identity: the exact layer's h equals numpy's unrounded h
+    _, _, hx = oracle_mod.moe_forward(x, lg, w13, s13, w2, s2, 1, 0, want_h=True)
+    np.testing.assert_allclose(hx[:, 0, :], hr, rtol=1e-12, atol=1e-15)

@@ -14,6 +14,8 @@ constexpr int kCombineBatch = 4;
 // sum_j g[t, j] * yp[pos[t, j], h0 .. h0+3] in fp32, j = 0..k-1 in order (one
 // fmaf per term from 0); kCombineBatch rows' loads are issued before their
 // multiply-adds so a thread waits for k / kCombineBatch round trips, not k
+// kL2: load yp from L2 only (rows written by other CTAs of the same launch)
+template <bool kL2 = false>
 __device__ __forceinline__ float4 combine4(const float* __restrict__ yp,
                                            const int32_t* __restrict__ pos,
                                            const float* __restrict__ gate, int64_t t, int64_t H,
@@ -26,7 +28,9 @@ __device__ __forceinline__ float4 combine4(const float* __restrict__ yp,
     for (int u = 0; u < kCombineBatch; ++u) {
       if (j0 + u < k) {
         g[u] = gate[t * k + j0 + u];
-        v[u] = *reinterpret_cast<const float4*>(yp + (int64_t)pos[t * k + j0 + u] * H + h0);
+        const float4* src =
+            reinterpret_cast<const float4*>(yp + (int64_t)pos[t * k + j0 + u] * H + h0);
+        v[u] = kL2 ? __ldcg(src) : *src;
       }
     }
 #pragma unroll

@@ -61,6 +61,7 @@ struct Work {
   float* yp;          // [T*k, H] per-slot expert outputs (fp32)
   float* part;        // router split-K partials [splits][T][E] (routed forward only)
   float* rlogits;     // router logits [T, E] (routed forward only)
+  uint8_t* sync;      // grid-wide barrier words of the whole-layer launch
   int max_chunks;
 };
 

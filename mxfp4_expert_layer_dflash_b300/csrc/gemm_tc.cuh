@@ -48,9 +48,14 @@
 
 #include <cuda.h>
 
+#include <climits>
+
+#include "combine.cuh"
 #include "common.cuh"
 #include "fmt.cuh"
+#include "grid_sync.cuh"
 #include "ptx.cuh"
+#include "route_layer.cuh"
 
 namespace moe {
 
@@ -99,6 +104,14 @@ struct TcParams {
   int* status;
   unsigned long long timeout_ns;
   NextGemm1 next;       // next.stages == 0 unless this is a chained layer's last GEMM launch
+  // ---- the whole-layer launch (kModeLayer): GEMM1, GEMM2 and the combine,
+  // and for T <= 32 also the routing and the activation step
+  LayerRouteParams route;  // route.T > 0: steps a1-a4 run inside the launch
+  GridSync sync;           // grid-wide barriers (act1 rows written; GEMM2 outputs written)
+  const int32_t* pos;      // routing done before the launch: [T*k] slots
+  const float* gate;       // [T*k] gates
+  uint16_t* y;             // [T, H] bf16 output of the combine
+  int T, H, k;
 };
 
 template <int kNMax>
@@ -125,8 +138,18 @@ struct TcCfg {
   static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-// Kernel modes: one GEMM per launch, or both GEMMs in one persistent launch.
-constexpr int kModeGemm1 = 0, kModeGemm2 = 1, kModeBoth = 2;
+// Kernel modes: one GEMM per launch, both GEMMs in one persistent launch, or
+// the whole layer in one persistent launch (both GEMMs, then the combine;
+// with the routing and the activation step in front for T <= 32).
+constexpr int kModeGemm1 = 0, kModeGemm2 = 1, kModeBoth = 2, kModeLayer = 3;
+
+// shared memory of a launch in mode kMode: the whole-layer launch with
+// narrow chunks also keeps its own routing (LayerRouteState)
+template <int kNMax, int kMode>
+constexpr size_t tc_smem_bytes() {
+  return TcCfg<kNMax>::kSmem +
+         (kMode == kModeLayer && kNMax == kChunkNarrow ? sizeof(LayerRouteState) : 0);
+}
 
 // Walks the (work item, k-stage) sequence of one CTA over all phases
 // (kPhases is 1 for single-GEMM launches, so the phase folds to a constant).
@@ -134,14 +157,16 @@ template <int kPhases>
 struct FillCursor {
   // per-launch constants, copied once (no parameter-space reads per item)
   const int4* chunks;
+  const uint32_t* packed;  // the chunk list in shared memory (whole-layer launch), or null
   int step, n0, ntot;      // n0: items of phase 0; ntot: items of all phases
   int mtl[2], kst[2];      // tile pairs per chunk and k-stages per item, per phase
   // position
   int item, ks, phase, mt, ksteps, chunk;
   int4 ch;
-  __device__ __forceinline__ void start(const TcParams& p, int first, int stp, int items0,
-                                        int items_all) {
+  __device__ __forceinline__ void start(const TcParams& p, const uint32_t* pk, int first, int stp,
+                                        int items0, int items_all) {
     chunks = p.chunks;
+    packed = pk;
     step = stp;
     n0 = items0;
     ntot = items_all;
@@ -167,7 +192,7 @@ struct FillCursor {
       const int m = phase ? mtl[1] : mtl[0];
       chunk = local / m;
       mt = local % m;
-      ch = chunks[chunk];
+      ch = packed ? unpack_chunk(packed[chunk]) : chunks[chunk];
       ksteps = phase ? kst[1] : kst[0];
     }
   }
@@ -218,12 +243,15 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 }
 
 // bounded wait until GEMM1 has published every tile pair of `chunk`
+// (whole-layer launch: `tag` != 0, also gives up when another CTA has)
 __device__ __forceinline__ bool wait_chunk_ready(const TcParams& p, int chunk, int target,
                                                  unsigned long long timeout_ns,
-                                                 const volatile int* abort) {
+                                                 const volatile int* abort, uint64_t tag = 0) {
   const uint64_t deadline = ptx::globaltimer() + timeout_ns;
+  uint32_t spins = 0;
   while (ld_acquire(p.gemm1_done + chunk) < target) {
     if (*abort || ptx::globaltimer() > deadline) return false;
+    if (tag && (++spins & 15u) == 0 && grid_aborted(p.sync, tag)) return false;
   }
   return true;
 }
@@ -231,11 +259,16 @@ __device__ __forceinline__ bool wait_chunk_ready(const TcParams& p, int chunk, i
 template <int kNMax, int kMode>
 __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_constant__ TcParams p) {
   using C = TcCfg<kNMax>;
-  constexpr int kPhases = kMode == kModeBoth ? 2 : 1;
+  constexpr bool kLayer = kMode == kModeLayer;
+  constexpr int kPhases = (kMode == kModeBoth || kLayer) ? 2 : 1;
   using Cursor = FillCursor<kPhases>;
-  // is this phase the SwiGLU GEMM1 / a GEMM2 waiting on same-launch h?
-  auto gated_phase = [](int phase) { return kMode == kModeGemm1 || (kMode == kModeBoth && phase == 0); };
-  auto dep_phase = [](int phase) { return kMode == kModeBoth && phase == 1; };
+  // whole-layer launch that also routes (T <= 32; narrow chunks only)
+  const bool route_in = kLayer && kNMax == kChunkNarrow && p.route.T > 0;
+  // is this phase the SwiGLU GEMM1 / one whose inputs this launch writes
+  // (GEMM2 reads GEMM1's h; with routing inside, GEMM1 reads the act1 rows
+  // that every CTA writes)?
+  auto gated_phase = [](int phase) { return kMode == kModeGemm1 || (kPhases == 2 && phase == 0); };
+  auto dep_phase = [&](int phase) { return kPhases == 2 && (phase == 1 || route_in); };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -250,6 +283,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // seen published (items of a CTA only increase); the scale stagers read it
   // instead of polling the global counters themselves
   int* dep_ready = reinterpret_cast<int*>(tmem_slot + 2);
+  // whole-layer launch that routes: this CTA's act1 rows are written
+  int* act_ready = reinterpret_cast<int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -264,6 +299,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     *dep_ready = -1;
+    *act_ready = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -284,12 +320,30 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // routing outputs, activations and (for GEMM2) h come from earlier kernels
   grid_dependency_wait();
 
-  const int n_chunks = p.meta[0];
+  // whole-layer launch: this call's barrier tag, and for T <= 32 the routing
+  // of the block, done by every CTA in its own shared memory (the stage
+  // buffers serve as scratch before the first copy lands in them)
+  LayerRouteState* rs =
+      reinterpret_cast<LayerRouteState*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
+  const uint64_t tag = kLayer ? grid_sync_tag(p.sync) : 0;
+  // the value a published (chunk, GEMM1 tile pair) flag holds in this call
+  // (a kind never written when the debug flag forces the wait to run out)
+  const uint64_t flag_want =
+      tag | (p.ph[1].dep_target == INT_MAX ? kChunkFlagNever : kChunkFlagKind);
+  if (route_in) {
+    layer_route_block(p.route, smem, rs, blockIdx.x == 0, p.status);
+    ptx::fence_proxy_async_smem();  // generic scratch writes before TMA writes the stages
+    __syncthreads();
+  }
+  const uint32_t* s_chunks = route_in ? rs->chunks : nullptr;
+  auto chunk_at = [&](int i) { return s_chunks ? unpack_chunk(s_chunks[i]) : p.chunks[i]; };
+  const int n_chunks = route_in ? rs->n_chunks : p.meta[0];
   const int items0 = n_chunks * p.ph[0].m_tiles;
   const int items_all = items0 + (kPhases > 1 ? n_chunks * p.ph[1].m_tiles : 0);
   auto fail = [&](int code) {
     set_status(p.status, code);
     *abort_flag = 1;
+    if (kLayer) grid_give_up(p.sync, tag);
   };
   auto deadline = [&]() { return ptx::globaltimer() + p.timeout_ns; };
 
@@ -300,6 +354,57 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     return __all_sync(0xffffffffu, ptx::mbar_wait(bar, parity, deadline(), abort_flag));
   };
 
+  // ---- whole-layer launch: work of the aux warps (1, 3 and the epilogue
+  // warps; 192 threads, named barriers 1-3), around the GEMM items
+  constexpr int kAuxWarps = 6, kAuxThreads = kAuxWarps * 32;
+  const int aux_w = warp == 1 ? 0 : warp == 3 ? 1 : warp - 6;  // valid for aux warps
+  // step a4 (routing inside the launch): the slot rows of the chunks of this
+  // CTA's GEMM1 items, a warp per (slot row, run of 32 blocks of 32); other
+  // CTAs multiplying the same chunk write the same bytes.  Then the rows are
+  // handed to this CTA's producer (its TMA reads them).
+  auto aux_act1 = [&]() {
+    const int64_t H = p.ph[0].K;
+    const int segs = (int)((H / 32 + 31) / 32);
+    int u = 0;  // unit counter over this CTA's rows, dealt round-robin to the aux warps
+    for (int item = blockIdx.x; item < items0; item += gridDim.x) {
+      const int4 ch = chunk_at(item / p.ph[0].m_tiles);
+      for (int r = 0; r < ch.z; ++r)
+        for (int sg = 0; sg < segs; ++sg, ++u)
+          if (u % kAuxWarps == aux_w)
+            layer_act1_unit(p.route.x, rs->perm[ch.y + r], ch.y + r, sg, H, p.route.xq,
+                            p.route.xs);
+    }
+    fence_proxy_async_global();  // generic writes before this CTA's TMA reads them
+    named_barrier_sync(1, kAuxThreads);
+    if (aux_w == 0 && lane == 0) st_release_cta(act_ready, 1);
+  };
+  // step a8 once every CTA's GEMM2 outputs are written: the gate-weighted sum
+  // of each token's k slot rows in slot order, the combine kernel's arithmetic
+  auto aux_combine = [&]() {
+    named_barrier_sync(2, kAuxThreads);  // this CTA's epilogue stores are done
+    if (aux_w == 0) {
+      if (lane == 0) grid_arrive(p.sync, kSyncOut, tag);
+      __syncwarp();
+      if (!grid_wait(p.sync, kSyncOut, tag, p.timeout_ns, abort_flag)) {
+        if (lane == 0) fail(kStatusTimeout);
+      } else if (blockIdx.x == 0 && lane == 0) {
+        grid_sync_retire(p.sync, tag);  // every CTA has read the counter by now
+      }
+    }
+    named_barrier_sync(3, kAuxThreads);
+    if (*abort_flag) return;
+    const int k = p.k;
+    const int64_t H = p.H, per_tok = H / 4, total = (int64_t)p.T * per_tok;
+    const int32_t* pos = route_in ? rs->pos : p.pos;
+    const float* gate = route_in ? rs->gate : p.gate;
+    for (int64_t i = (int64_t)blockIdx.x * kAuxThreads + aux_w * 32 + lane; i < total;
+         i += (int64_t)gridDim.x * kAuxThreads) {
+      const int64_t t = i / per_tok, h0 = (i - t * per_tok) * 4;
+      *reinterpret_cast<uint2*>(p.y + t * H + h0) =
+          bf16x4_bits(combine4<true>(p.yp, pos, gate, t, H, k, h0));
+    }
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer
     // Like the MMA issuer: a convergent warp walks the fills and one elected
@@ -307,22 +412,88 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
     uint32_t fill = 0;
     bool ok = true;
+    bool act_seen = !route_in;  // every CTA's act1 rows written (routing inside the launch)
+    // With the routing inside the launch, the weight tiles of the first fills
+    // do not wait for the act1 barrier: they are issued at once (each stage's
+    // barrier expects both operands' bytes; the activation tiles follow once
+    // the barrier is passed), so the barrier's latency hides behind them.
+    uint32_t prefilled = 0;
+    if (route_in) {
+      int it = blockIdx.x, ks = 0;
+      while (prefilled < (uint32_t)C::kStages && it < items_all) {
+        const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
+        const TcPhase& ph = p.ph[phase];
+        const int local = it - (phase ? items0 : 0);
+        const int chunk = local / ph.m_tiles;
+        const int row0 = chunk_at(chunk).x * ph.R + (local - chunk * ph.m_tiles) * ph.m_stride;
+        const uint32_t tx = C::kA * C::kTxA + (uint32_t)((chunk_at(chunk).z + 15) & ~15) * 128;
+        uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
+        ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
+        ptx::tma_load_2d_warp(st, &ph.map_w, &full[prefilled], ks * kBlockK, row0, pol_w);
+        ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[prefilled], ks * kBlockK,
+                              row0 + ph.half, pol_w);
+        ++prefilled;
+        if (++ks == ph.K / kBlockK) {
+          ks = 0;
+          it += gridDim.x;
+        }
+      }
+    }
     for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x) {
       const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
       const TcPhase& ph = p.ph[phase];
       const int local = item - (phase ? items0 : 0);
       const int chunk = local / ph.m_tiles;
       const int mt = local - chunk * ph.m_tiles;
-      const int4 ch = p.chunks[chunk];
-      // h of this chunk must be published by GEMM1 (unless the look-ahead of
-      // the previous item already saw it complete)
-      if (dep_phase(phase) && ld_acquire_cta(dep_ready) < item) {
-        const bool ready = wait_chunk_ready(p, chunk, ph.dep_target, p.timeout_ns, abort_flag);
+      const int4 ch = chunk_at(chunk);
+      // With the routing inside the launch, a GEMM1 item's activation tiles
+      // are this CTA's own act1 rows: wait (bounded) until its aux warps have
+      // written them.
+      if (!act_seen && phase == 0) {
+        const uint64_t until = deadline();
+        bool ready = true;
+        while (ld_acquire_cta(act_ready) == 0) {
+          if (*abort_flag || ptx::globaltimer() > until) {
+            ready = false;
+            break;
+          }
+        }
         if (!__all_sync(0xffffffffu, ready)) {
           if (lane == 0) fail(kStatusTimeout);
           break;
         }
+        act_seen = true;
         fence_proxy_async_global();
+      }
+      // h of this chunk must be published by GEMM1 (unless the look-ahead of
+      // the previous item already saw it complete); a GEMM1 item whose act1
+      // rows come from this launch is ready once the wait above is passed
+      if (dep_phase(phase) && ld_acquire_cta(dep_ready) < item) {
+        bool ready = true;
+        if (phase == 1) {
+          if (kLayer) {  // every GEMM1 tile pair of the chunk has set its flag
+            const uint64_t until = deadline();
+            uint32_t spins = 0;
+            while (!chunk_tiles_published(p.sync, chunk * p.ph[0].m_tiles * 4,
+                                          p.ph[0].m_tiles * 4, flag_want)) {
+              bool stop = false;
+              if ((++spins & 7u) == 0)
+                stop = *abort_flag || grid_aborted(p.sync, tag) || ptx::globaltimer() > until;
+              if (__any_sync(0xffffffffu, stop)) {
+                ready = false;
+                break;
+              }
+            }
+            if (ready) fence_acquire_gpu();
+          } else {
+            ready = wait_chunk_ready(p, chunk, ph.dep_target, p.timeout_ns, abort_flag);
+          }
+        }
+        if (!__all_sync(0xffffffffu, ready)) {
+          if (lane == 0) fail(kStatusTimeout);
+          break;
+        }
+        if (phase == 1) fence_proxy_async_global();
         if (lane == 0) st_release_cta(dep_ready, item);
       }
       // Look-ahead (single-launch path): read the next item's chunk counter now
@@ -330,9 +501,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       // this item's copies; if the chunk is complete, publish the next item
       // early so the scale stagers can load its h scales ahead of time.
       const int nxt = item + (int)gridDim.x;
+      // the next item is a GEMM1 item of a launch that routes: ready already
+      if (route_in && nxt < items0 && lane == 0) st_release_cta(dep_ready, nxt);
       bool look = kPhases > 1 && nxt < items_all && nxt >= items0;
       int look_cnt = 0;
-      if (look) look_cnt = ld_relaxed(p.gemm1_done + (nxt - items0) / p.ph[1].m_tiles);
+      bool look_flags = true;  // (whole-layer launch) this lane's flags of the next chunk
+      if (look) {
+        const int nch = (nxt - items0) / p.ph[1].m_tiles;
+        if (kLayer) {
+          for (int i = lane; i < p.ph[0].m_tiles * 4; i += 32)
+            look_flags &= ld_relaxed_u64(p.sync.chunk_flags + nch * p.ph[0].m_tiles * 4 + i) ==
+                          flag_want;
+        } else {
+          look_cnt = ld_relaxed(p.gemm1_done + nch);
+        }
+      }
       const int ksteps = ph.K / kBlockK;
       const int nrows = (ch.z + 15) & ~15;
       const int row0 = ch.x * ph.R + mt * ph.m_stride;
@@ -340,21 +523,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       for (int ks = 0; ks < ksteps; ++ks, ++fill) {
         const int s = (int)(fill % C::kStages);
         const uint32_t use = fill / C::kStages;
-        if (!wait_all(&empty[s], (use & 1) ^ 1)) {
-          if (lane == 0) fail(kStatusTimeout);
-          ok = false;
-          break;
-        }
         uint8_t* st = smem + s * C::kStageBytes;
-        ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
-        ptx::tma_load_2d_warp(st, &ph.map_w, &full[s], ks * kBlockK, row0, pol_w);
-        ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[s], ks * kBlockK, row0 + ph.half,
-                              pol_w);
+        if (fill >= prefilled) {  // (prefilled fills have their weight tiles in flight)
+          if (!wait_all(&empty[s], (use & 1) ^ 1)) {
+            if (lane == 0) fail(kStatusTimeout);
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
+          ptx::tma_load_2d_warp(st, &ph.map_w, &full[s], ks * kBlockK, row0, pol_w);
+          ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[s], ks * kBlockK,
+                                row0 + ph.half, pol_w);
+        }
         for (int r = 0; r < nrows; r += kBoxRowsB)
           ptx::tma_load_2d_warp(st + C::kA * C::kATile + r * 128, &ph.map_x, &full[s],
                                 ks * kBlockK, ch.y + r, pol_x);
         if (look && ks == min(3, ksteps - 1)) {
-          if (__all_sync(0xffffffffu, look_cnt >= p.ph[1].dep_target)) {
+          if (__all_sync(0xffffffffu, kLayer ? look_flags : look_cnt >= p.ph[1].dep_target)) {
             fence_acq_rel_gpu();  // the relaxed load plus this fence: an acquire
             fence_proxy_async_global();
             if (lane == 0) st_release_cta(dep_ready, nxt);
@@ -391,7 +576,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x, ++j) {
       const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
       const int local = item - (phase ? items0 : 0);
-      const int4 ch = p.chunks[local / p.ph[phase].m_tiles];
+      const int4 ch = chunk_at(local / p.ph[phase].m_tiles);
       const int ksteps = p.ph[phase].K / kBlockK;
       const uint32_t N = (uint32_t)((ch.z + 15) & ~15);
       const int b = j % C::kAccBufs;
@@ -448,7 +633,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     bool vec = true;
     for (int ph = 0; ph < kPhases; ++ph) vec = vec && (p.ph[ph].K % (32 * 16)) == 0;
     Cursor ld, stc;
-    ld.start(p, blockIdx.x, gridDim.x, items0, items_all);
+    ld.start(p, s_chunks, blockIdx.x, gridDim.x, items0, items_all);
     stc = ld;
     uint32_t grp[2][kSfGroup][C::kWords];
     bool deferred[2] = {false, false};
@@ -529,7 +714,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
 #pragma unroll
         for (int w = 0; w < C::kWords; ++w) g[i][w] = 0;
       grp_at[gi] = ld;
-      if (kMode == kModeBoth) deferred[gi] = __any_sync(0xffffffffu, group_blocked(ld));
+      if (kPhases == 2) deferred[gi] = __any_sync(0xffffffffu, group_blocked(ld));
       if (!deferred[gi]) {
         if (vec) {
           if (ld.valid()) words_of_group(g, ld);
@@ -575,7 +760,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     while (ok && stc.valid()) {
 #pragma unroll
       for (int gi = 0; gi < 2; ++gi) {
-        if (kMode == kModeBoth && ok && stc.valid() && deferred[gi] &&
+        if (kPhases == 2 && ok && stc.valid() && deferred[gi] &&
             !finish_group(gi, grp[gi])) {
           if (lane == 0) fail(kStatusTimeout);
           ok = false;
@@ -610,10 +795,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
+    if (route_in) aux_act1();
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     Cursor c;
-    c.start(p, blockIdx.x, gridDim.x, items0, items_all);
+    c.start(p, s_chunks, blockIdx.x, gridDim.x, items0, items_all);
     for (int j = 0; c.valid(); ++j) {
       const TcPhase& ph = p.ph[c.phase];
       const int4 ch = c.ch;
@@ -671,7 +857,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_empty[b]);
-      if (kMode == kModeBoth && gated_phase(c.phase)) {
+      if (kLayer && gated_phase(c.phase)) {
+        // publish this warp's quarter of the tile pair of h: its generic
+        // stores made visible to other CTAs' TMA reads (async proxy) and
+        // loads, then its own flag (four per tile pair; no barrier among the
+        // epilogue warps, which may leave their loops at different items
+        // when a wait runs out)
+        fence_proxy_async_global();
+        __syncwarp();
+        if (lane == 0) publish_chunk_tile(p.sync, (chunk * ph.m_tiles + mt) * 4 + q, tag);
+      } else if (kPhases == 2 && gated_phase(c.phase)) {
         // publish this warp's quarter of h: its generic stores made visible to
         // other CTAs' TMA reads (async proxy) and loads, then one release
         // increment per warp (four per tile pair)
@@ -682,6 +877,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       }
       c.next_item();
     }
+    if (kLayer) aux_combine();
+  } else if (kLayer && (warp == 1 || warp == 3)) {
+    // ------------------------------------------------------------ aux (whole-layer launch)
+    if (route_in) aux_act1();
+    aux_combine();
   }
 
   if (*abort_flag) {  // let copies already in flight land before the CTA exits

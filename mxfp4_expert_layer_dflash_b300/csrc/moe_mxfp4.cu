@@ -120,12 +120,16 @@ bool set_small_route_smem() {
 template <int kN>
 bool set_gemm_smem() {
   const int bytes = (int)TcCfg<kN>::kSmem;
+  static_assert(tc_smem_bytes<kN, kModeLayer>() <= 232448, "shared memory of the layer launch");
   return cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeGemm1>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeGemm2>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeBoth>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeLayer>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem_bytes<kN, kModeLayer>()) == cudaSuccess;
 }
 
 // Launches `kernel` with programmatic stream serialization: it may be
@@ -148,9 +152,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Returns the launch's error (cudaSuccess when enqueued).
+// Returns the launch's error (cudaSuccess when enqueued).  `first`: the
+// call's first kernel (an ordinary launch, never overlapping earlier work).
 template <int kN>
-cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm) {
+cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams& prm,
+                        bool first = false) {
   const size_t smem = TcCfg<kN>::kSmem;
   if (mode == kModeGemm1)
     return launch_pdl(gemm_tc_kernel<kN, kModeGemm1>, dim3(grid), dim3(kTcThreads), smem, stream,
@@ -158,16 +164,19 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
   if (mode == kModeGemm2)
     return launch_pdl(gemm_tc_kernel<kN, kModeGemm2>, dim3(grid), dim3(kTcThreads), smem, stream,
                       prm);
-  // Both GEMMs in one launch: GEMM2 items wait for other CTAs' GEMM1 items, so
-  // every CTA must be resident at once.  A cooperative launch guarantees that,
-  // or fails without running anything.  It is also programmatic when the
-  // driver accepts both attributes: CTAs that start early block in
-  // grid_dependency_wait() before any cross-CTA wait, and the preceding kernel
-  // never waits on them.
+  // Both GEMMs (and, for the whole-layer mode, the combine and maybe the
+  // routing) in one launch: CTAs wait for other CTAs' work, so every CTA must
+  // be resident at once.  A cooperative launch guarantees that, or fails
+  // without running anything.  It is also programmatic when the driver
+  // accepts both attributes and the launch is not the call's first: CTAs that
+  // start early block in grid_dependency_wait() before any cross-CTA wait,
+  // and the preceding kernel never waits on them.
+  void (*kernel)(TcParams) =
+      mode == kModeLayer ? gemm_tc_kernel<kN, kModeLayer> : gemm_tc_kernel<kN, kModeBoth>;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = mode == kModeLayer ? tc_smem_bytes<kN, kModeLayer>() : smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeCooperative;
@@ -175,12 +184,12 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
-  if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge) return e;
+  cfg.numAttrs = first ? 1 : 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge || first) return e;
   (void)cudaGetLastError();  // the combination was refused: cooperative only
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemm_tc_kernel<kN, kModeBoth>, prm);
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
 constexpr int kRouterNMax = 256;                        // router tokens per work item
@@ -309,7 +318,7 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
 
 struct Layout {
   size_t topk_idx, topk_w, cnt, off, perm, pos, chunks, done, meta, xq, xs, hq, hs, yp, part,
-      rlogits, total;
+      rlogits, sync, total;
   int max_chunks;
 };
 
@@ -342,6 +351,9 @@ Layout layout_for(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act
   L.yp = take(TK * H * 4);
   L.part = take(routed ? (size_t)router_part_bytes(T, E) : 0);
   L.rlogits = take(routed ? (size_t)(T * E * 4) : 0);
+  // the whole-layer launch's barrier words and its flags per (chunk, GEMM1
+  // tile pair, epilogue warp)
+  L.sync = take(kGridSyncBytes + (size_t)L.max_chunks * (I / 128) * 4 * 8);
   L.total = o;
   return L;
 }
@@ -365,6 +377,7 @@ Work carve(void* base, const Layout& L) {
   w.yp = reinterpret_cast<float*>(b + L.yp);
   w.part = reinterpret_cast<float*>(b + L.part);
   w.rlogits = reinterpret_cast<float*>(b + L.rlogits);
+  w.sync = b + L.sync;
   w.max_chunks = L.max_chunks;
   return w;
 }
@@ -686,6 +699,116 @@ int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, 
   return MOE_OK;
 }
 
+// The MXFP8 GEMMs' parameters: phase 0 = GEMM1 (gate/up rows paired, SwiGLU
+// epilogue into hq/hs), phase 1 = GEMM2 (output rows r and r + 128 paired,
+// fp32 rows into yp)
+int mxfp8_gemm_params(const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                      const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
+                      DeviceState* d, unsigned long long timeout_ns, TcParams& p) {
+  const int TK = T * k;
+  TcPhase& g1 = p.ph[0];
+  TcPhase& g2 = p.ph[1];
+  int rc;
+  if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
+                     H / 2, 128, 128)) ||
+      (rc = make_map(&g1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)) ||
+      (rc = make_map(&g2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
+                     I / 2, 128, 128)) ||
+      (rc = make_map(&g2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
+    return rc;
+  g1.w_sf = w13s;
+  g1.x_sf = w.xs;
+  g1.K = H;
+  g1.R = 2 * I;
+  g1.m_tiles = I / 128;
+  g1.m_stride = 128;
+  g1.half = I;
+  g1.out_dim = I;
+  g1.rows_total = E * 2 * I;
+  g2.w_sf = w2s;
+  g2.x_sf = w.hs;
+  g2.K = I;
+  g2.R = H;
+  g2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
+  g2.m_stride = 256;
+  g2.half = 128;
+  g2.out_dim = H;
+  g2.rows_total = E * H;
+  p.chunks = w.chunks;
+  p.meta = w.meta;
+  p.hq = w.hq;
+  p.hs = w.hs;
+  p.yp = w.yp;
+  p.status = d->status;
+  p.timeout_ns = timeout_ns;
+  return MOE_OK;
+}
+
+std::atomic<uint32_t> g_calls{0};  // host call number: the salt of the grid barriers' tags
+constexpr int kLayerLaunchTooLarge = 1;   // enqueue_layer: the cooperative launch was refused
+
+// The whole layer in one persistent launch (MXFP8 mode): both GEMMs and the
+// combine; with `route_in` (T <= kSmallRouteTokens) also the routing and the
+// activation step, and then it is the call's first kernel.  Without it the
+// routing kernels have run before (w holds their arrays).
+int enqueue_layer(const float* logits, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
+                  const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
+                  bool route_in, bool first, const Work& w, void* y, DeviceState* d,
+                  cudaStream_t stream, unsigned long long timeout_ns, const moe_opts* opts,
+                  Steps& st) {
+  TcParams p{};
+  int rc;
+  if ((rc = mxfp8_gemm_params(w13, w13s, w2, w2s, T, H, I, E, k, w, d, timeout_ns, p))) return rc;
+  p.gemm1_done = w.done;
+  p.ph[1].dep_target = 4 * p.ph[0].m_tiles;  // four epilogue warps publish per tile pair
+  if (opts && (opts->debug_flags & MOE_DEBUG_FORCE_DEP_TIMEOUT))
+    p.ph[1].dep_target = INT_MAX;  // never reached: the dependency wait runs out
+  if (route_in) {
+    LayerRouteParams& r = p.route;
+    r.logits = logits;
+    r.x = x;
+    r.T = T;
+    r.E = E;
+    r.k = k;
+    r.chunk_max = kChunkNarrow;
+    r.max_chunks = w.max_chunks;
+    r.topk_idx = w.topk_idx;
+    r.topk_w = w.topk_w;
+    r.cnt = w.cnt;
+    r.off = w.off;
+    r.perm = w.perm;
+    r.pos = w.pos;
+    r.chunks = w.chunks;
+    r.meta = w.meta;
+    r.xq = w.xq;
+    r.xs = w.xs;
+  }
+  p.sync.counter = reinterpret_cast<uint32_t*>(w.sync);
+  p.sync.abort = reinterpret_cast<uint64_t*>(w.sync + 8);
+  p.sync.flags = reinterpret_cast<uint64_t*>(w.sync + 16);
+  p.sync.chunk_flags = reinterpret_cast<uint64_t*>(w.sync + kGridSyncBytes);
+  p.sync.salt = g_calls.fetch_add(1, std::memory_order_relaxed) + 1;
+  p.pos = w.pos;
+  p.gate = w.topk_w;
+  p.y = static_cast<uint16_t*>(y);
+  p.T = T;
+  p.H = H;
+  p.k = k;
+  if (d->sms > kMaxGridSync) return MOE_ERR_UNSUPPORTED_SHAPE;
+  const bool wide = T >= kWideMinTokens;
+  st.mark();
+  const cudaError_t e = wide ? launch_gemm<kChunkWide>(kModeLayer, d->sms, stream, p, first)
+                             : launch_gemm<kChunkNarrow>(kModeLayer, d->sms, stream, p, first);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    // the GPU cannot hold every CTA at once (e.g. a partitioned device):
+    // nothing ran, the caller takes the multi-launch path
+    return e == cudaErrorCooperativeLaunchTooLarge ? kLayerLaunchTooLarge : MOE_ERR_CUDA;
+  }
+  st.launched();
+  return launch_status();
+}
+
 // steps a5-a7: the two grouped GEMMs (one persistent launch or two)
 // `next` (a chained layer, MXFP8 mode): the last GEMM launch prefetches the
 // next layer's first GEMM1 weight tiles into L2
@@ -698,40 +821,9 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
   const bool bf_wide = chunk_for(act, T) == kChunkBf16Wide;
   int rc = MOE_OK;
   if (act == MOE_ACT_MXFP8) {
-    TcPhase g1{}, g2{};
-    if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
-                       H / 2, 128, 128)) ||
-        (rc = make_map(&g1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)) ||
-        (rc = make_map(&g2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
-                       I / 2, 128, 128)) ||
-        (rc = make_map(&g2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
-      return rc;
-    g1.w_sf = w13s;
-    g1.x_sf = w.xs;
-    g1.K = H;
-    g1.R = 2 * I;
-    g1.m_tiles = I / 128;
-    g1.m_stride = 128;
-    g1.half = I;
-    g1.out_dim = I;
-    g1.rows_total = E * 2 * I;
-    g2.w_sf = w2s;
-    g2.x_sf = w.hs;
-    g2.K = I;
-    g2.R = H;
-    g2.m_tiles = (H + 255) / 256;  // an odd last tile pairs with rows past the expert
-    g2.m_stride = 256;
-    g2.half = 128;
-    g2.out_dim = H;
-    g2.rows_total = E * H;
     TcParams p{};
-    p.chunks = w.chunks;
-    p.meta = w.meta;
-    p.hq = w.hq;
-    p.hs = w.hs;
-    p.yp = w.yp;
-    p.status = d->status;
-    p.timeout_ns = timeout_ns;
+    if ((rc = mxfp8_gemm_params(w13, w13s, w2, w2s, T, H, I, E, k, w, d, timeout_ns, p))) return rc;
+    TcPhase g1 = p.ph[0], g2 = p.ph[1];
     auto launch = [&](int mode, const TcParams& prm) {
       const cudaError_t e = wide ? launch_gemm<kChunkWide>(mode, d->sms, stream, prm)
                                  : launch_gemm<kChunkNarrow>(mode, d->sms, stream, prm);
@@ -874,15 +966,40 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   // wide token chunks cut the MMA instructions per token when experts get
   // many tokens (large T); narrow chunks keep the weight pipeline deepest
   const int chunk = chunk_for(act, T);
-  if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
+  const bool split = opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING);
+  const bool persistent =
+      act == MOE_ACT_MXFP8 &&
+      (path == MOE_PATH_PERSISTENT ||
+       (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_PERSISTENT));
+  // the whole layer in one launch: for T <= 32 also the routing (steps a1-a4)
+  const bool route_in = persistent && T <= kSmallRouteTokens && !split;
+  if (route_in) {
+    rc = enqueue_layer(lg, x, w13, w13s, w2, w2s, T, H, I, E, k, true, !routed, w, y, d, stream,
+                       timeout_ns, opts, st);
+    if (rc != kLayerLaunchTooLarge) {
+      if (rc) return rc;
+      st.mark();
+      return launch_status();
+    }
+  }
+  if (T <= kSmallRouteTokens && !split) {
     if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
       return rc;
   } else if ((rc = enqueue_route(lg, !routed, T, E, k, chunk, w, d, stream, st)) ||
              (rc = enqueue_act(act, x, w, T, H, k, d, stream, st))) {
     return rc;
   }
-  if ((rc = enqueue_gemms(act, path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream, timeout_ns,
-                          opts, st)))
+  if (persistent && !route_in) {
+    rc = enqueue_layer(lg, x, w13, w13s, w2, w2s, T, H, I, E, k, false, false, w, y, d, stream,
+                       timeout_ns, opts, st);
+    if (rc != kLayerLaunchTooLarge) {
+      if (rc) return rc;
+      st.mark();
+      return launch_status();
+    }
+  }
+  if ((rc = enqueue_gemms(act, persistent ? MOE_PATH_MULTI : path, w13, w13s, w2, w2s, T, H, I,
+                          E, k, w, d, stream, timeout_ns, opts, st)))
     return rc;
   const int cap = d->sms * 8;
   st.mark();

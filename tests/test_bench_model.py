@@ -33,6 +33,6 @@ def test_step_names_follow_the_launch_sequence():
     assert bench.step_names(1, 256) == ["route_topk", "route_permute", "act_quant", "gemm1",
                                         "gemm2", "combine"]
     assert bench.step_names(2, 256) == ["route_topk", "route_permute", "act_quant",
-                                        "gemm1+gemm2", "combine"]
+                                        "gemm1+gemm2+combine"]
     assert bench.step_names(1, 8) == ["route_act", "gemm1", "gemm2", "combine"]
-    assert bench.step_names(2, 32) == ["route_act", "gemm1+gemm2", "combine"]
+    assert bench.step_names(2, 32) == ["layer"]          # the whole layer in one launch

@@ -78,7 +78,12 @@ __device__ __forceinline__ int mxfp8_block(const float* v, uint8_t* out) {
   int code = block_scale_code(amax, 8);
   float inv = exp2_exact(127 - code);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) out[i] = e4m3_encode_satfinite(v[i] * inv);
+  for (int i = 0; i < 32; i += 2) {  // two values per conversion instruction
+    const __nv_fp8x2_storage_t pr =
+        __nv_cvt_float2_to_fp8x2(make_float2(v[i] * inv, v[i + 1] * inv), __NV_SATFINITE, __NV_E4M3);
+    out[i] = (uint8_t)(pr & 0xFFu);
+    out[i + 1] = (uint8_t)(pr >> 8);
+  }
   return code;
 }
 

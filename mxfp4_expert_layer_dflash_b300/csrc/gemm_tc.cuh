@@ -268,7 +268,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // (GEMM2 reads GEMM1's h; with routing inside, GEMM1 reads the act1 rows
   // that every CTA writes)?
   auto gated_phase = [](int phase) { return kMode == kModeGemm1 || (kPhases == 2 && phase == 0); };
-  auto dep_phase = [&](int phase) { return kPhases == 2 && (phase == 1 || route_in); };
+  auto dep_phase = [&](int phase) { return kPhases == 2 && phase == 1; };
+  // are this phase's activation scales written during the launch (so they
+  // need coherent loads)?  GEMM2's h; GEMM1's act1 rows when the launch routes
+  auto coherent_x = [&](int phase) { return dep_phase(phase) || route_in; };
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem =
       reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -283,8 +286,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // seen published (items of a CTA only increase); the scale stagers read it
   // instead of polling the global counters themselves
   int* dep_ready = reinterpret_cast<int*>(tmem_slot + 2);
-  // whole-layer launch that routes: this CTA's act1 rows are written
-  int* act_ready = reinterpret_cast<int*>(tmem_slot + 3);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -299,7 +300,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     ptx::mbar_init(drain, 1);
     *abort_flag = 0;
     *dep_ready = -1;
-    *act_ready = 0;
     ptx::fence_mbar_init();
   }
   if (warp == 2) {
@@ -325,6 +325,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // buffers serve as scratch before the first copy lands in them)
   LayerRouteState* rs =
       reinterpret_cast<LayerRouteState*>(smem + C::kStages * C::kStageBytes + C::kBarBytes);
+  // step a4 reads token rows of x soon, while every CTA's first weight tiles
+  // flood the memory system: CTA t brings row t into L2 now
+  if (route_in && warp == 1 && lane == 0 && (int)blockIdx.x < p.route.T)
+    ptx::bulk_prefetch_l2(p.route.x + (int64_t)blockIdx.x * p.ph[0].K,
+                          (uint32_t)p.ph[0].K * 2u);
   const uint64_t tag = kLayer ? grid_sync_tag(p.sync) : 0;
   // the value a published (chunk, GEMM1 tile pair) flag holds in this call
   // (a kind never written when the debug flag forces the wait to run out)
@@ -345,6 +350,91 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     *abort_flag = 1;
     if (kLayer) grid_give_up(p.sync, tag);
   };
+
+  // With the routing inside the launch: the producer first issues the weight
+  // tiles of its first fills (each stage's barrier expects both operands'
+  // bytes; the activation tiles follow once they exist), then every warp of
+  // the CTA runs step a4 for the chunks of the CTA's GEMM1 items — a warp per
+  // (slot row, run of 32 blocks of 32), two units' loads in flight — while
+  // those tiles stream in.  Other CTAs multiplying the same chunk write the
+  // same bytes, so only this CTA's own writes must precede its copies.
+  uint32_t prefilled = 0;  // (producer) fills whose weight tiles are in flight
+  if (route_in) {
+    if (warp == 0) {
+      const uint64_t pol_w0 = ptx::policy_evict_first();
+      int it = blockIdx.x, ks = 0;
+      while (prefilled < (uint32_t)C::kStages && it < items_all) {
+        const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
+        const TcPhase& ph = p.ph[phase];
+        const int local = it - (phase ? items0 : 0);
+        const int chunk = local / ph.m_tiles;
+        const int4 ch = chunk_at(chunk);
+        const int row0 = ch.x * ph.R + (local - chunk * ph.m_tiles) * ph.m_stride;
+        const uint32_t tx = C::kA * C::kTxA + (uint32_t)((ch.z + 15) & ~15) * 128;
+        uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
+        ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
+        ptx::tma_load_2d_warp(st, &ph.map_w, &full[prefilled], ks * kBlockK, row0, pol_w0);
+        ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[prefilled], ks * kBlockK,
+                              row0 + ph.half, pol_w0);
+        ++prefilled;
+        if (++ks == ph.K / kBlockK) {
+          ks = 0;
+          it += gridDim.x;
+        }
+      }
+    }
+    const int64_t H = p.ph[0].K;
+    const int segs = (int)((H / 32 + 31) / 32);
+    constexpr int kWarps = kTcThreads / 32;
+    int held_t = -1, held_slot = 0, held_sg = 0;
+    uint4 held[4];
+    auto load_unit = [&](int t, int sg, uint4 (&raw)[4]) {
+      const int64_t b = (int64_t)sg * 32 + lane;
+      if (b < H / 32) {
+        const uint4* src = reinterpret_cast<const uint4*>(p.route.x + (int64_t)t * H + b * 32);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) raw[i] = src[i];
+      }
+    };
+    auto finish_unit = [&](int slot, int sg, const uint4 (&raw)[4]) {
+      const int64_t b = (int64_t)sg * 32 + lane;
+      if (b >= H / 32) return;
+      float v[32];
+      uint8_t c[32];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t wd[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[8 * i + 2 * j] = __uint_as_float(wd[j] << 16);
+          v[8 * i + 2 * j + 1] = __uint_as_float(wd[j] & 0xFFFF0000u);
+        }
+      }
+      const int code = mxfp8_block(v, c);
+      store_u8x32(p.route.xq + (int64_t)slot * H + b * 32, c);
+      p.route.xs[(int64_t)slot * (H / 32) + b] = (uint8_t)code;
+    };
+    int u = 0;  // unit counter over this CTA's rows, dealt round-robin to the warps
+    for (int item = blockIdx.x; item < items0; item += gridDim.x) {
+      const int4 ch = chunk_at(item / p.ph[0].m_tiles);
+      for (int r = 0; r < ch.z; ++r) {
+        for (int sg = 0; sg < segs; ++sg, ++u) {
+          if (u % kWarps != warp) continue;
+          uint4 raw[4];
+          load_unit(rs->perm[ch.y + r], sg, raw);
+          if (held_t >= 0) finish_unit(held_slot, held_sg, held);
+          held_t = 1;
+          held_slot = ch.y + r;
+          held_sg = sg;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) held[i] = raw[i];
+        }
+      }
+    }
+    if (held_t >= 0) finish_unit(held_slot, held_sg, held);
+    fence_proxy_async_global();  // generic writes before this CTA's TMA reads them
+    __syncthreads();
+  }
   auto deadline = [&]() { return ptx::globaltimer() + p.timeout_ns; };
 
   // Bounded wait whose outcome is the same in every lane of the warp: lanes can
@@ -358,26 +448,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // warps; 192 threads, named barriers 1-3), around the GEMM items
   constexpr int kAuxWarps = 6, kAuxThreads = kAuxWarps * 32;
   const int aux_w = warp == 1 ? 0 : warp == 3 ? 1 : warp - 6;  // valid for aux warps
-  // step a4 (routing inside the launch): the slot rows of the chunks of this
-  // CTA's GEMM1 items, a warp per (slot row, run of 32 blocks of 32); other
-  // CTAs multiplying the same chunk write the same bytes.  Then the rows are
-  // handed to this CTA's producer (its TMA reads them).
-  auto aux_act1 = [&]() {
-    const int64_t H = p.ph[0].K;
-    const int segs = (int)((H / 32 + 31) / 32);
-    int u = 0;  // unit counter over this CTA's rows, dealt round-robin to the aux warps
-    for (int item = blockIdx.x; item < items0; item += gridDim.x) {
-      const int4 ch = chunk_at(item / p.ph[0].m_tiles);
-      for (int r = 0; r < ch.z; ++r)
-        for (int sg = 0; sg < segs; ++sg, ++u)
-          if (u % kAuxWarps == aux_w)
-            layer_act1_unit(p.route.x, rs->perm[ch.y + r], ch.y + r, sg, H, p.route.xq,
-                            p.route.xs);
-    }
-    fence_proxy_async_global();  // generic writes before this CTA's TMA reads them
-    named_barrier_sync(1, kAuxThreads);
-    if (aux_w == 0 && lane == 0) st_release_cta(act_ready, 1);
-  };
   // step a8 once every CTA's GEMM2 outputs are written: the gate-weighted sum
   // of each token's k slot rows in slot order, the combine kernel's arithmetic
   auto aux_combine = [&]() {
@@ -412,33 +482,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
     uint32_t fill = 0;
     bool ok = true;
-    bool act_seen = !route_in;  // every CTA's act1 rows written (routing inside the launch)
-    // With the routing inside the launch, the weight tiles of the first fills
-    // do not wait for the act1 barrier: they are issued at once (each stage's
-    // barrier expects both operands' bytes; the activation tiles follow once
-    // the barrier is passed), so the barrier's latency hides behind them.
-    uint32_t prefilled = 0;
-    if (route_in) {
-      int it = blockIdx.x, ks = 0;
-      while (prefilled < (uint32_t)C::kStages && it < items_all) {
-        const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
-        const TcPhase& ph = p.ph[phase];
-        const int local = it - (phase ? items0 : 0);
-        const int chunk = local / ph.m_tiles;
-        const int row0 = chunk_at(chunk).x * ph.R + (local - chunk * ph.m_tiles) * ph.m_stride;
-        const uint32_t tx = C::kA * C::kTxA + (uint32_t)((chunk_at(chunk).z + 15) & ~15) * 128;
-        uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
-        ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
-        ptx::tma_load_2d_warp(st, &ph.map_w, &full[prefilled], ks * kBlockK, row0, pol_w);
-        ptx::tma_load_2d_warp(st + C::kATile, &ph.map_w, &full[prefilled], ks * kBlockK,
-                              row0 + ph.half, pol_w);
-        ++prefilled;
-        if (++ks == ph.K / kBlockK) {
-          ks = 0;
-          it += gridDim.x;
-        }
-      }
-    }
     for (int item = blockIdx.x; ok && item < items_all; item += gridDim.x) {
       const int phase = (kPhases > 1 && item >= items0) ? 1 : 0;
       const TcPhase& ph = p.ph[phase];
@@ -446,31 +489,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       const int chunk = local / ph.m_tiles;
       const int mt = local - chunk * ph.m_tiles;
       const int4 ch = chunk_at(chunk);
-      // With the routing inside the launch, a GEMM1 item's activation tiles
-      // are this CTA's own act1 rows: wait (bounded) until its aux warps have
-      // written them.
-      if (!act_seen && phase == 0) {
-        const uint64_t until = deadline();
-        bool ready = true;
-        while (ld_acquire_cta(act_ready) == 0) {
-          if (*abort_flag || ptx::globaltimer() > until) {
-            ready = false;
-            break;
-          }
-        }
-        if (!__all_sync(0xffffffffu, ready)) {
-          if (lane == 0) fail(kStatusTimeout);
-          break;
-        }
-        act_seen = true;
-        fence_proxy_async_global();
-      }
       // h of this chunk must be published by GEMM1 (unless the look-ahead of
-      // the previous item already saw it complete); a GEMM1 item whose act1
-      // rows come from this launch is ready once the wait above is passed
+      // the previous item already saw it complete)
       if (dep_phase(phase) && ld_acquire_cta(dep_ready) < item) {
         bool ready = true;
-        if (phase == 1) {
+        {
           if (kLayer) {  // every GEMM1 tile pair of the chunk has set its flag
             const uint64_t until = deadline();
             uint32_t spins = 0;
@@ -493,7 +516,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           if (lane == 0) fail(kStatusTimeout);
           break;
         }
-        if (phase == 1) fence_proxy_async_global();
+        fence_proxy_async_global();
         if (lane == 0) st_release_cta(dep_ready, item);
       }
       // Look-ahead (single-launch path): read the next item's chunk counter now
@@ -501,8 +524,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
       // this item's copies; if the chunk is complete, publish the next item
       // early so the scale stagers can load its h scales ahead of time.
       const int nxt = item + (int)gridDim.x;
-      // the next item is a GEMM1 item of a launch that routes: ready already
-      if (route_in && nxt < items0 && lane == 0) st_release_cta(dep_ready, nxt);
       bool look = kPhases > 1 && nxt < items_all && nxt >= items0;
       int look_cnt = 0;
       bool look_flags = true;  // (whole-layer launch) this lane's flags of the next chunk
@@ -654,7 +675,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
           const unsigned int* src = reinterpret_cast<const unsigned int*>(
               ph.x_sf + (int64_t)(c.ch.y + n) * sf_row + c.ks * 4);
           // h scales written earlier in this launch need a coherent load
-          w[C::kA + jb] = dep_phase(c.phase) ? __ldcg(src) : __ldg(src);
+          w[C::kA + jb] = coherent_x(c.phase) ? __ldcg(src) : __ldg(src);
         }
       }
     };
@@ -680,7 +701,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
         if (n < c0.ch.z) {
           const uint4* src = reinterpret_cast<const uint4*>(
               ph.x_sf + (int64_t)(c0.ch.y + n) * sf_row + c0.ks * 4);
-          const uint4 v = dep_phase(c0.phase) ? __ldcg(src) : __ldg(src);
+          const uint4 v = coherent_x(c0.phase) ? __ldcg(src) : __ldg(src);
           g[0][C::kA + jb] = v.x;
           g[1][C::kA + jb] = v.y;
           g[2][C::kA + jb] = v.z;
@@ -795,7 +816,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     }
   } else if (warp >= 8) {
     // ------------------------------------------------------------ epilogue
-    if (route_in) aux_act1();
     const int q = warp & 3;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     Cursor c;
@@ -880,7 +900,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
     if (kLayer) aux_combine();
   } else if (kLayer && (warp == 1 || warp == 3)) {
     // ------------------------------------------------------------ aux (whole-layer launch)
-    if (route_in) aux_act1();
     aux_combine();
   }
 

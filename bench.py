@@ -46,8 +46,10 @@ KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f
                   for f in ("common.cuh", "fmt.cuh", "gemm_tc.cuh", "ptx.cuh")]
 # kernels of one forward in launch order, per execution path
 STEP_NAMES = {1: ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"],
-              2: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2+combine"]}
-PATHS = {"auto": 0, "multi": 1, "persistent": 2}
+              2: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2+combine"],
+              3: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2", "combine"]}
+PATHS = {"auto": 0, "multi": 1, "persistent": 2, "gemms": 3}
+PATH_NAMES = {1: "multi", 2: "persistent", 3: "gemms"}
 SMALL_ROUTE_TOKENS = 32  # up to this T the first three steps are one kernel, route_act
 
 
@@ -127,28 +129,33 @@ class ClockSampler:
         self.window = None
         self.source = None
 
-    def _handle(self):
-        import pynvml
+    def _nvml(self):
+        """NVML through the driver's own library (ctypes; read-only queries), and a handle for
+        this process's CUDA device (matched by UUID, else by index)."""
         import torch
-        pynvml.nvmlInit()
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
         uuid = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
         for u in (uuid, "GPU-" + uuid):
-            try:
-                return pynvml.nvmlDeviceGetHandleByUUID(u)
-            except Exception:  # noqa: BLE001 - try the other spelling, then the index
-                pass
-        return pynvml.nvmlDeviceGetHandleByIndex(self.cuda_index)
+            if nv.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0:
+                return nv, h
+        if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle")
+        return nv, h
 
-    def _run_nvml(self, h):
-        import pynvml
-        mx = float(pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM))
+    def _run_nvml(self, nv, h):
+        sm_clock = ctypes.c_uint(1)  # NVML_CLOCK_SM
+        mx, sm, rs = ctypes.c_uint(0), ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        nv.nvmlDeviceGetMaxClockInfo(h, sm_clock, ctypes.byref(mx))
+        reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
         while not self._stop.is_set():
-            try:
-                sm = float(pynvml.nvmlDeviceGetClockInfo(h, pynvml.NVML_CLOCK_SM))
-                rs = int(pynvml.nvmlDeviceGetCurrentClocksEventReasons(h))
-                self.samples.append((time.perf_counter(), sm, mx, rs))
-            except Exception:  # noqa: BLE001 - a failed read is skipped
-                pass
+            if nv.nvmlDeviceGetClockInfo(h, sm_clock, ctypes.byref(sm)) == 0 and \
+                    reasons(h, ctypes.byref(rs)) == 0:
+                self.samples.append((time.perf_counter(), float(sm.value), float(mx.value),
+                                     int(rs.value)))
             self._stop.wait(self.period)
 
     def __enter__(self):
@@ -156,8 +163,8 @@ class ClockSampler:
         self._stop = threading.Event()
         self.proc = None
         try:
-            h = self._handle()
-            self.thread = threading.Thread(target=self._run_nvml, args=(h,), daemon=True)
+            nv, h = self._nvml()
+            self.thread = threading.Thread(target=self._run_nvml, args=(nv, h), daemon=True)
             self.thread.start()
             self.source = f"NVML every {self.period * 1e3:.0f} ms"
         except Exception:  # noqa: BLE001 - no NVML: nvidia-smi at its fastest period
@@ -383,7 +390,7 @@ def measure_config(L, steps, flush_buf):
     del w
     torch.cuda.empty_cache()
     return {"layer": L.desc, "touched_experts": touched, "alg_bytes": b_layer,
-            "path": {1: "multi", 2: "persistent"}[moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E,
+            "path": PATH_NAMES[moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E,
                                                                              L.k)],
             "us_hot": hot_us, "us_cold_l2_flushed": cold_us, "issued_as": how,
             "tokens_per_s_cold": L.T / (cold_us * 1e-6),
@@ -748,8 +755,8 @@ def run_ours(args, L, rank, world, local_rank):
 
     pk, pk_src = peaks()
     hbm = float(pk["hbm_gbs"])
-    gemm_bytes = {"gemm1": b_gemm1, "gemm2": b_gemm2, "gemm1+gemm2+combine": b_gemm1 + b_gemm2,
-                  "layer": b_layer}
+    gemm_bytes = {"gemm1": b_gemm1, "gemm2": b_gemm2, "gemm1+gemm2": b_gemm1 + b_gemm2,
+                  "gemm1+gemm2+combine": b_gemm1 + b_gemm2, "layer": b_layer}
     dominant = max((n for n in names if n in gemm_bytes), key=lambda n: step_ms[n])
     dom_bytes = gemm_bytes[dominant]
     achieved = dom_bytes / (step_ms[dominant] * 1e-3) / 1e9
@@ -767,7 +774,7 @@ def run_ours(args, L, rank, world, local_rank):
                    "seq_len": 8, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (packed weights %.2f GB)" % (b_layer / 1e9),
                    "touched_experts": touched, "act_mode": args.act,
-                   "path": {1: "multi", 2: "persistent"}[path]},
+                   "path": PATH_NAMES[path]},
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": achieved, "peak": hbm,
                      "unit": "GB/s", "frac": achieved / hbm, "traffic": traffic,
                      "peak_source": f"{pk_src} hbm_gbs", "algorithmic_bytes": dom_bytes},

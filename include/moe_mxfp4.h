@@ -67,9 +67,13 @@ typedef enum {
 #define MOE_ACT_BF16 1   /* x used as bf16, h rounded to bf16 */
 
 /* execution paths of moe_opts.path (the bf16 mode always runs the multi path) */
-#define MOE_PATH_AUTO 0       /* moe_mxfp4_select_path decides */
+#define MOE_PATH_AUTO 0       /* moe_mxfp4_select_path decides (MULTI or GEMMS) */
 #define MOE_PATH_MULTI 1      /* routing kernels, GEMM1, GEMM2, combine */
-#define MOE_PATH_PERSISTENT 2 /* routing kernels, one kernel for both GEMMs, combine */
+#define MOE_PATH_PERSISTENT 2 /* the whole layer in one launch for T <= 32 (routing,
+                                 activation step, both GEMMs, combine; for the routed
+                                 layer the router too); above that the routing kernels,
+                                 then one launch for both GEMMs and the combine */
+#define MOE_PATH_GEMMS 3      /* routing kernels, one launch for both GEMMs, combine */
 
 /*
  * moe_mxfp4_forward — the MoE expert layer.
@@ -125,11 +129,13 @@ typedef struct {
   /* optional step markers: caller-created events; the library records
    * step_events[i] on `stream` just before the i-th kernel of the call and one
    * more after the last (i < n_step_events).  Kernel order: multi path —
-   * route_topk, route_permute, act_quant, gemm1, gemm2, combine; persistent
-   * path — route_topk, route_permute, act_quant, gemm1+gemm2, combine.  For
-   * T <= 32 the first three are one kernel, route_act (unless
-   * MOE_DEBUG_SPLIT_ROUTING).  moe_mxfp4_forward_routed puts router_gemm,
-   * router_reduce first. */
+   * route_topk, route_permute, act_quant, gemm1, gemm2, combine (for
+   * T <= 32 the first three are one kernel, route_act, unless
+   * MOE_DEBUG_SPLIT_ROUTING); persistent path — for T <= 32 one kernel, the
+   * whole layer (with the router too for moe_mxfp4_forward_routed), else
+   * route_topk, route_permute, act_quant, gemm1+gemm2+combine.
+   * moe_mxfp4_forward_routed otherwise puts router_gemm, router_reduce
+   * first. */
   cudaEvent_t* step_events;
   int n_step_events;
 } moe_opts;
@@ -137,8 +143,9 @@ typedef struct {
 /* debug_flags: cap every bounded device wait at ~1 ms instead of ~2 s; used
  * to exercise the timeout path without faulting anything */
 #define MOE_DEBUG_SHORT_TIMEOUT 1u
-/* debug_flags: on the single-launch path (MOE_PATH_PERSISTENT, MXFP8 mode),
- * make GEMM2 wait for a GEMM1 completion count that is never reached, so the
+/* debug_flags: on the paths that run both GEMMs in one launch
+ * (MOE_PATH_PERSISTENT, MOE_PATH_GEMMS; MXFP8 mode), make GEMM2 wait for a
+ * GEMM1 publication that never comes, so the
  * cross-CTA dependency wait runs out (after ~1 ms with MOE_DEBUG_SHORT_TIMEOUT):
  * the call then reports MOE_ERR_DEVICE_TIMEOUT through moe_mxfp4_get_status and
  * y is unspecified.  Exercises the device timeout path without any fault;
@@ -214,14 +221,17 @@ size_t moe_mxfp4_workspace_size_chain(int n_layers, int T, int H, int I, int E, 
 
 /*
  * moe_mxfp4_select_path — the path MOE_PATH_AUTO takes for this shape on the
- * current device: MOE_PATH_PERSISTENT when a bound on the GEMM work items
+ * current device: MOE_PATH_GEMMS when a bound on the GEMM work items
  * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is between 5 and 8 per
- * SM, else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  The
- * single launch saves the gap and tail between the GEMMs on layers with a
+ * SM, else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  One
+ * launch for both GEMMs saves the gap and tail between them on layers with a
  * handful of work items per SM; two launches stream weights faster on large
- * layers and start sooner on tiny ones.  The paths give bitwise equal
- * results.  Returns a negative moe_status on invalid arguments.  No
- * counterpart in the papers: a support call.
+ * layers and start sooner on tiny ones.  The automatic choice never takes
+ * MOE_PATH_PERSISTENT: on this part its serial start (routing and the
+ * activation step inside the launch) costs more than the launches it saves,
+ * which overlap one another.  Every path gives bitwise equal results.
+ * Returns a negative moe_status on invalid arguments.  No counterpart in the
+ * papers: a support call.
  */
 int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode);
 
@@ -248,6 +258,9 @@ size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode)
  *  hq [T*k, I], hs [T*k, I/32]                    act2(h) in slot order, same
  *                                                 forms
  *  yp [T*k, H] fp32                               W2 act2(h) per slot
+ *  logits [T, E] fp32                             the router's logits (the
+ *                                                 routed layer's layout only;
+ *                                                 SIZE_MAX otherwise)
  *  x_stream[2] [T, H] bf16                        SIZE_MAX here (chain only)
  *  total                                          moe_mxfp4_workspace_size
  * The layout depends only on the arguments.  Returns MOE_OK or an error for
@@ -257,11 +270,17 @@ size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode)
 typedef struct {
   size_t topk_idx, topk_w, cnt, off, perm, pos;
   size_t xq, xs, hq, hs, yp;
+  size_t logits;
   size_t x_stream[2];
   size_t total;
 } moe_workspace_layout;
 int moe_mxfp4_workspace_layout(int T, int H, int I, int E, int k, int act_mode,
                                moe_workspace_layout* out);
+
+/* the same for a workspace of moe_mxfp4_forward_routed (total =
+ * moe_mxfp4_workspace_size_routed); logits holds the router's logits */
+int moe_mxfp4_workspace_layout_routed(int T, int H, int I, int E, int k, int act_mode,
+                                      moe_workspace_layout* out);
 
 /*
  * moe_mxfp4_workspace_layout_chain — the same for layer `layer` (0 <= layer <
@@ -381,7 +400,12 @@ int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H,
  * front: router weights instead of router logits (see moe_router_topk); the
  * logits never leave the call.  opts as moe_mxfp4_forward_ex (NULL =
  * defaults); a caller workspace must hold moe_mxfp4_workspace_size_routed
- * bytes.
+ * bytes.  On the single-launch path (MXFP8 mode) with T <= 32 the router
+ * runs inside the layer's one launch: each warp multiplies one expert's
+ * weight row with every token row (exact bf16 products, fp32 sums in a fixed
+ * order), one grid-wide barrier, then the routing; otherwise it is a
+ * tensor-core GEMM in front (moe_router_topk's arithmetic).  Both orders stay
+ * within the same error bound of the exact logits; each is deterministic.
  */
 int moe_mxfp4_forward_routed(const void* x_bf16, const void* w_router_bf16,
                              const uint8_t* w13_fp4, const uint8_t* w13_e8m0,

@@ -17,7 +17,7 @@ LIB_PATH = os.environ.get("MOE_MXFP4_LIB") or os.path.join(_HERE, "libmoe_mxfp4.
 
 MOE_OK = 0
 MOE_ACT_MXFP8, MOE_ACT_BF16 = 0, 1
-MOE_PATH_AUTO, MOE_PATH_MULTI, MOE_PATH_PERSISTENT = 0, 1, 2
+MOE_PATH_AUTO, MOE_PATH_MULTI, MOE_PATH_PERSISTENT, MOE_PATH_GEMMS = 0, 1, 2, 3
 MOE_DEBUG_SHORT_TIMEOUT = 1
 MOE_DEBUG_FORCE_DEP_TIMEOUT = 2
 MOE_DEBUG_SPLIT_ROUTING = 4
@@ -49,7 +49,8 @@ class moe_workspace_layout(ctypes.Structure):
     """Byte offsets of a forward's intermediate arrays inside a caller workspace."""
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("topk_idx", "topk_w", "cnt", "off", "perm", "pos", "xq", "xs", "hq", "hs",
-                 "yp")] + [("x_stream", ctypes.c_size_t * 2), ("total", ctypes.c_size_t)]
+                 "yp", "logits")] + [("x_stream", ctypes.c_size_t * 2),
+                                     ("total", ctypes.c_size_t)]
 
 
 _lib = None
@@ -107,6 +108,9 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_workspace_layout.argtypes = [i, i, i, i, i, i,
                                                  ctypes.POINTER(moe_workspace_layout)]
         L.moe_mxfp4_workspace_layout.restype = i
+        L.moe_mxfp4_workspace_layout_routed.argtypes = [i, i, i, i, i, i,
+                                                        ctypes.POINTER(moe_workspace_layout)]
+        L.moe_mxfp4_workspace_layout_routed.restype = i
         L.moe_mxfp4_workspace_layout_chain.argtypes = [i, i, i, i, i, i, i, i,
                                                        ctypes.POINTER(moe_workspace_layout)]
         L.moe_mxfp4_workspace_layout_chain.restype = i
@@ -243,7 +247,7 @@ def moe_verify_block(p, q, draft, u, U, S, g, V, n_acc, tokens, stream=None):
 
 def moe_mxfp4_select_path(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
     """The path MOE_PATH_AUTO takes on the current device (MOE_PATH_MULTI or
-    MOE_PATH_PERSISTENT)."""
+    MOE_PATH_GEMMS)."""
     rc = int(lib().moe_mxfp4_select_path(T, H, I, E, k, act_mode))
     if rc < 0:
         raise MoeError(rc, "moe_mxfp4_select_path")
@@ -284,6 +288,13 @@ def moe_mxfp4_workspace_layout(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> moe_wor
     out = moe_workspace_layout()
     _check(lib().moe_mxfp4_workspace_layout(T, H, I, E, k, act_mode, ctypes.byref(out)),
            "moe_mxfp4_workspace_layout")
+    return out
+
+
+def moe_mxfp4_workspace_layout_routed(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> moe_workspace_layout:
+    out = moe_workspace_layout()
+    _check(lib().moe_mxfp4_workspace_layout_routed(T, H, I, E, k, act_mode, ctypes.byref(out)),
+           "moe_mxfp4_workspace_layout_routed")
     return out
 
 

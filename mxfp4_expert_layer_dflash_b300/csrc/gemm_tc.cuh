@@ -335,6 +335,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) gemm_tc_kernel(const __grid_con
   // (a kind never written when the debug flag forces the wait to run out)
   const uint64_t flag_want =
       tag | (p.ph[1].dep_target == INT_MAX ? kChunkFlagNever : kChunkFlagKind);
+  if (route_in && p.route.w_router) {
+    // the router in front: this CTA computes its experts' logits for the
+    // block (the stage buffers as scratch), then every CTA waits for every
+    // expert's (one barrier)
+    layer_router_logits(p.route, p.ph[0].K, const_cast<float*>(p.route.logits),
+                        reinterpret_cast<float*>(smem));
+    if (threadIdx.x == 0) grid_arrive(p.sync, kSyncLogits, tag);
+    if (warp == 0 && !grid_wait(p.sync, kSyncLogits, tag, p.timeout_ns, abort_flag) && lane == 0) {
+      set_status(p.status, kStatusTimeout);
+      *abort_flag = 1;
+      grid_give_up(p.sync, tag);
+    }
+    __syncthreads();
+  }
   if (route_in) {
     layer_route_block(p.route, smem, rs, blockIdx.x == 0, p.status);
     ptx::fence_proxy_async_smem();  // generic scratch writes before TMA writes the stages

@@ -24,7 +24,8 @@ namespace moe {
 
 constexpr int kMaxGridSync = 256;  // most CTAs a synchronised launch may have
 constexpr int kSyncOut = 0;        // barrier: every CTA's GEMM2 outputs are written
-constexpr int kSyncKinds = 1;
+constexpr int kSyncLogits = 1;     // barrier: every CTA's router logits are written
+constexpr int kSyncKinds = 2;
 constexpr uint64_t kChunkFlagKind = 2;      // a (chunk, GEMM1 tile pair) published
 constexpr uint64_t kChunkFlagNever = 0xFE;  // a kind no flag ever holds (forced timeout)
 // bytes of scratch before the per-chunk flags: the counter (8), the abort word

@@ -441,6 +441,7 @@ moe_workspace_layout public_layout(const Layout& L, size_t route_shift, size_t a
   o.hq = act_shift + L.hq;
   o.hs = act_shift + L.hs;
   o.yp = act_shift + L.yp;
+  o.logits = L.rlogits < L.sync ? act_shift + L.rlogits : SIZE_MAX;  // routed layouts only
   o.x_stream[0] = o.x_stream[1] = SIZE_MAX;
   return o;
 }
@@ -677,7 +678,7 @@ int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
   const int64_t item_bound = chunk_bound * (I / 128 + (H + 255) / 256);
   return item_bound >= (int64_t)kPersistentMinItemsPerSm * sms &&
                  item_bound <= (int64_t)kPersistentItemsPerSm * sms
-             ? MOE_PATH_PERSISTENT
+             ? MOE_PATH_GEMMS
              : MOE_PATH_MULTI;
 }
 
@@ -749,13 +750,14 @@ constexpr int kLayerLaunchTooLarge = 1;   // enqueue_layer: the cooperative laun
 
 // The whole layer in one persistent launch (MXFP8 mode): both GEMMs and the
 // combine; with `route_in` (T <= kSmallRouteTokens) also the routing and the
-// activation step, and then it is the call's first kernel.  Without it the
-// routing kernels have run before (w holds their arrays).
+// activation step, and with `w_router` the router in front (its logits are
+// written to `logits`).  Without `route_in` the routing kernels have run
+// before (w holds their arrays).
 int enqueue_layer(const float* logits, const uint16_t* x, const uint8_t* w13, const uint8_t* w13s,
                   const uint8_t* w2, const uint8_t* w2s, int T, int H, int I, int E, int k,
                   bool route_in, bool first, const Work& w, void* y, DeviceState* d,
                   cudaStream_t stream, unsigned long long timeout_ns, const moe_opts* opts,
-                  Steps& st) {
+                  Steps& st, const void* w_router = nullptr) {
   TcParams p{};
   int rc;
   if ((rc = mxfp8_gemm_params(w13, w13s, w2, w2s, T, H, I, E, k, w, d, timeout_ns, p))) return rc;
@@ -767,6 +769,7 @@ int enqueue_layer(const float* logits, const uint16_t* x, const uint8_t* w13, co
     LayerRouteParams& r = p.route;
     r.logits = logits;
     r.x = x;
+    r.w_router = static_cast<const uint16_t*>(w_router);
     r.T = T;
     r.E = E;
     r.k = k;
@@ -830,9 +833,11 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       if (e == cudaSuccess) st.launched();
       return e;
     };
-    bool persistent = path == MOE_PATH_PERSISTENT ||
-                      (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) ==
-                                                    MOE_PATH_PERSISTENT);
+    // both GEMMs in one launch: the chain's MOE_PATH_PERSISTENT asks for it
+    // too (the chain has no whole-layer launch)
+    bool persistent = path == MOE_PATH_GEMMS || path == MOE_PATH_PERSISTENT ||
+                      (path == MOE_PATH_AUTO &&
+                       auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_GEMMS);
     if (persistent) {  // both GEMMs in one launch
       g2.dep_target = 4 * g1.m_tiles;  // four epilogue warps publish per tile pair
       if (opts && (opts->debug_flags & MOE_DEBUG_FORCE_DEP_TIMEOUT))
@@ -937,7 +942,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
   const int path = opts ? opts->path : MOE_PATH_AUTO;
   if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_GEMMS) return MOE_ERR_INVALID_ARG;
   if (!aligned(w13, 32) || !aligned(w2, 32)) return MOE_ERR_ALIGNMENT;
   if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
       !aligned(y, 16))
@@ -958,30 +963,35 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   const unsigned long long timeout_ns =
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
-  if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
-                                     timeout_ns, st)))
-    return rc;
   const float* lg = routed ? w.rlogits : logits;
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
   // wide token chunks cut the MMA instructions per token when experts get
   // many tokens (large T); narrow chunks keep the weight pipeline deepest
   const int chunk = chunk_for(act, T);
   const bool split = opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING);
-  const bool persistent =
-      act == MOE_ACT_MXFP8 &&
-      (path == MOE_PATH_PERSISTENT ||
-       (path == MOE_PATH_AUTO && auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_PERSISTENT));
+  // the whole layer in one launch (explicit MOE_PATH_PERSISTENT); the other
+  // paths run routing, GEMMs and combine as stream-ordered kernels, the GEMMs
+  // as one launch (MOE_PATH_GEMMS) or two
+  const bool persistent = act == MOE_ACT_MXFP8 && path == MOE_PATH_PERSISTENT;
+  const int gemm_path =
+      act != MOE_ACT_MXFP8 ? MOE_PATH_MULTI
+      : path == MOE_PATH_AUTO ? auto_path(T, H, I, E, k, act, d->sms)
+      : path == MOE_PATH_PERSISTENT ? MOE_PATH_MULTI  // (only after a refused layer launch)
+                                    : path;
   // the whole layer in one launch: for T <= 32 also the routing (steps a1-a4)
   const bool route_in = persistent && T <= kSmallRouteTokens && !split;
-  if (route_in) {
-    rc = enqueue_layer(lg, x, w13, w13s, w2, w2s, T, H, I, E, k, true, !routed, w, y, d, stream,
-                       timeout_ns, opts, st);
+  if (route_in) {  // (with the router inside too when the layer is routed)
+    rc = enqueue_layer(lg, x, w13, w13s, w2, w2s, T, H, I, E, k, true, true, w, y, d, stream,
+                       timeout_ns, opts, st, w_router);
     if (rc != kLayerLaunchTooLarge) {
       if (rc) return rc;
       st.mark();
       return launch_status();
     }
   }
+  if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
+                                     timeout_ns, st)))
+    return rc;
   if (T <= kSmallRouteTokens && !split) {
     if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
       return rc;
@@ -998,8 +1008,8 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
       return launch_status();
     }
   }
-  if ((rc = enqueue_gemms(act, persistent ? MOE_PATH_MULTI : path, w13, w13s, w2, w2s, T, H, I,
-                          E, k, w, d, stream, timeout_ns, opts, st)))
+  if ((rc = enqueue_gemms(act, gemm_path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream,
+                          timeout_ns, opts, st)))
     return rc;
   const int cap = d->sms * 8;
   st.mark();
@@ -1030,7 +1040,7 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
   const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
   const int path = opts ? opts->path : MOE_PATH_AUTO;
   if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
-  if (path < MOE_PATH_AUTO || path > MOE_PATH_PERSISTENT) return MOE_ERR_INVALID_ARG;
+  if (path < MOE_PATH_AUTO || path > MOE_PATH_GEMMS) return MOE_ERR_INVALID_ARG;
   if (!aligned(x_bf16, 16) || !aligned(y, 16)) return MOE_ERR_ALIGNMENT;
   for (int l = 0; l < n; ++l) {
     if (!logits[l] || !w13[l] || !w13s[l] || !w2[l] || !w2s[l]) return MOE_ERR_INVALID_ARG;
@@ -1406,6 +1416,18 @@ int moe_mxfp4_workspace_layout(int T, int H, int I, int E, int k, int act_mode,
   if (rc) return rc;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
   const Layout L = layout_for(T, H, I, E, k, act_mode);
+  *out = public_layout(L, 0, 0);
+  out->total = L.total;
+  return MOE_OK;
+}
+
+int moe_mxfp4_workspace_layout_routed(int T, int H, int I, int E, int k, int act_mode,
+                                      moe_workspace_layout* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  int rc = validate_shape(T, H, I, E, k);
+  if (rc) return rc;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  const Layout L = layout_for(T, H, I, E, k, act_mode, true);
   *out = public_layout(L, 0, 0);
   out->total = L.total;
   return MOE_OK;

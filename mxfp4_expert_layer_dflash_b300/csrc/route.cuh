@@ -42,7 +42,8 @@ __device__ __forceinline__ uint32_t warp_redux_min(uint32_t v) {
 // Round j picks the largest remaining logit, the lowest expert index among
 // equal ones: the warp's largest key (one reduction), then the lowest index
 // among the lanes whose own best has that key (a second one).
-template <int MAXPL>
+// kL2: load the logits from L2 only (written by other CTAs of the same launch)
+template <int MAXPL, bool kL2 = false>
 __device__ __forceinline__ void route_topk_token(const float* __restrict__ logits, int t, int E,
                                                  int k, int32_t* __restrict__ idx,
                                                  float* __restrict__ w, int* status) {
@@ -52,7 +53,8 @@ __device__ __forceinline__ void route_topk_token(const float* __restrict__ logit
 #pragma unroll
   for (int i = 0; i < MAXPL; ++i) {
     const int e = lane + 32 * i;
-    key[i] = e < E ? topk_key(l[e]) : 0u;  // 0: below every finite logit's key
+    // 0: below every finite logit's key
+    key[i] = e < E ? topk_key(kL2 ? __ldcg(l + e) : l[e]) : 0u;
   }
   float my_v = 0.0f;
   int my_e = 0;

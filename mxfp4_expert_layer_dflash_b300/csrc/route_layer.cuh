@@ -53,8 +53,9 @@ struct LayerRouteState {
 
 // Inputs and global outputs of the in-kernel routing
 struct LayerRouteParams {
-  const float* logits;  // [T, E]
+  const float* logits;  // [T, E] (written by the launch itself when w_router is given)
   const uint16_t* x;    // [T, H] bf16
+  const uint16_t* w_router;  // [E, H] bf16 router weights, or null: logits are an input
   int T, E, k, chunk_max, max_chunks;  // T = 0: routing is not done in the kernel
   // published by CTA 0 (the forward's workspace)
   int32_t* topk_idx;
@@ -118,14 +119,24 @@ __device__ __forceinline__ void layer_route_block(const LayerRouteParams& r, uin
   int32_t* s_cnt = s_perm + kLayerMaxTK;          // [E]
   int32_t* s_off = s_cnt + E + 1;                 // [E + 1]
 
-  // (1) top-k + softmax: warp w takes tokens w, w + 12, w + 24
+  // (1) top-k + softmax: warp w takes tokens w, w + 12, w + 24 (logits the
+  // launch computed itself are read from L2)
   for (int t = warp; t < T; t += kLayerThreads / 32) {
-    if (E <= 128)
-      route_topk_token<4>(r.logits, t, E, k, s_idx, s_w, status);
-    else if (E <= 384)
-      route_topk_token<12>(r.logits, t, E, k, s_idx, s_w, status);
-    else
-      route_topk_token<32>(r.logits, t, E, k, s_idx, s_w, status);
+    if (r.w_router) {
+      if (E <= 128)
+        route_topk_token<4, true>(r.logits, t, E, k, s_idx, s_w, status);
+      else if (E <= 384)
+        route_topk_token<12, true>(r.logits, t, E, k, s_idx, s_w, status);
+      else
+        route_topk_token<32, true>(r.logits, t, E, k, s_idx, s_w, status);
+    } else {
+      if (E <= 128)
+        route_topk_token<4>(r.logits, t, E, k, s_idx, s_w, status);
+      else if (E <= 384)
+        route_topk_token<12>(r.logits, t, E, k, s_idx, s_w, status);
+      else
+        route_topk_token<32>(r.logits, t, E, k, s_idx, s_w, status);
+    }
   }
   for (int e = tid; e < E; e += kLayerThreads) s_cnt[e] = 0;
   __syncthreads();
@@ -216,6 +227,97 @@ __device__ __forceinline__ void layer_route_block(const LayerRouteParams& r, uin
     if (tid == 0) {
       r.meta[0] = st->n_chunks;
       r.meta[1] = s_tot[0] >> 16;
+    }
+  }
+}
+
+// The router in front of the routing (logits = x W_r^T with bf16 W_r, read as
+// a plain linear layer; expert routing is part of the pipeline the runtime is
+// built around: techllm.github.io, "3. TileRT").  CTA c takes experts
+// [c E / G, (c + 1) E / G); its threads split H into runs of 16 elements,
+// each thread multiplying its runs of the experts' weight rows with the same
+// runs of up to 8 token rows at a time (exact bf16 products, fp32 sums in
+// ascending element order, every load of a run independent of the others),
+// then the threads' sums are added by a fixed butterfly within each warp and
+// the warps' in warp order.  Deterministic; the order differs from the
+// standalone router's tensor-core sums, within the same error bound.
+// `s_part`: 12 x 8 x 4 floats of shared memory.  All threads call it.
+constexpr int kRouterTok = 8, kRouterExp = 4;
+__device__ __forceinline__ void layer_router_logits(const LayerRouteParams& r, int64_t H,
+                                                    float* __restrict__ logits,
+                                                    float* __restrict__ s_part) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kLayerThreads / 32;
+  const int G = (int)gridDim.x, c = (int)blockIdx.x, E = r.E, T = r.T;
+  const int e_begin = (int)((int64_t)c * E / G), e_end = (int)((int64_t)(c + 1) * E / G);
+  const int runs = (int)(H / 16);
+  for (int eg = e_begin; eg < e_end; eg += kRouterExp) {
+    const int ne = min(kRouterExp, e_end - eg);
+    for (int tg = 0; tg < T; tg += kRouterTok) {
+      const int nt = min(kRouterTok, T - tg);
+      float acc[kRouterTok][kRouterExp];
+#pragma unroll
+      for (int t = 0; t < kRouterTok; ++t)
+#pragma unroll
+        for (int e = 0; e < kRouterExp; ++e) acc[t][e] = 0.0f;
+      for (int run = tid; run < runs; run += kLayerThreads) {
+        uint4 wv[kRouterExp][2], xv[kRouterTok][2];
+#pragma unroll
+        for (int e = 0; e < kRouterExp; ++e) {
+          if (e < ne) {
+            const uint4* src = reinterpret_cast<const uint4*>(r.w_router + (int64_t)(eg + e) * H) +
+                               2 * run;
+            wv[e][0] = src[0];
+            wv[e][1] = src[1];
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) {
+          if (t < nt) {
+            const uint4* src = reinterpret_cast<const uint4*>(r.x + (int64_t)(tg + t) * H) + 2 * run;
+            xv[t][0] = src[0];
+            xv[t][1] = src[1];
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) {
+#pragma unroll
+          for (int e = 0; e < kRouterExp; ++e) {
+            if (t < nt && e < ne) {
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t ww[4] = {wv[e][h].x, wv[e][h].y, wv[e][h].z, wv[e][h].w};
+                const uint32_t xx[4] = {xv[t][h].x, xv[t][h].y, xv[t][h].z, xv[t][h].w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  acc[t][e] = fmaf(__uint_as_float(ww[j] << 16), __uint_as_float(xx[j] << 16),
+                                   acc[t][e]);
+                  acc[t][e] = fmaf(__uint_as_float(ww[j] & 0xFFFF0000u),
+                                   __uint_as_float(xx[j] & 0xFFFF0000u), acc[t][e]);
+                }
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRouterTok; ++t) {
+#pragma unroll
+        for (int e = 0; e < kRouterExp; ++e) {
+          float v = acc[t][e];
+#pragma unroll
+          for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) s_part[(warp * kRouterTok + t) * kRouterExp + e] = v;
+        }
+      }
+      __syncthreads();
+      if (tid < nt * ne) {
+        const int t = tid / ne, e = tid - t * ne;
+        float v = 0.0f;
+        for (int w = 0; w < kWarps; ++w) v += s_part[(w * kRouterTok + t) * kRouterExp + e];
+        logits[(int64_t)(tg + t) * E + eg + e] = v;
+      }
+      __syncthreads();
     }
   }
 }

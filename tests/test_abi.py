@@ -200,6 +200,12 @@ def test_workspace_layout_is_disjoint_and_aligned(moe, T, H, I, E, k, act):
     lay = moe.moe_mxfp4_workspace_layout(T, H, I, E, k, act)
     assert lay.total == moe.moe_mxfp4_workspace_size(T, H, I, E, k, act)
     assert lay.x_stream[0] == lay.x_stream[1] == 2**64 - 1     # SIZE_MAX: single layer
+    assert lay.logits == 2**64 - 1                             # no router in this layout
+    rl = moe.moe_mxfp4_workspace_layout_routed(T, H, I, E, k, act)
+    assert rl.total == moe.moe_mxfp4_workspace_size_routed(T, H, I, E, k, act)
+    assert rl.logits % 256 == 0 and rl.logits + T * E * 4 <= rl.total
+    for n, o, b in _regions(rl, T, H, I, E, k, act):
+        assert o + b <= rl.logits or rl.logits + T * E * 4 <= o, n
     regs = sorted(_regions(lay, T, H, I, E, k, act), key=lambda r: r[1])
     for (n0, o0, b0), (n1, o1, b1) in zip(regs, regs[1:]):
         assert o0 + b0 <= o1, (n0, n1)

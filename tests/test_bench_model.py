@@ -36,3 +36,4 @@ def test_step_names_follow_the_launch_sequence():
                                         "gemm1+gemm2+combine"]
     assert bench.step_names(1, 8) == ["route_act", "gemm1", "gemm2", "combine"]
     assert bench.step_names(2, 32) == ["layer"]          # the whole layer in one launch
+    assert bench.step_names(3, 8) == ["route_act", "gemm1+gemm2", "combine"]

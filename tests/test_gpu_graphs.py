@@ -28,6 +28,7 @@ def _capture(fn):
 
 @pytest.mark.parametrize("name,path", [("mid_t8", moe.MOE_PATH_MULTI),
                                        ("mid_t8", moe.MOE_PATH_PERSISTENT),
+                                       ("mid_t8", moe.MOE_PATH_GEMMS),
                                        ("full_e32_t64", moe.MOE_PATH_AUTO)])
 def test_layer_graph_replay_is_bitwise_equal(name, path):
     L = LY.LAYERS[name]

@@ -6,7 +6,8 @@ tokens the routing kernels run first and the launch does the GEMMs and the combi
 meet at grid-wide barriers built on scratch that need not start at zero.
 
 Checked here, all through the C ABI:
-- one launch per forward at T <= 32 (the library's launch counter), four above;
+- one launch per forward at T <= 32 (the library's launch counter), four above; one for the
+  routed layer too, whose router then runs inside the launch;
 - the routing arrays CTA 0 publishes and the act1 codes the CTAs write, bit for bit against the
   oracle, across top-k widths, expert counts and tie-heavy logits;
 - y bit-identical to the multi-launch path (same arithmetic, same order);
@@ -133,18 +134,38 @@ def test_graph_replays_of_the_layer_launch():
         assert _eq(y, want)
 
 
-def test_routed_layer_through_the_layer_launch():
-    """Router in front (three launches), then the layer launch with the routing inside: the
-    same bits as the layer fed the router's logits."""
+def _abs_dot(x_bits, w_bits):
+    xa = np.abs(bf16_to_f64(x_bits))
+    wa = np.abs(bf16_to_f64(w_bits))
+    return xa @ wa.T
+
+
+@pytest.mark.parametrize("T,H,E,k", [(8, 1024, 64, 8), (32, 2048, 384, 8), (3, 512, 1000, 16)])
+def test_router_inside_the_layer_launch(O, T, H, E, k):
+    """The routed layer on the single-launch path at T <= 32: one launch computes the logits
+    (every warp one expert's row against all token rows), routes and runs the layer.  Read back
+    from the workspace: the logits lie within the router's error bound of the exact ones
+    (64 * 2^-24 * sum |x||w| per logit), the routing arrays are the oracle's routing of those
+    logits bit for bit, and y equals the multi-launch layer fed the same logits."""
     from synth import synth as S
-    L, _, _, inp = _inputs(8, 1024, 512, 64, 8, 93)
-    w_r = dev(S.router_bf16(93, L.E, L.H))
-    idx = torch.empty((L.T, L.k), dtype=torch.int32, device="cuda")
-    gate = torch.empty((L.T, L.k), dtype=torch.float32, device="cuda")
-    logits = torch.empty((L.T, L.E), dtype=torch.float32, device="cuda")
-    moe.moe_router_topk(inp[0], w_r, L.T, L.H, L.E, L.k, idx, gate, logits_out=logits)
-    y1 = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
-    moe.moe_mxfp4_forward_routed(inp[0], w_r, *inp[2:], L.T, L.H, L.I, L.E, L.k, y1, path=P)
-    y2 = _fwd((inp[0], logits) + inp[2:], L, M)
+    I = 256
+    L, xh, _, inp = _inputs(T, H, I, E, k, 95 + T)
+    w_r = S.router_bf16(95 + T, E, H)
+    lay = moe.moe_mxfp4_workspace_layout_routed(T, H, I, E, k)
+    ws = torch.randint(0, 256, (lay.total,), dtype=torch.uint8, device="cuda")
+    y1 = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+    moe.moe_mxfp4_forward_routed(inp[0], dev(w_r), *inp[2:], T, H, I, E, k, y1)   # set-up
+    n0 = moe.moe_mxfp4_launch_count()
+    moe.moe_mxfp4_forward_routed(inp[0], dev(w_r), *inp[2:], T, H, I, E, k, y1, path=P,
+                                 workspace=ws, workspace_bytes=lay.total)
     assert moe.moe_mxfp4_get_status() == 0
+    assert moe.moe_mxfp4_launch_count() - n0 == 1
+    lg = ws[lay.logits:lay.logits + T * E * 4].cpu().numpy().view(np.float32).reshape(T, E)
+    exact = O.router_logits(xh, w_r)
+    bound = 64 * 2.0 ** -24 * _abs_dot(xh, w_r)
+    assert (np.abs(lg - exact) <= bound).all()
+    a = _ws_arrays(ws, lay, T, H, I, E, k, moe.MOE_ACT_MXFP8)
+    pos = _check_routing(O, a, lg.copy(), k)
+    _check_act1(O, a, xh, pos, moe.MOE_ACT_MXFP8)
+    y2 = _fwd((inp[0], dev(lg.copy())) + inp[2:], L, M)
     assert _eq(y1, y2)

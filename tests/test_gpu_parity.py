@@ -123,7 +123,7 @@ def test_route_ties_and_shapes(O, T, E, k):
 
 # ------------------------------------------------------------------ the layer
 
-PATHS = [moe.MOE_PATH_MULTI, moe.MOE_PATH_PERSISTENT]
+PATHS = [moe.MOE_PATH_MULTI, moe.MOE_PATH_PERSISTENT, moe.MOE_PATH_GEMMS]
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -221,6 +221,7 @@ def _layer_inputs(O, T, H, I, E, k, seed, logits=None):
                                             (520, 128, 256, 3, 1, True)])
 @pytest.mark.parametrize("act,path", [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI),
                                       (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
+                                      (moe.MOE_ACT_MXFP8, moe.MOE_PATH_GEMMS),
                                       (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)])
 def test_forward_edge_shapes(O, T, H, I, E, k, ties, act, path):
     lg = np.zeros((T, E), np.float32) if ties else None   # ties: all tokens on experts 0..k-1
@@ -240,12 +241,14 @@ def test_forward_edge_shapes(O, T, H, I, E, k, ties, act, path):
 
 @pytest.mark.parametrize("name", SMALL + FULL)
 def test_persistent_equals_multi_kernel_bitwise(name):
-    """Both execution paths run the same arithmetic in the same order."""
+    """Every execution path runs the same arithmetic in the same order: the whole layer in
+    one launch, both GEMMs in one launch, and one launch per step."""
     L = LY.LAYERS[name]
     inp = device_layer(L)
     ym = gpu_forward(L, inp, path=moe.MOE_PATH_MULTI)
-    yp = gpu_forward(L, inp, path=moe.MOE_PATH_PERSISTENT)
-    assert torch.equal(ym.view(torch.int16), yp.view(torch.int16))
+    for path in (moe.MOE_PATH_PERSISTENT, moe.MOE_PATH_GEMMS):
+        yp = gpu_forward(L, inp, path=path)
+        assert torch.equal(ym.view(torch.int16), yp.view(torch.int16)), path
     del inp
     torch.cuda.empty_cache()
 
@@ -253,8 +256,8 @@ def test_persistent_equals_multi_kernel_bitwise(name):
 def test_auto_path_choice():
     """One launch for layers with a handful of GEMM work items per SM, two otherwise."""
     sel = moe.moe_mxfp4_select_path
-    assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT      # 8 tokens, mid shape
-    assert sel(32, 2048, 1024, 64, 8) == moe.MOE_PATH_PERSISTENT     # 32 tokens, mid shape
+    assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_GEMMS           # 8 tokens, mid shape
+    assert sel(32, 2048, 1024, 64, 8) == moe.MOE_PATH_GEMMS          # 32 tokens, mid shape
     assert sel(1, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI          # too few items per SM
     assert sel(16, 256, 128, 8, 2) == moe.MOE_PATH_MULTI
     assert sel(256, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # full shape, 256 tokens

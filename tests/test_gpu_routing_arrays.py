@@ -122,7 +122,8 @@ def test_forward_routing_arrays_and_act1_codes(O, name, flags, act):
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("path", [moe.MOE_PATH_MULTI, moe.MOE_PATH_PERSISTENT])
+@pytest.mark.parametrize("path", [moe.MOE_PATH_MULTI, moe.MOE_PATH_PERSISTENT,
+                                  moe.MOE_PATH_GEMMS])
 @pytest.mark.parametrize("name", ["tiny", "mid_t8"])
 def test_forward_act2_codes_against_emulation(O, name, path):
     """GEMM1's SwiGLU + MXFP8 epilogue output (hq/hs) against the oracle's act2(h): the same

@@ -23,28 +23,29 @@ def O():
     return oracle
 
 
+@pytest.mark.parametrize("path", [moe.MOE_PATH_PERSISTENT, moe.MOE_PATH_GEMMS])
 @pytest.mark.parametrize("name", ["tiny", "full_e32_t64"])
-def test_dependency_wait_times_out_and_context_survives(O, name):
+def test_dependency_wait_times_out_and_context_survives(O, name, path):
     L = LY.LAYERS[name]
     inp = device_layer(L)
     x, lg, w13, s13, w2, s2 = inp
     y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
     assert moe.moe_mxfp4_get_status() == 0
     moe.moe_mxfp4_forward_ex(x, lg, w13, s13, w2, s2, L.T, L.H, L.I, L.E, L.k, y,
-                             path=moe.MOE_PATH_PERSISTENT,
+                             path=path,
                              debug_flags=moe.MOE_DEBUG_SHORT_TIMEOUT
                              | moe.MOE_DEBUG_FORCE_DEP_TIMEOUT)
     assert moe.moe_mxfp4_get_status() == moe.MOE_ERR_DEVICE_TIMEOUT
     assert moe.moe_mxfp4_get_status() == 0          # reading the status clears it
     # the context survives: the same call without the flags is correct
     if name == "tiny":
-        y2 = bf16_to_f64(host_bf16(gpu_forward(L, inp, path=moe.MOE_PATH_PERSISTENT)))
+        y2 = bf16_to_f64(host_bf16(gpu_forward(L, inp, path=path)))
         w = LY.host_packed_weights(L, O.mxfp4_quantize)
         _, yref, _ = O.moe_forward(LY.host_x(L), LY.host_logits(L), *w, L.k, O.ACT_MXFP8)
         assert rel_fro(y2, yref) <= 1e-2
     else:
         ym = gpu_forward(L, inp, path=moe.MOE_PATH_MULTI)
-        yp = gpu_forward(L, inp, path=moe.MOE_PATH_PERSISTENT)
+        yp = gpu_forward(L, inp, path=path)
         assert torch.equal(ym.view(torch.int16), yp.view(torch.int16))
     del inp
     torch.cuda.empty_cache()

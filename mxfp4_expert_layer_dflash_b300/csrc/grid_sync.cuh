@@ -23,10 +23,20 @@
 namespace moe {
 
 constexpr int kMaxGridSync = 256;  // most CTAs a synchronised launch may have
-constexpr int kSyncOut = 0;        // barrier: every CTA's GEMM2 outputs are written
-constexpr int kSyncLogits = 1;     // barrier: every CTA's router logits are written
-constexpr int kSyncKinds = 2;
-constexpr uint64_t kChunkFlagKind = 2;      // a (chunk, GEMM1 tile pair) published
+// barrier slots (one flag per CTA each).  Consecutive layers of a launch use
+// alternate slots for the same barrier: a CTA with no work in a layer reaches
+// that layer's barrier right after the previous one, and must not overwrite a
+// flag another CTA still waits on.
+constexpr int kSyncOut = 0;     // (+ layer % 2) every CTA's GEMM2 outputs of a layer are written
+constexpr int kSyncLogits = 2;  // every CTA's router logits are written
+constexpr int kSyncAct = 3;     // (+ layer % 2) every CTA's act1 rows of a layer are written
+constexpr int kSyncKinds = 5;
+// the low byte of a flag value: which event, and of which layer of the launch
+constexpr uint64_t kChunkFlagKind = 0x10;   // + layer: a (chunk, GEMM1 tile pair) published
+constexpr uint64_t kLogitsKind = 0x30;
+constexpr uint64_t kOutKind = 0x40;         // + layer
+constexpr uint64_t kActKind = 0x80;         // + layer
+constexpr int kMaxLaunchLayers = 16;        // layers of one chained launch (kinds stay apart)
 constexpr uint64_t kChunkFlagNever = 0xFE;  // a kind no flag ever holds (forced timeout)
 // bytes of scratch before the per-chunk flags: the counter (8), the abort word
 // (8), the barrier flags
@@ -75,10 +85,11 @@ __device__ __forceinline__ void grid_sync_retire(const GridSync& g, uint64_t tag
 }
 
 // One thread of the CTA, after the CTA's writes are ordered before it (a
-// barrier among the writing threads): make them visible, then arrive.
-__device__ __forceinline__ void grid_arrive(const GridSync& g, int kind, uint64_t tag) {
+// barrier among the writing threads): make them visible, then arrive at the
+// barrier in `slot` with `value` (the call's tag | the event's kind).
+__device__ __forceinline__ void grid_arrive(const GridSync& g, int slot, uint64_t value) {
   __threadfence();
-  st_release_u64(g.flags + (size_t)kind * kMaxGridSync + blockIdx.x, tag | (uint64_t)kind);
+  st_release_u64(g.flags + (size_t)slot * kMaxGridSync + blockIdx.x, value);
 }
 
 __device__ __forceinline__ void grid_give_up(const GridSync& g, uint64_t tag) {
@@ -89,15 +100,17 @@ __device__ __forceinline__ bool grid_aborted(const GridSync& g, uint64_t tag) {
   return ld_relaxed_u64(g.abort) == (tag | 0xFFull);
 }
 
-// Warp-collective bounded wait until every CTA of the grid has arrived at
-// barrier `kind` (a warp-uniform result: false on timeout, on the CTA's own
-// abort flag or on another CTA's give-up).
-__device__ __forceinline__ bool grid_wait(const GridSync& g, int kind, uint64_t tag,
-                                          unsigned long long timeout_ns,
+// Warp-collective bounded wait until every CTA of the grid has arrived at the
+// barrier in `slot` with `want` (a warp-uniform result: false on timeout, on
+// the CTA's own abort flag or on another CTA's give-up).  A CTA arrives at the
+// barriers of a slot in one order, and no CTA can arrive at the next before
+// every CTA has passed this one, so a flag never skips past the value waited
+// for.
+__device__ __forceinline__ bool grid_wait(const GridSync& g, int slot, uint64_t want,
+                                          uint64_t tag, unsigned long long timeout_ns,
                                           const volatile int* abort_cta) {
   const int lane = threadIdx.x & 31;
-  const uint64_t want = tag | (uint64_t)kind;
-  const uint64_t* f = g.flags + (size_t)kind * kMaxGridSync;
+  const uint64_t* f = g.flags + (size_t)slot * kMaxGridSync;
   const int G = (int)gridDim.x;
   const uint64_t deadline = ptx::globaltimer() + timeout_ns;
   uint32_t spins = 0;
@@ -119,9 +132,9 @@ __device__ __forceinline__ bool grid_wait(const GridSync& g, int kind, uint64_t 
 
 // One thread, after the writes of a quarter of a (chunk, tile pair) of h are
 // ordered before it: publish them to the other CTAs (and their TMA reads).
-__device__ __forceinline__ void publish_chunk_tile(const GridSync& g, int idx, uint64_t tag) {
+__device__ __forceinline__ void publish_chunk_tile(const GridSync& g, int idx, uint64_t value) {
   __threadfence();
-  st_release_u64(g.chunk_flags + idx, tag | kChunkFlagKind);
+  st_release_u64(g.chunk_flags + idx, value);
 }
 
 // Warp-collective: are flags [first, first + n) all equal to `want`?  Relaxed

@@ -129,7 +129,36 @@ bool set_gemm_smem() {
                               cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
          cudaFuncSetAttribute(gemm_tc_kernel<kN, kModeLayer>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tc_smem_bytes<kN, kModeLayer>()) == cudaSuccess &&
+         cudaFuncSetAttribute(gemm_chain_kernel<kN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tc_smem_bytes<kN, kModeLayer>()) == cudaSuccess;
+}
+
+// Launches `kernel` (a persistent kernel whose CTAs wait on one another) as a
+// cooperative launch of one CTA per SM: every CTA is resident at once or the
+// launch fails without running (cudaErrorCooperativeLaunchTooLarge).  Also
+// programmatic when the driver accepts both attributes and it is not the
+// call's first kernel.
+template <typename P>
+cudaError_t launch_cooperative(void (*kernel)(P), int grid, size_t smem, cudaStream_t stream,
+                               const P& prm, bool first) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = first ? 1 : 2;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge || first) return e;
+  (void)cudaGetLastError();  // the combination was refused: cooperative only
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, prm);
 }
 
 // Launches `kernel` with programmatic stream serialization: it may be
@@ -166,30 +195,13 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
                       prm);
   // Both GEMMs (and, for the whole-layer mode, the combine and maybe the
   // routing) in one launch: CTAs wait for other CTAs' work, so every CTA must
-  // be resident at once.  A cooperative launch guarantees that, or fails
-  // without running anything.  It is also programmatic when the driver
-  // accepts both attributes and the launch is not the call's first: CTAs that
+  // be resident at once (a cooperative launch).  When programmatic, CTAs that
   // start early block in grid_dependency_wait() before any cross-CTA wait,
   // and the preceding kernel never waits on them.
-  void (*kernel)(TcParams) =
-      mode == kModeLayer ? gemm_tc_kernel<kN, kModeLayer> : gemm_tc_kernel<kN, kModeBoth>;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3((unsigned)grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = mode == kModeLayer ? tc_smem_bytes<kN, kModeLayer>() : smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = first ? 1 : 2;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, prm);
-  if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge || first) return e;
-  (void)cudaGetLastError();  // the combination was refused: cooperative only
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, prm);
+  if (mode == kModeLayer)
+    return launch_cooperative(gemm_tc_kernel<kN, kModeLayer>, grid,
+                              tc_smem_bytes<kN, kModeLayer>(), stream, prm, first);
+  return launch_cooperative(gemm_tc_kernel<kN, kModeBoth>, grid, smem, stream, prm, first);
 }
 
 constexpr int kRouterNMax = 256;                        // router tokens per work item
@@ -746,6 +758,15 @@ int mxfp8_gemm_params(const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2
 }
 
 std::atomic<uint32_t> g_calls{0};  // host call number: the salt of the grid barriers' tags
+
+// the barrier words of a persistent launch (in the call's scratch) and a new salt
+void set_grid_sync(TcParams& p, const Work& w) {
+  p.sync.counter = reinterpret_cast<uint32_t*>(w.sync);
+  p.sync.abort = reinterpret_cast<uint64_t*>(w.sync + 8);
+  p.sync.flags = reinterpret_cast<uint64_t*>(w.sync + 16);
+  p.sync.chunk_flags = reinterpret_cast<uint64_t*>(w.sync + kGridSyncBytes);
+  p.sync.salt = g_calls.fetch_add(1, std::memory_order_relaxed) + 1;
+}
 constexpr int kLayerLaunchTooLarge = 1;   // enqueue_layer: the cooperative launch was refused
 
 // The whole layer in one persistent launch (MXFP8 mode): both GEMMs and the
@@ -786,11 +807,7 @@ int enqueue_layer(const float* logits, const uint16_t* x, const uint8_t* w13, co
     r.xq = w.xq;
     r.xs = w.xs;
   }
-  p.sync.counter = reinterpret_cast<uint32_t*>(w.sync);
-  p.sync.abort = reinterpret_cast<uint64_t*>(w.sync + 8);
-  p.sync.flags = reinterpret_cast<uint64_t*>(w.sync + 16);
-  p.sync.chunk_flags = reinterpret_cast<uint64_t*>(w.sync + kGridSyncBytes);
-  p.sync.salt = g_calls.fetch_add(1, std::memory_order_relaxed) + 1;
+  set_grid_sync(p, w);
   p.pos = w.pos;
   p.gate = w.topk_w;
   p.y = static_cast<uint16_t*>(y);
@@ -1076,6 +1093,67 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
                                    st)))
       return rc;
     if ((rc = enqueue_act(act, x, carve_chain(ws, C, 0), T, H, k, d, stream, st))) return rc;
+  }
+  if (act == MOE_ACT_MXFP8 && path == MOE_PATH_PERSISTENT) {
+    // Whole layers in one launch: up to kMaxLaunchLayers layers per launch,
+    // each layer's combine writing the next layer's act1 rows (and, with the
+    // residual, the stream) inside the launch.
+    const bool wide = T >= kWideMinTokens;
+    for (int l0 = 0; l0 < n; l0 += kMaxLaunchLayers) {
+      const int nl = std::min(kMaxLaunchLayers, n - l0);
+      ChainParams cp{};
+      const Work w0 = carve_chain(ws, C, l0);
+      if ((rc = mxfp8_gemm_params(w13[l0], w13s[l0], w2[l0], w2s[l0], T, H, I, E, k, w0, d,
+                                  timeout_ns, cp.p)))
+        return rc;
+      cp.p.ph[1].dep_target = 4 * cp.p.ph[0].m_tiles;
+      if (opts && (opts->debug_flags & MOE_DEBUG_FORCE_DEP_TIMEOUT))
+        cp.p.ph[1].dep_target = INT_MAX;  // never reached: the dependency wait runs out
+      set_grid_sync(cp.p, w0);
+      cp.p.route.xq = w0.xq;  // the combines write the next layers' act1 rows here
+      cp.p.route.xs = w0.xs;
+      cp.p.T = T;
+      cp.p.H = H;
+      cp.p.k = k;
+      for (int i = 0; i < nl; ++i) {
+        const int l = l0 + i;
+        const Work wl = carve_chain(ws, C, l);
+        ChainLayer& L = cp.lay[i];
+        if ((rc = make_map(&L.map_w[0], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13[l], H,
+                           (uint64_t)E * 2 * I, H / 2, 128, 128)) ||
+            (rc = make_map(&L.map_w[1], CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2[l], I,
+                           (uint64_t)E * H, I / 2, 128, 128)))
+          return rc;
+        L.w_sf[0] = w13s[l];
+        L.w_sf[1] = w2s[l];
+        L.chunks = wl.chunks;
+        L.meta = wl.meta;
+        L.pos = wl.pos;
+        L.gate = wl.topk_w;
+        const bool last = l == n - 1;
+        L.x_res = residual ? (l == 0 ? x : xb[l & 1]) : nullptr;
+        L.x_out = last ? static_cast<uint16_t*>(y) : residual ? xb[(l + 1) & 1] : nullptr;
+        L.pos_next = last ? nullptr : carve_chain(ws, C, l + 1).pos;
+      }
+      cp.n_layers = nl;
+      if (d->sms > kMaxGridSync) return MOE_ERR_UNSUPPORTED_SHAPE;
+      st.mark();
+      const cudaError_t e =
+          wide ? launch_cooperative(gemm_chain_kernel<kChunkWide>, d->sms,
+                                    tc_smem_bytes<kChunkWide, kModeLayer>(), stream, cp, false)
+               : launch_cooperative(gemm_chain_kernel<kChunkNarrow>, d->sms,
+                                    tc_smem_bytes<kChunkNarrow, kModeLayer>(), stream, cp,
+                                    false);
+      if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        // (a device that cannot hold every CTA at once: nothing of this launch ran)
+        return e == cudaErrorCooperativeLaunchTooLarge ? MOE_ERR_UNSUPPORTED_SHAPE
+                                                        : MOE_ERR_CUDA;
+      }
+      st.launched();
+    }
+    st.mark();
+    return launch_status();
   }
   const int64_t threads = (int64_t)T * H / 4;
   for (int l = 0; l < n; ++l) {

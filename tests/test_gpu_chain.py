@@ -52,7 +52,7 @@ def _successive(x, lgs, ws, L, act, path=moe.MOE_PATH_AUTO):
 
 
 MODES = [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI), (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
-         (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)]
+         (moe.MOE_ACT_MXFP8, moe.MOE_PATH_GEMMS), (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)]
 
 
 @pytest.mark.parametrize("act,path", MODES)
@@ -67,19 +67,22 @@ def test_chain_without_residual_is_successive_calls(T, H, I, E, k, n, act, path)
     assert torch.equal(yc.view(torch.int16), ys.view(torch.int16))
 
 
-def test_chain_full_shape_is_successive_calls():
+@pytest.mark.parametrize("path", [moe.MOE_PATH_AUTO, moe.MOE_PATH_PERSISTENT])
+def test_chain_full_shape_is_successive_calls(path):
     Ls, lgs, ws = _layers(8, 6144, 2048, 384, 8, 2, 500)
     x = dev(LY.host_x(Ls[0]))
-    yc = _chain(x, lgs, ws, Ls[0], False, moe.MOE_ACT_MXFP8)
+    yc = _chain(x, lgs, ws, Ls[0], False, moe.MOE_ACT_MXFP8, path)
     ys = _successive(x, lgs, ws, Ls[0], moe.MOE_ACT_MXFP8)
     assert torch.equal(yc.view(torch.int16), ys.view(torch.int16))
     del ws
     torch.cuda.empty_cache()
 
 
-@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+@pytest.mark.parametrize("act,path", [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_AUTO),
+                                      (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
+                                      (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)])
 @pytest.mark.parametrize("T,H,I,E,k,n", [(16, 256, 128, 8, 2, 3), (5, 384, 256, 4, 2, 2)])
-def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act):
+def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act, path):
     from oracle import oracle as O
     Ls = [LY.Layer(f"res{l}", H, I, E, k, T, 300 + l) for l in range(n)]
     xh = LY.host_x(Ls[0])
@@ -89,7 +92,7 @@ def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act):
         w13, s13, w2, s2 = LY.host_packed_weights(L, O.mxfp4_quantize)
         wh.append((w13, s13 + 2, w2, s2 + 2))          # every weight x 4, exactly
     y = _chain(dev(xh), [dev(a) for a in lgh], [tuple(dev(a) for a in w) for w in wh], Ls[0],
-               True, act)
+               True, act, path)
     yg = bf16_to_f64(host_bf16(y))
     mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_EXACT
     yref = bf16_to_f64(O.moe_chain(xh, lgh, wh, k, mode, residual=True))
@@ -189,3 +192,44 @@ def test_chain_of_the_most_layers():
     yg = bf16_to_f64(host_bf16(y))
     assert float(np.abs(yref - bf16_to_f64(xh)).max()) > 0.1   # the last layer does move it
     assert rel_fro(yg, yref) <= MXFP8_FRO and max_err_over_rms(yg, yref) <= MXFP8_MAX
+
+
+@pytest.mark.parametrize("T,n", [(8, 4), (40, 3), (8, 40)])
+def test_chain_in_one_launch(T, n):
+    """MOE_PATH_PERSISTENT runs up to 16 chained layers in one launch (after the routing of
+    every layer): one launch per 16 layers plus the routing's, bit-identical to the chain of
+    per-layer launches, with and without the residual stream."""
+    H, I, E, k = 256, 128, 16, 4
+    Ls, lgs, ws = _layers(T, H, I, E, k, n, 2600 + T + n)
+    x = dev(LY.host_x(Ls[0]))
+    for residual in (False, True):
+        y_multi = _chain(x, lgs, ws, Ls[0], residual, moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI)
+        _chain(x, lgs, ws, Ls[0], residual, moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT)
+        n0 = moe.moe_mxfp4_launch_count()
+        y_one = _chain(x, lgs, ws, Ls[0], residual, moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT)
+        launches = moe.moe_mxfp4_launch_count() - n0
+        routing = 1 if T <= 32 else 3          # one routing launch, or two plus act1
+        assert launches == routing + (n + 15) // 16
+        assert torch.equal(y_one.view(torch.int16), y_multi.view(torch.int16))
+        if not residual:
+            ys = _successive(x, lgs, ws, Ls[0], moe.MOE_ACT_MXFP8)
+            assert torch.equal(y_one.view(torch.int16), ys.view(torch.int16))
+
+
+def test_chain_in_one_launch_timeout_and_recovery():
+    """The chained launch's GEMM2 dependency wait forced to run out: the call reports
+    MOE_ERR_DEVICE_TIMEOUT, every CTA gives up (barriers included), and the next chain on the
+    same workspace is correct."""
+    Ls, lgs, ws = _layers(8, 256, 128, 8, 2, 3, 2700)
+    x = dev(LY.host_x(Ls[0]))
+    want = _chain(x, lgs, ws, Ls[0], True, moe.MOE_ACT_MXFP8, moe.MOE_PATH_MULTI)
+    y = torch.empty_like(want)
+    moe.moe_mxfp4_forward_chain(x, lgs, [w[0] for w in ws], [w[1] for w in ws],
+                                [w[2] for w in ws], [w[3] for w in ws], 8, 256, 128, 8, 2, y,
+                                residual=True, path=moe.MOE_PATH_PERSISTENT,
+                                debug_flags=moe.MOE_DEBUG_SHORT_TIMEOUT
+                                | moe.MOE_DEBUG_FORCE_DEP_TIMEOUT)
+    assert moe.moe_mxfp4_get_status() == moe.MOE_ERR_DEVICE_TIMEOUT
+    assert moe.moe_mxfp4_get_status() == 0
+    y2 = _chain(x, lgs, ws, Ls[0], True, moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT)
+    assert torch.equal(y2.view(torch.int16), want.view(torch.int16))

@@ -174,7 +174,9 @@ def test_small_block_routing_kernel_bit_exact(O, E):
                 _check_routing(O, a, lg, k)
 
 
-@pytest.mark.parametrize("act", [moe.MOE_ACT_MXFP8, moe.MOE_ACT_BF16])
+@pytest.mark.parametrize("act,path", [(moe.MOE_ACT_MXFP8, moe.MOE_PATH_AUTO),
+                                      (moe.MOE_ACT_MXFP8, moe.MOE_PATH_PERSISTENT),
+                                      (moe.MOE_ACT_BF16, moe.MOE_PATH_AUTO)])
 @pytest.mark.parametrize("T,H,I,E,k,n,flags", [
     (8, 256, 128, 64, 8, 4, 0),                              # one launch routes every layer
     (8, 256, 128, 64, 8, 4, moe.MOE_DEBUG_SPLIT_ROUTING),    # the two general launches
@@ -182,7 +184,7 @@ def test_small_block_routing_kernel_bit_exact(O, E):
     (5, 384, 128, 384, 8, 3, 0),
     (64, 256, 128, 40, 4, 3, 0),                             # T > 32: general launches
 ])
-def test_chain_routing_arrays_bit_exact(O, T, H, I, E, k, n, flags, act):
+def test_chain_routing_arrays_bit_exact(O, T, H, I, E, k, n, flags, act, path):
     """Every layer's routing arrays of a chain, bit for bit; then the last layer's act1 rows,
     which the previous layer's combine wrote straight into its slots: with the residual on,
     the workspace keeps that layer's bf16 input, and its rows quantised by the oracle's rule
@@ -196,7 +198,7 @@ def test_chain_routing_arrays_bit_exact(O, T, H, I, E, k, n, flags, act):
     y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
     moe.moe_mxfp4_forward_chain(x, [dev(a) for a in lgh], [w[0] for w in ws_w],
                                 [w[1] for w in ws_w], [w[2] for w in ws_w], [w[3] for w in ws_w],
-                                T, H, I, E, k, y, residual=True, act_mode=act,
+                                T, H, I, E, k, y, residual=True, act_mode=act, path=path,
                                 workspace=ws, workspace_bytes=nb, debug_flags=flags)
     assert moe.moe_mxfp4_get_status() == 0
     pos = None

@@ -43,7 +43,9 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "gemm_traffic.txt")
 # the sources the GEMM kernels compile from (the DRAM traffic figures stay valid while
 # these are unchanged; host-side code does not change a kernel's traffic)
 KERNEL_SOURCES = [os.path.join(ROOT, "mxfp4_expert_layer_dflash_b300", "csrc", f)
-                  for f in ("common.cuh", "fmt.cuh", "gemm_tc.cuh", "ptx.cuh")]
+                  for f in ("combine.cuh", "common.cuh", "fmt.cuh", "gemm_tc.cuh", "grid_sync.cuh",
+                            "ptx.cuh", "quant.cuh", "route.cuh", "route_layer.cuh",
+                            "route_small.cuh")]
 # kernels of one forward in launch order, per execution path
 STEP_NAMES = {1: ["route_topk", "route_permute", "act_quant", "gemm1", "gemm2", "combine"],
               2: ["route_topk", "route_permute", "act_quant", "gemm1+gemm2+combine"],

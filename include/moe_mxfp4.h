@@ -49,7 +49,7 @@ typedef struct CUevent_st* cudaEvent_t;
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = -1,      /* null pointer, negative size, k out of range */
-  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 128, E or k too large */
+  MOE_ERR_UNSUPPORTED_SHAPE = -2, /* H or I not a multiple of 32, E or k too large */
   MOE_ERR_ALIGNMENT = -3,        /* a pointer is not aligned as documented */
   MOE_ERR_CUDA = -4,             /* a CUDA runtime call failed (launch, alloc, ...) */
   MOE_ERR_NO_MEMORY = -5,        /* workspace could not be allocated / is too small */
@@ -94,15 +94,23 @@ typedef enum {
  *  x_bf16         [T, H]       bf16 activations
  *  router_logits  [T, E]       fp32
  *  w13_fp4        [E, 2I, H/2] packed E2M1, element 2i in the low nibble of
- *                              byte i; 32-byte aligned
+ *                              byte i
  *  w13_e8m0       [E, 2I, H/32] one E8M0 scale per 32 elements along H
- *  w2_fp4         [E, H, I/2]  packed E2M1; 32-byte aligned
+ *  w2_fp4         [E, H, I/2]  packed E2M1
  *  w2_e8m0        [E, H, I/32]
  *  T >= 0 (T = 0 returns MOE_OK and launches nothing), H and I multiples of
- *  128, 1 <= E <= MOE_MAX_E, 1 <= k <= min(E, MOE_MAX_K)
+ *  32, 1 <= E <= MOE_MAX_E, 1 <= k <= min(E, MOE_MAX_K)
  *  y_bf16         [T, H]       bf16 output, overwritten
  *  stream         CUDA stream the work is ordered on (0 = legacy default)
- * Other pointers must be 16-byte aligned.  Scratch space comes from a
+ * Every pointer must be 16-byte aligned.  The GEMMs load FP4 weight rows 128
+ * elements at a time by TMA (the 16U4_ALIGN16B operand form), so they take
+ * H and I multiples of 128 and FP4 weights 32-byte aligned directly; any other
+ * layer (H or I a multiple of 32 only, or FP4 weights 16-byte aligned only)
+ * runs on zero-padded copies made in the scratch on every call — H and I
+ * rounded up to multiples of 128, the copies' extra weights, scales and
+ * activations zero — which gives the same y (zero terms add nothing to any
+ * sum, and the padding is whole blocks of 32) at the cost of copying the
+ * weights each call.  Scratch space comes from a
  * library-owned per-device cache that grows on first use of a larger shape
  * (a cudaMalloc outside any stream capture).
  * Sharing: every call on a device that is not given its own workspace
@@ -200,6 +208,9 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
  * Arguments: router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0 are HOST
  * arrays of n_layers device pointers, each as in moe_mxfp4_forward (one
  * layer's tensors); the shape (T, H, I, E, k) is shared by all layers.
+ * Chains take only the widths the GEMMs read directly: H and I multiples of
+ * 128 and FP4 weights 32-byte aligned (MOE_ERR_UNSUPPORTED_SHAPE /
+ * MOE_ERR_ALIGNMENT otherwise; no padded copies).
  * 1 <= n_layers <= MOE_MAX_CHAIN; residual is 0 or 1; y_bf16 [T, H] may equal
  * x_bf16.  opts as moe_mxfp4_forward_ex (act_mode, path, workspace of at least
  * moe_mxfp4_workspace_size_chain bytes, debug flags); step markers follow the
@@ -236,6 +247,17 @@ int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode);
 
 /* bytes of scratch a forward of this shape needs (0 on invalid arguments) */
 size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode);
+
+/*
+ * moe_mxfp4_workspace_size_padded — scratch bytes of a layer call that runs on
+ * zero-padded copies (see moe_mxfp4_forward): what a caller workspace must
+ * hold when the FP4 weight pointers are 16- but not 32-byte aligned (for H or
+ * I not multiples of 128, moe_mxfp4_workspace_size already returns this).
+ * routed = 1 for moe_mxfp4_forward_routed (the router weights are copied
+ * too), 0 otherwise.  Returns 0 for unsupported arguments.
+ */
+size_t moe_mxfp4_workspace_size_padded(int T, int H, int I, int E, int k, int act_mode,
+                                       int routed);
 
 /*
  * moe_mxfp4_workspace_layout — where a forward leaves its intermediate arrays
@@ -354,9 +376,11 @@ int moe_mxfp8_quantize_rows(const void* x_bf16, int64_t rows, int64_t K, uint8_t
  * library routine.
  *
  * Limits and sharing:
- *  - Shapes whose scratch (moe_mxfp4_workspace_size(T, H, I, E, k, 0)) exceeds
- *    MOE_NOALLOC_SCRATCH_BYTES return MOE_ERR_NO_MEMORY before anything is
- *    launched; at H = 6144, I = 2048, E = 384, k = 8 the largest T is 317.
+ *  - Shapes whose scratch (moe_mxfp4_workspace_size(T, H, I, E, k, 0), or
+ *    moe_mxfp4_workspace_size_padded(T, H, I, E, k, 0, 0) when the FP4
+ *    weights are only 16-byte aligned) exceeds MOE_NOALLOC_SCRATCH_BYTES
+ *    return MOE_ERR_NO_MEMORY before anything is launched; at H = 6144,
+ *    I = 2048, E = 384, k = 8 the largest T is 317.
  *  - All calls share the one array and it keeps the last call's contents;
  *    nothing in it needs to start at zero (every scratch byte a call reads is
  *    written earlier in the same call).  Calls that overlap on the GPU (on

@@ -22,7 +22,8 @@ MOE_DEBUG_SHORT_TIMEOUT = 1
 MOE_DEBUG_FORCE_DEP_TIMEOUT = 2
 MOE_DEBUG_SPLIT_ROUTING = 4
 MOE_DEBUG_STALL_DECODE = 8
-MOE_ERR_DEVICE_TIMEOUT = -6
+MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED_SHAPE, MOE_ERR_ALIGNMENT = -1, -2, -3
+MOE_ERR_CUDA, MOE_ERR_NO_MEMORY, MOE_ERR_DEVICE_TIMEOUT = -4, -5, -6
 MOE_MAX_K, MOE_MAX_E, MOE_MAX_CHAIN = 16, 1024, 256
 MOE_NOALLOC_SCRATCH_BYTES = 80 * 1024 * 1024
 
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         L.moe_mxfp4_workspace_size_chain.restype = sz
         L.moe_mxfp4_workspace_size_routed.argtypes = [i, i, i, i, i, i]
         L.moe_mxfp4_workspace_size_routed.restype = sz
+        L.moe_mxfp4_workspace_size_padded.argtypes = [i, i, i, i, i, i, i]
+        L.moe_mxfp4_workspace_size_padded.restype = sz
         L.moe_router_topk.argtypes = [vp, vp, i, i, i, i, vp, vp, vp, vp]
         L.moe_router_topk.restype = i
         L.mxfp8_quantize.argtypes = [vp, i64, i64, vp, vp, vp]
@@ -218,6 +221,10 @@ def moe_mxfp4_forward_routed(x_bf16, w_router_bf16, w13_fp4, w13_e8m0, w2_fp4, w
 
 def moe_mxfp4_workspace_size_routed(T, H, I, E, k, act_mode=MOE_ACT_MXFP8) -> int:
     return int(lib().moe_mxfp4_workspace_size_routed(T, H, I, E, k, act_mode))
+
+
+def moe_mxfp4_workspace_size_padded(T, H, I, E, k, act_mode=MOE_ACT_MXFP8, routed=False) -> int:
+    return int(lib().moe_mxfp4_workspace_size_padded(T, H, I, E, k, act_mode, int(routed)))
 
 
 def moe_router_topk(x_bf16, w_router_bf16, T, H, E, k, topk_idx, topk_w, logits_out=None,

@@ -28,6 +28,7 @@
 #include "fmt.cuh"
 #include "gemm_bf16.cuh"
 #include "gemm_tc.cuh"
+#include "pad.cuh"
 #include "quant.cuh"
 #include "route.cuh"
 #include "route_small.cuh"
@@ -480,12 +481,58 @@ int validate_shape(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
   if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0) return MOE_ERR_INVALID_ARG;
   if (k > E) return MOE_ERR_INVALID_ARG;
   if (k > MOE_MAX_K || E > MOE_MAX_E) return MOE_ERR_UNSUPPORTED_SHAPE;
-  if (H % 128 || I % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (H % 32 || I % 32) return MOE_ERR_UNSUPPORTED_SHAPE;
   if (T * k > (int64_t)1 << 30 || T * k * H > ((int64_t)1 << 40)) return MOE_ERR_UNSUPPORTED_SHAPE;
   return MOE_OK;
 }
 
 int launch_status() { return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// widths the GEMM kernels take directly (their FP4 weight rows are TMA-loaded
+// 128 elements at a time); other multiples of 32 run on zero-padded copies
+bool tc_widths(int64_t H, int64_t I) { return H % 128 == 0 && I % 128 == 0; }
+
+int64_t round128(int64_t v) { return (v + 127) / 128 * 128; }
+
+// A layer run on zero-padded copies (H or I rounded up to a multiple of 128,
+// or FP4 weights only 16-byte aligned): the padded layer's own scratch first
+// (so its routing arrays and activation buffers sit where the layout of the
+// padded shape puts them), then the copies of the weights, x, y and the router
+// weights (routed layers).
+struct PadLayout {
+  int64_t Hp, Ip;
+  Layout inner;
+  size_t w13, w13s, w2, w2s, x, y, wr, total;
+};
+
+PadLayout pad_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act,
+                     bool routed) {
+  PadLayout P{};
+  P.Hp = round128(H);
+  P.Ip = round128(I);
+  P.inner = layout_for(T, P.Hp, P.Ip, E, k, act, routed);
+  size_t o = P.inner.total;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align256(o + bytes);
+    return at;
+  };
+  P.w13 = take((size_t)(E * 2 * P.Ip * P.Hp / 2));
+  P.w13s = take((size_t)(E * 2 * P.Ip * P.Hp / 32));
+  P.w2 = take((size_t)(E * P.Hp * P.Ip / 2));
+  P.w2s = take((size_t)(E * P.Hp * P.Ip / 32));
+  P.x = take((size_t)(T * P.Hp * 2));
+  P.y = take((size_t)(T * P.Hp * 2));
+  P.wr = take(routed ? (size_t)(E * P.Hp * 2) : 0);
+  P.total = o;
+  return P;
+}
+
+// scratch bytes of a layer call whose FP4 weights are 32-byte aligned
+size_t layer_bytes(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int act, bool routed) {
+  return tc_widths(H, I) ? layout_for(T, H, I, E, k, act, routed).total
+                         : pad_layout(T, H, I, E, k, act, routed).total;
+}
 
 int grid_for(int64_t work, int per_block, int cap) {
   int64_t g = (work + per_block - 1) / per_block;
@@ -943,6 +990,11 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
   return MOE_OK;
 }
 
+int forward_padded(const void* x_bf16, const float* logits, const uint8_t* w13,
+                   const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int T, int H, int I,
+                   int E, int k, void* y, cudaStream_t stream, const moe_opts* opts,
+                   const void* w_router);
+
 // The layer.  Exactly one of `logits` (router logits [T, E]) and `w_router`
 // (router weights [E, H] bf16: the router GEMM runs in front of the top-k)
 // is given.
@@ -960,15 +1012,15 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   const int path = opts ? opts->path : MOE_PATH_AUTO;
   if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
   if (path < MOE_PATH_AUTO || path > MOE_PATH_GEMMS) return MOE_ERR_INVALID_ARG;
-  if (!aligned(w13, 32) || !aligned(w2, 32)) return MOE_ERR_ALIGNMENT;
-  if (!aligned(x_bf16, 16) || !aligned(logits, 16) || !aligned(w13s, 16) || !aligned(w2s, 16) ||
-      !aligned(y, 16))
+  if (!aligned(w13, 16) || !aligned(w2, 16) || !aligned(x_bf16, 16) || !aligned(logits, 16) ||
+      !aligned(w13s, 16) || !aligned(w2s, 16) || !aligned(y, 16))
     return MOE_ERR_ALIGNMENT;
+  if (opts && opts->workspace && !aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
+  if (!tc_widths(H, I) || !aligned(w13, 32) || !aligned(w2, 32))
+    return forward_padded(x_bf16, logits, w13, w13s, w2, w2s, T, H, I, E, k, y, stream, opts,
+                          w_router);
   const Layout L = layout_for(T, H, I, E, k, act, routed);
-  if (opts && opts->workspace) {
-    if (!aligned(opts->workspace, 256)) return MOE_ERR_ALIGNMENT;
-    if (opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
-  }
+  if (opts && opts->workspace && opts->workspace_bytes < L.total) return MOE_ERR_NO_MEMORY;
   if (T == 0) return MOE_OK;
 
   DeviceState* d = nullptr;
@@ -1039,6 +1091,69 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   return launch_status();
 }
 
+// The layer on zero-padded copies: weights, x (and the router weights) are
+// copied into the scratch with H and I rounded up to multiples of 128 (gate
+// rows to [0, I), up rows to [Ip, Ip + I) of each expert's padded w13), the
+// padded layer runs, and y keeps the first H columns of its padded output.
+// The added weights and activations are zero, so every real output is the
+// same sum as without them.  The copies are made on every call (one read and
+// one write of the weights): a path for shapes the GEMMs cannot take, not a
+// fast one.
+int forward_padded(const void* x_bf16, const float* logits, const uint8_t* w13,
+                   const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s, int T, int H, int I,
+                   int E, int k, void* y, cudaStream_t stream, const moe_opts* opts,
+                   const void* w_router) {
+  const bool routed = w_router != nullptr;
+  const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
+  const PadLayout P = pad_layout(T, H, I, E, k, act, routed);
+  if (opts && opts->workspace && opts->workspace_bytes < P.total) return MOE_ERR_NO_MEMORY;
+  if (T == 0) return MOE_OK;
+  DeviceState* d = nullptr;
+  int rc = device_state(&d);
+  if (rc) return rc;
+  void* ws = opts ? opts->workspace : nullptr;
+  if (!ws && (rc = cached_workspace(d, P.total, &ws))) return rc;
+  uint8_t* b = static_cast<uint8_t*>(ws);
+  const int64_t Hp = P.Hp, Ip = P.Ip;
+  const dim3 grid(d->sms * 4), block(256);
+  Steps st{nullptr, stream};
+  // the first copy is an ordinary launch: the previous call may still use
+  // the scratch; the others (and the padded layer's kernels) follow in order
+  bool first = true;
+  auto pad = [&](const void* src, uint8_t* dst, int64_t groups, int64_t src_rows,
+                 int64_t dst_rows, int64_t src_row_bytes, int64_t dst_row_bytes, int64_t n0,
+                 int64_t d1 = 0, int64_t n1 = 0, int64_t s1 = 0) {
+    const PadSpec ps{static_cast<const uint8_t*>(src), dst, groups, src_rows, dst_rows,
+                     src_row_bytes, dst_row_bytes, 0, n0, 0, d1, n1, s1};
+    cudaError_t e;
+    if (first) {
+      pad_rows_kernel<<<grid, block, 0, stream>>>(ps);
+      e = cudaGetLastError();
+    } else {
+      e = launch_pdl(pad_rows_kernel, grid, block, 0, stream, ps);
+    }
+    first = false;
+    st.launched();
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  };
+  if ((rc = pad(w13, b + P.w13, E, 2 * I, 2 * Ip, H / 2, Hp / 2, I, Ip, I, I)) ||
+      (rc = pad(w13s, b + P.w13s, E, 2 * I, 2 * Ip, H / 32, Hp / 32, I, Ip, I, I)) ||
+      (rc = pad(w2, b + P.w2, E, H, Hp, I / 2, Ip / 2, H)) ||
+      (rc = pad(w2s, b + P.w2s, E, H, Hp, I / 32, Ip / 32, H)) ||
+      (rc = pad(x_bf16, b + P.x, 1, T, T, 2 * H, 2 * Hp, T)) ||
+      (routed && (rc = pad(w_router, b + P.wr, 1, E, E, 2 * H, 2 * Hp, E))))
+    return rc;
+  moe_opts o = opts ? *opts : moe_opts{};
+  o.act_mode = act;
+  o.workspace = ws;
+  o.workspace_bytes = P.inner.total;
+  if ((rc = forward_impl(b + P.x, logits, b + P.w13, b + P.w13s, b + P.w2, b + P.w2s, T,
+                         (int)Hp, (int)Ip, E, k, b + P.y, stream, &o,
+                         routed ? b + P.wr : nullptr)))
+    return rc;
+  return pad(b + P.y, static_cast<uint8_t*>(y), 1, T, T, 2 * Hp, 2 * H, T);
+}
+
 // A chain of layers over one token block: x_0 = x, x_{l+1} = bf16_RNE(y_l +
 // residual * x_l), y = x_n.  Routing depends only on each layer's logits, so
 // every layer is routed first, all layers at once (two launches, or at T <= 32
@@ -1054,6 +1169,7 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
     return MOE_ERR_INVALID_ARG;
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
+  if (!tc_widths(H, I)) return MOE_ERR_UNSUPPORTED_SHAPE;  // chains take no padded layers
   const int act = opts ? opts->act_mode : MOE_ACT_MXFP8;
   const int path = opts ? opts->path : MOE_PATH_AUTO;
   if (act != MOE_ACT_MXFP8 && act != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
@@ -1221,7 +1337,15 @@ int moe_mxfp4_forward_ex(const void* x_bf16, const float* router_logits, const u
 size_t moe_mxfp4_workspace_size(int T, int H, int I, int E, int k, int act_mode) {
   if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
-  return layout_for(T, H, I, E, k, act_mode).total;
+  return layer_bytes(T, H, I, E, k, act_mode, false);
+}
+
+size_t moe_mxfp4_workspace_size_padded(int T, int H, int I, int E, int k, int act_mode,
+                                       int routed) {
+  if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
+  if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
+  if (routed != 0 && routed != 1) return 0;
+  return pad_layout(T, H, I, E, k, act_mode, routed == 1).total;
 }
 
 int moe_mxfp4_forward_chain(int n_layers, const void* x_bf16, const float* const* router_logits,
@@ -1236,7 +1360,7 @@ int moe_mxfp4_forward_chain(int n_layers, const void* x_bf16, const float* const
 size_t moe_mxfp4_workspace_size_chain(int n_layers, int T, int H, int I, int E, int k,
                                       int act_mode) {
   if (n_layers < 1 || n_layers > MOE_MAX_CHAIN) return 0;
-  if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
+  if (validate_shape(T, H, I, E, k) != MOE_OK || !tc_widths(H, I)) return 0;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
   return chain_layout(n_layers, T, H, I, E, k, act_mode).total;
 }
@@ -1247,7 +1371,7 @@ int moe_mxfp4_select_path(int T, int H, int I, int E, int k, int act_mode) {
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
   DeviceState* d = nullptr;
   if ((rc = device_state(&d))) return rc;
-  return auto_path(T, H, I, E, k, act_mode, d->sms);
+  return auto_path(T, (int)round128(H), (int)round128(I), E, k, act_mode, d->sms);
 }
 
 int mxfp4_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_fp4, uint8_t* out_e8m0,
@@ -1325,7 +1449,7 @@ int moe_mxfp4_forward_routed(const void* x_bf16, const void* w_router_bf16,
 size_t moe_mxfp4_workspace_size_routed(int T, int H, int I, int E, int k, int act_mode) {
   if (validate_shape(T, H, I, E, k) != MOE_OK) return 0;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return 0;
-  return layout_for(T, H, I, E, k, act_mode, true).total;
+  return layer_bytes(T, H, I, E, k, act_mode, true);
 }
 
 int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H, int E, int k,
@@ -1333,6 +1457,7 @@ int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H,
   if (!x_bf16 || !w_router_bf16 || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
   int rc = validate_shape(T, H, 128, E, k);
   if (rc) return rc;
+  if (H % 128) return MOE_ERR_UNSUPPORTED_SHAPE;  // the router GEMM's K tiles
   if (!aligned(x_bf16, 16) || !aligned(w_router_bf16, 16)) return MOE_ERR_ALIGNMENT;
   if (T == 0) return MOE_OK;
   DeviceState* d = nullptr;
@@ -1493,9 +1618,10 @@ int moe_mxfp4_workspace_layout(int T, int H, int I, int E, int k, int act_mode,
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
-  const Layout L = layout_for(T, H, I, E, k, act_mode);
+  // a padded layer's routing arrays and buffers are those of the padded shape
+  const Layout L = layout_for(T, round128(H), round128(I), E, k, act_mode);
   *out = public_layout(L, 0, 0);
-  out->total = L.total;
+  out->total = layer_bytes(T, H, I, E, k, act_mode, false);
   return MOE_OK;
 }
 
@@ -1505,9 +1631,10 @@ int moe_mxfp4_workspace_layout_routed(int T, int H, int I, int E, int k, int act
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
-  const Layout L = layout_for(T, H, I, E, k, act_mode, true);
+  // a padded layer's routing arrays and buffers are those of the padded shape
+  const Layout L = layout_for(T, round128(H), round128(I), E, k, act_mode, true);
   *out = public_layout(L, 0, 0);
-  out->total = L.total;
+  out->total = layer_bytes(T, H, I, E, k, act_mode, true);
   return MOE_OK;
 }
 
@@ -1518,6 +1645,7 @@ int moe_mxfp4_workspace_layout_chain(int n_layers, int layer, int T, int H, int 
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
   if (act_mode != MOE_ACT_MXFP8 && act_mode != MOE_ACT_BF16) return MOE_ERR_INVALID_ARG;
+  if (!tc_widths(H, I)) return MOE_ERR_UNSUPPORTED_SHAPE;
   const ChainLayout C = chain_layout(n_layers, T, H, I, E, k, act_mode);
   *out = public_layout(C.base, (size_t)layer * C.route_block, C.act_shift);
   out->x_stream[0] = C.xb[0];
@@ -1570,11 +1698,14 @@ int moe_mxfp4_forward_noalloc(const void* x_bf16, const float* router_logits,
     return MOE_ERR_INVALID_ARG;
   int rc = validate_shape(T, H, I, E, k);
   if (rc) return rc;
-  if (!aligned(w13_fp4, 32) || !aligned(w2_fp4, 32) || !aligned(x_bf16, 16) ||
+  if (!aligned(w13_fp4, 16) || !aligned(w2_fp4, 16) || !aligned(x_bf16, 16) ||
       !aligned(router_logits, 16) || !aligned(w13_e8m0, 16) || !aligned(w2_e8m0, 16) ||
       !aligned(y_bf16, 16))
     return MOE_ERR_ALIGNMENT;
-  if (layout_for(T, H, I, E, k, MOE_ACT_MXFP8).total > (size_t)MOE_NOALLOC_SCRATCH_BYTES)
+  const bool padded = !tc_widths(H, I) || !aligned(w13_fp4, 32) || !aligned(w2_fp4, 32);
+  if ((padded ? pad_layout(T, H, I, E, k, MOE_ACT_MXFP8, false).total
+              : layout_for(T, H, I, E, k, MOE_ACT_MXFP8).total) >
+      (size_t)MOE_NOALLOC_SCRATCH_BYTES)
     return MOE_ERR_NO_MEMORY;  // needs more scratch than the static array holds
   if (T == 0) return forward_impl(x_bf16, router_logits, w13_fp4, w13_e8m0, w2_fp4, w2_e8m0, T, H,
                                   I, E, k, y_bf16, stream, nullptr);

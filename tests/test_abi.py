@@ -54,7 +54,8 @@ def test_workspace_size(moe):
     big = moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8)
     assert 0 < small < big
     assert moe.moe_mxfp4_workspace_size(256, 6144, 2048, 384, 8, 1) > big
-    assert moe.moe_mxfp4_workspace_size(16, 250, 128, 8, 2) == 0       # H % 128
+    assert moe.moe_mxfp4_workspace_size(16, 250, 128, 8, 2) == 0       # H % 32
+    assert moe.moe_mxfp4_workspace_size(16, 256, 112, 8, 2) == 0       # I % 32
     assert moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 9) == 0       # k > E
     assert moe.moe_mxfp4_workspace_size(16, 256, 128, 8, 2, 7) == 0    # bad act mode
 
@@ -75,9 +76,10 @@ def test_host_validation_rejects_before_launch(moe):
     assert _fwd(moe, k=9) == -1
     assert _fwd(moe, k=17, E=32) == -2
     assert _fwd(moe, E=2000, k=2) == -2
-    assert _fwd(moe, H=200) == -2
-    assert _fwd(moe, I=96) == -2
-    assert _fwd(moe, w13=1040) == -3        # fp4 weights need 32-byte alignment
+    assert _fwd(moe, H=200) == -2           # widths: multiples of 32
+    assert _fwd(moe, I=80) == -2
+    assert _fwd(moe, w13=1032) == -3        # every pointer 16-byte aligned
+    assert _fwd(moe, w2=4100) == -3
     assert _fwd(moe, x=258) == -3
     assert _fwd(moe, T=0) == 0               # no-op, nothing launched
     L = moe.lib()
@@ -102,7 +104,7 @@ def test_forward_ex_rejects_small_workspace(moe):
 
 def test_select_path_validates_on_host(moe):
     L = moe.lib()
-    assert L.moe_mxfp4_select_path(16, 250, 128, 8, 2, 0) == -2     # H % 128
+    assert L.moe_mxfp4_select_path(16, 250, 128, 8, 2, 0) == -2     # H % 32
     assert L.moe_mxfp4_select_path(16, 256, 128, 8, 9, 0) == -1     # k > E
     assert L.moe_mxfp4_select_path(16, 256, 128, 8, 2, 5) == -1     # bad act mode
 
@@ -117,6 +119,7 @@ def test_next_rows_validate_on_host(moe):
     assert L.moe_fp8_dense_forward(256, 512, 1024, 0, 256, 64, 2048, None) == 0
     # router: shapes as the layer
     assert L.moe_router_topk(256, 512, 4, 250, 8, 2, None, 1024, 2048, None) == -2
+    assert L.moe_router_topk(256, 512, 4, 160, 8, 2, None, 1024, 2048, None) == -2  # K tiles
     assert L.moe_router_topk(256, 512, 4, 256, 8, 9, None, 1024, 2048, None) == -1
     assert L.moe_router_topk(256, None, 4, 256, 8, 2, None, 1024, 2048, None) == -1
     assert L.moe_router_topk(256, 512, 0, 256, 8, 2, None, 1024, 2048, None) == 0
@@ -179,6 +182,7 @@ def test_chain_workspace_size(moe):
     assert one < c1 < c4                          # residual buffers; a routing block per layer
     assert moe.moe_mxfp4_workspace_size_chain(0, 16, 256, 128, 8, 2) == 0
     assert moe.moe_mxfp4_workspace_size_chain(2, 16, 250, 128, 8, 2) == 0
+    assert moe.moe_mxfp4_workspace_size_chain(2, 16, 160, 128, 8, 2) == 0   # no padded chains
     assert moe.moe_mxfp4_workspace_size_chain(2, 16, 256, 128, 8, 2, 9) == 0
 
 
@@ -241,6 +245,7 @@ def test_chain_workspace_layout(moe):
     import ctypes
     assert L.moe_mxfp4_workspace_layout_chain(3, 3, T, H, I, E, k, 0, ctypes.byref(lay)) == -1
     assert L.moe_mxfp4_workspace_layout_chain(3, 0, T, 250, I, E, k, 0, ctypes.byref(lay)) == -2
+    assert L.moe_mxfp4_workspace_layout_chain(3, 0, T, 160, I, E, k, 0, ctypes.byref(lay)) == -2
     assert L.moe_mxfp4_workspace_layout(T, H, I, E, k, 0, None) == -1
 
 
@@ -252,7 +257,7 @@ def test_noalloc_checks_arguments_before_its_scratch_limit(moe):
     args = [256, 512, 1024, 2048, 4096, 8192]
     assert L.moe_mxfp4_forward_noalloc(None, *args[1:], big_T, 6144, 2048, 384, 8, 16384,
                                        None) == -1
-    assert L.moe_mxfp4_forward_noalloc(*args[:2], 1040, *args[3:], big_T, 6144, 2048, 384, 8,
+    assert L.moe_mxfp4_forward_noalloc(*args[:2], 1032, *args[3:], big_T, 6144, 2048, 384, 8,
                                        16384, None) == -3
     assert L.moe_mxfp4_forward_noalloc(*args, big_T, 6144, 2048, 384, 8, 16384, None) == -5
     assert L.moe_mxfp4_forward_noalloc(*args, 4, 250, 128, 8, 2, 16384, None) == -2
@@ -260,3 +265,33 @@ def test_noalloc_checks_arguments_before_its_scratch_limit(moe):
 
 def test_alloc_counter_is_exported(moe):
     assert moe.moe_mxfp4_alloc_count() >= 0
+
+
+def test_padded_workspace_sizes(moe):
+    """Widths that are multiples of 32 but not of 128 run on zero-padded copies: their scratch
+    is the padded shape's layout followed by the copies of the weights, x and y."""
+    T, H, I, E, k = 16, 160, 96, 8, 2
+    Hp, Ip = 256, 128
+    n = moe.moe_mxfp4_workspace_size(T, H, I, E, k)
+    assert n == moe.moe_mxfp4_workspace_size_padded(T, H, I, E, k)
+    copies = E * 2 * Ip * Hp // 2 + E * 2 * Ip * Hp // 32 + E * Hp * Ip // 2 + E * Hp * Ip // 32
+    copies += 2 * T * Hp * 2
+    assert n >= moe.moe_mxfp4_workspace_size(T, Hp, Ip, E, k) + copies
+    nr = moe.moe_mxfp4_workspace_size_routed(T, H, I, E, k)
+    assert nr == moe.moe_mxfp4_workspace_size_padded(T, H, I, E, k, routed=True)
+    assert nr >= moe.moe_mxfp4_workspace_size_routed(T, Hp, Ip, E, k) + copies + E * Hp * 2
+    # 16-byte aligned FP4 weights at native widths: the padded size is the larger one
+    assert (moe.moe_mxfp4_workspace_size_padded(T, 256, 128, E, k)
+            > moe.moe_mxfp4_workspace_size(T, 256, 128, E, k))
+    assert moe.moe_mxfp4_workspace_size_padded(T, 250, 128, E, k) == 0
+    assert moe.moe_mxfp4_workspace_size_padded(T, H, I, E, k, routed=2) == 0
+
+
+@pytest.mark.parametrize("act", [0, 1])
+def test_padded_layout_is_the_padded_shapes(moe, act):
+    T, H, I, E, k = 16, 160, 96, 8, 2
+    lay = moe.moe_mxfp4_workspace_layout(T, H, I, E, k, act)
+    ref = moe.moe_mxfp4_workspace_layout(T, 256, 128, E, k, act)
+    for name in ("topk_idx", "topk_w", "cnt", "off", "perm", "pos", "xq", "xs", "hq", "hs", "yp"):
+        assert getattr(lay, name) == getattr(ref, name), name
+    assert lay.total == moe.moe_mxfp4_workspace_size(T, H, I, E, k, act) > ref.total

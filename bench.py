@@ -352,11 +352,12 @@ CONFIG_LAYERS = [("c0", "tiny"), ("c1", "mid_t8"), ("c2", "full_t8"), ("c3", "fu
                  ("c4", "full_t1024_zipf")]
 
 
-def measure_config(L, steps, flush_buf):
+def measure_config(L, steps, flush, flush_dirty):
     """µs per layer of one config: hot (back-to-back forwards, L2 warm) and cold (L2
-    flushed before each forward by writing a buffer twice its size; the forward alone is
-    timed with events around it), plus the routing's touched experts.  The forward is
-    replayed from a CUDA graph so that small layers are not timed by the host's enqueue."""
+    emptied before each forward by `flush`; the forward alone is timed with events around
+    it; also with the dirty-line flush, for comparison), plus the routing's touched experts.
+    The forward is replayed from a CUDA graph so that small layers are not timed by the
+    host's enqueue."""
     import torch
     import mxfp4_expert_layer_dflash_b300 as moe
     from synth import layers as LY
@@ -385,8 +386,9 @@ def measure_config(L, steps, flush_buf):
     b.record()
     torch.cuda.synchronize()
     hot_us = a.elapsed_time(b) / steps * 1e3
-    cold_us, _ = _time_cold(fwd, min(steps, 50), flush_buf)
-    bf16_us, _ = _time_cold(fwd_bf16, min(steps, 50), flush_buf)
+    cold_us, _ = _time_cold(fwd, min(steps, 50), flush)
+    dirty_us, _ = _time_cold(fwd, min(steps, 50), flush_dirty)
+    bf16_us, _ = _time_cold(fwd_bf16, min(steps, 50), flush)
     if moe.moe_mxfp4_get_status() != 0:
         raise RuntimeError(f"device status error in config {L.name}")
     del w
@@ -394,7 +396,8 @@ def measure_config(L, steps, flush_buf):
     return {"layer": L.desc, "touched_experts": touched, "alg_bytes": b_layer,
             "path": PATH_NAMES[moe.moe_mxfp4_select_path(L.T, L.H, L.I, L.E,
                                                                              L.k)],
-            "us_hot": hot_us, "us_cold_l2_flushed": cold_us, "issued_as": how,
+            "us_hot": hot_us, "us_cold_l2_flushed": cold_us, "flush": flush.desc,
+            "us_cold_l2_dirty": dirty_us, "issued_as": how,
             "tokens_per_s_cold": L.T / (cold_us * 1e-6),
             "hbm_gbs_cold": b_layer / (cold_us * 1e-6) / 1e9,
             "bf16_mode_us_cold": bf16_us, "bf16_mode_hbm_gbs_cold": b_layer / (bf16_us * 1e-6) / 1e9}
@@ -424,7 +427,32 @@ def _replayable(fn):
         return fn, "eager"
 
 
-def _time_cold(fn, steps, flush_buf):
+class L2Flush:
+    """Empties the L2 before a cold-cache call: writes a buffer of twice the L2's size
+    (126 MB), then (unless `dirty`) reads another of the same size, so that the call starts
+    with none of its data in L2 and with no dirty lines of the flush left, whose write-back it
+    would otherwise pay (11-18 µs at the full layer shape: 126 MB of write-back)."""
+
+    def __init__(self, dirty=False):
+        import torch
+        n = 2 * 126 * 2**20 // 4
+        self.w = torch.empty(n, dtype=torch.float32, device="cuda")
+        self.r = None if dirty else torch.ones(n, dtype=torch.float32, device="cuda")
+        self.acc = torch.zeros(1, dtype=torch.float32, device="cuda")
+
+    def __call__(self):
+        import torch
+        self.w.add_(1)
+        if self.r is not None:
+            torch.sum(self.r, dim=0, keepdim=True, out=self.acc)
+
+    @property
+    def desc(self):
+        return ("252 MB written, then 252 MB read" if self.r is not None
+                else "252 MB written (L2 left full of dirty lines)")
+
+
+def _time_cold(fn, steps, flush):
     """median µs of one call with L2 flushed before each (events around the call only),
     and how the call was issued ("graph" replay or "eager")"""
     import torch
@@ -432,7 +460,7 @@ def _time_cold(fn, steps, flush_buf):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(steps)]
     for e0, e1 in ev:
-        flush_buf.add_(1)
+        flush()
         e0.record()
         run()
         e1.record()
@@ -440,7 +468,7 @@ def _time_cold(fn, steps, flush_buf):
     return statistics.median(e0.elapsed_time(e1) for e0, e1 in ev) * 1e3, how
 
 
-def measure_next_rows(pk, flush_buf):
+def measure_next_rows(pk, flush):
     """The steps beside the layer: the router (split-K bf16 GEMM + top-k), the layer with the
     router in front, a dense MXFP8 projection (K = N = 6144), the rejection-sampling
     verification of the drafted block, each against its roofline, and a chain of 4 layers in
@@ -460,7 +488,7 @@ def measure_next_rows(pk, flush_buf):
         idx = torch.empty((T, k), dtype=torch.int32, device="cuda")
         gate = torch.empty((T, k), dtype=torch.float32, device="cuda")
         us, how = _time_cold(lambda: moe.moe_router_topk(x, w, T, H, E, k, idx, gate), 50,
-                             flush_buf)
+                             flush)
         byt = E * H * 2 + T * H * 2 + T * k * 8
         fl = 2.0 * T * H * E
         rep[f"router_t{T}"] = {
@@ -480,7 +508,7 @@ def measure_next_rows(pk, flush_buf):
         del wf
         y = torch.empty((T, N), dtype=torch.bfloat16, device="cuda")
         us, how = _time_cold(lambda: moe.moe_fp8_dense_forward(x, codes, sc, T, K, N, y), 50,
-                             flush_buf)
+                             flush)
         byt = N * K + N * K // 32 + T * K * 2 + T * N * 2
         fl = 2.0 * T * K * N
         rep[f"dense_fp8_t{T}"] = {
@@ -497,7 +525,7 @@ def measure_next_rows(pk, flush_buf):
     n_acc = torch.empty(Sq, dtype=torch.int32, device="cuda")
     tok = torch.empty((Sq, g + 1), dtype=torch.int32, device="cuda")
     us, how = _time_cold(lambda: moe.moe_verify_block(*tens, Ut, Sq, g, V, n_acc, tok), 50,
-                         flush_buf)
+                         flush)
     rows = int(sum(2 if a < g else 1 for a in n_acc.cpu().numpy()))
     byt = rows * V * 4 + Sq * g * 16 + Sq * (g + 2) * 4
     rep["verify_s32_g7"] = {
@@ -515,9 +543,9 @@ def measure_next_rows(pk, flush_buf):
         torch.bfloat16).cuda()
     y = torch.empty((L.T, L.H), dtype=torch.bfloat16, device="cuda")
     us_r, how = _time_cold(lambda: moe.moe_mxfp4_forward_routed(x, w_r, *wts, L.T, L.H, L.I,
-                                                                L.E, L.k, y), 20, flush_buf)
+                                                                L.E, L.k, y), 20, flush)
     us_l, _ = _time_cold(lambda: moe.moe_mxfp4_forward(x, lg, *wts, L.T, L.H, L.I, L.E, L.k, y),
-                         20, flush_buf)
+                         20, flush)
     rep["routed_layer_t256"] = {"shape": L.desc + ", router in front", "us_cold": us_r,
                                 "us_cold_layer_on_given_logits": us_l, "issued_as": how}
     del wts
@@ -525,8 +553,8 @@ def measure_next_rows(pk, flush_buf):
     # a chain of 4 layers (distinct weights and logits) against 4 successive calls
     for name in ("mid_t8", "full_t8"):
         chain, succ, n, L = _chain_calls(LY.LAYERS[name], 4)
-        us_c, how = _time_cold(chain, 20, flush_buf)
-        us_s, _ = _time_cold(succ, 20, flush_buf)
+        us_c, how = _time_cold(chain, 20, flush)
+        us_s, _ = _time_cold(succ, 20, flush)
         rep[f"chain_{name}_x{n}"] = {
             "shape": f"{n} layers of {L.desc.replace(f' seed={L.seed}', '')}, no residual",
             "us_cold_per_layer_chain": us_c / n, "us_cold_per_layer_successive": us_s / n,
@@ -792,10 +820,11 @@ def run_ours(args, L, rank, world, local_rank):
     }
     if world == 1 and not args.no_config_sweep:
         log("[rank 0] measuring every config (hot and L2-flushed)")
-        flush = torch.empty(2 * 126 * 2**20 // 4, dtype=torch.float32, device="cuda")
+        flush, flush_dirty = L2Flush(), L2Flush(dirty=True)
         rep = {}
         for tag, name in CONFIG_LAYERS:
-            r = measure_config(LY.LAYERS[name], 200 if LY.LAYERS[name].T < 256 else 50, flush)
+            r = measure_config(LY.LAYERS[name], 200 if LY.LAYERS[name].T < 256 else 50, flush,
+                               flush_dirty)
             r["hbm_frac_cold"] = r["hbm_gbs_cold"] / hbm
             Lc = LY.LAYERS[name]
             flops = 2.0 * Lc.T * Lc.k * 3 * Lc.H * Lc.I
@@ -816,7 +845,7 @@ def run_ours(args, L, rank, world, local_rank):
         out["configs_report"] = rep
         log("[rank 0] measuring the router, the routed layer and the dense projection")
         out["next_rows"] = measure_next_rows(pk, flush)
-        del flush
+        del flush, flush_dirty
     if world == 1 and not args.no_cpu_baseline:
         log("[rank 0] timing the CPU oracle over the layer")
         run, n_tok, sample = oracle_layer_sample(L, args.act, args.cpu_tokens)

@@ -101,6 +101,8 @@ struct TcParams {
   uint8_t* hs;          // [T*k, I/32]
   float* yp;            // [T*k, H]
   int* gemm1_done;      // [chunks] GEMM1 epilogue-warp publications per chunk (persistent path)
+  int early_chunks;     // the chunk list was final before the preceding kernel ran: the
+                        // producer may read it, and issue weight tiles, before the wait
   int* status;
   unsigned long long timeout_ns;
   NextGemm1 next;       // next.stages == 0 unless this is a chained layer's last GEMM launch
@@ -393,8 +395,43 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tbase = *tmem_slot;
-  // everything above touches only this CTA's shared memory and TMEM; the
-  // routing outputs, activations and (for GEMM2) h come from earlier kernels
+  // Programmatic launch: the preceding kernel may still run.  Its outputs (the
+  // activation tiles and scales, h for GEMM2) are read only after the wait
+  // below; but in a single-GEMM launch whose routing finished before that
+  // kernel started (early_chunks: the preceding kernel is the activation step
+  // or a chain's combine, or GEMM1 for GEMM2), the chunk list is final, and
+  // the weights are inputs, so the producer already issues the weight tiles
+  // of its first fills (each
+  // stage's barrier expects both operands' bytes; the activation tiles follow
+  // after the wait) — the weight stream starts while the preceding kernel
+  // finishes, on the SMs it has left.
+  uint32_t prefilled = 0;  // (producer) fills whose weight tiles are in flight
+  if ((kMode == kModeGemm1 || kMode == kModeGemm2) && p.early_chunks && warp == 0) {
+    const int nch = p.meta[0];
+    const int items0 = nch * p.ph[0].m_tiles;
+    const int items_all = items0 + (kPhases > 1 ? nch * p.ph[kPhases - 1].m_tiles : 0);
+    const uint64_t pol_w0 = ptx::policy_evict_first();
+    int it = blockIdx.x, ks = 0;
+    while (prefilled < (uint32_t)C::kStages && it < items_all) {
+      const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
+      const TcPhase& ph = p.ph[phase];
+      const int local = it - (phase ? items0 : 0);
+      const int chunk = local / ph.m_tiles;
+      const int4 ch = p.chunks[chunk];
+      const int row0 = ch.x * ph.R + (local - chunk * ph.m_tiles) * ph.m_stride;
+      const uint32_t tx = C::kA * C::kTxA + (uint32_t)((ch.z + 15) & ~15) * 128;
+      uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
+      ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
+      ptx::tma_load_2d_warp(st, map_w(phase, 0), &full[prefilled], ks * kBlockK, row0, pol_w0);
+      ptx::tma_load_2d_warp(st + C::kATile, map_w(phase, 0), &full[prefilled], ks * kBlockK,
+                            row0 + ph.half, pol_w0);
+      ++prefilled;
+      if (++ks == ph.K / kBlockK) {
+        ks = 0;
+        it += gridDim.x;
+      }
+    }
+  }
   grid_dependency_wait();
 
   // whole-layer launch: this call's barrier tag, and for T <= 32 the routing
@@ -456,7 +493,6 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
   // (slot row, run of 32 blocks of 32), two units' loads in flight — while
   // those tiles stream in.  Other CTAs multiplying the same chunk write the
   // same bytes, so only this CTA's own writes must precede its copies.
-  uint32_t prefilled = 0;  // (producer) fills whose weight tiles are in flight
   if (route_in) {
     const int items0 = s_nchunks * m1, items_all = items0 + s_nchunks * m2;
     if (warp == 0) {

@@ -879,10 +879,16 @@ int enqueue_layer(const float* logits, const uint16_t* x, const uint8_t* w13, co
 // steps a5-a7: the two grouped GEMMs (one persistent launch or two)
 // `next` (a chained layer, MXFP8 mode): the last GEMM launch prefetches the
 // next layer's first GEMM1 weight tiles into L2
+// `chunks_before`: the chunk list was final before the kernel in front of the
+// GEMMs started (that kernel is the activation step or a combine), so a GEMM1
+// launch may start its weight stream before its dependency wait (GEMM2
+// launches always may; the both-GEMMs launch does not: the copy code cost its
+// stages more than the early start gained).
 int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                   const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
                   DeviceState* d, cudaStream_t stream, unsigned long long timeout_ns,
-                  const moe_opts* opts, Steps& st, const NextGemm1* next = nullptr) {
+                  const moe_opts* opts, Steps& st, const NextGemm1* next = nullptr,
+                  bool chunks_before = false) {
   const int TK = T * k;
   const bool wide = act == MOE_ACT_MXFP8 && T >= kWideMinTokens;
   const bool bf_wide = chunk_for(act, T) == kChunkBf16Wide;
@@ -902,6 +908,7 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
     bool persistent = path == MOE_PATH_GEMMS || path == MOE_PATH_PERSISTENT ||
                       (path == MOE_PATH_AUTO &&
                        auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_GEMMS);
+    p.early_chunks = chunks_before ? 1 : 0;
     if (persistent) {  // both GEMMs in one launch
       g2.dep_target = 4 * g1.m_tiles;  // four epilogue warps publish per tile pair
       if (opts && (opts->debug_flags & MOE_DEBUG_FORCE_DEP_TIMEOUT))
@@ -930,6 +937,7 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       if (launch(kModeGemm1, p) != cudaSuccess) return MOE_ERR_CUDA;
       p.ph[0] = g2;
       p.next = next ? *next : NextGemm1{};
+      p.early_chunks = 1;  // GEMM1 ran after the routing finished
       st.mark();
       if (launch(kModeGemm2, p) != cudaSuccess) return MOE_ERR_CUDA;
     }
@@ -1077,8 +1085,11 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
       return launch_status();
     }
   }
+  // (the small-block routing kernel writes the chunk list right before the
+  // GEMMs; the split path's activation step runs after it is final)
+  const bool chunks_before = !(T <= kSmallRouteTokens && !split);
   if ((rc = enqueue_gemms(act, gemm_path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream,
-                          timeout_ns, opts, st)))
+                          timeout_ns, opts, st, nullptr, chunks_before)))
     return rc;
   const int cap = d->sms * 8;
   st.mark();
@@ -1198,7 +1209,9 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
       (opts && (opts->debug_flags & MOE_DEBUG_SHORT_TIMEOUT)) ? 1000000ull : 2000000000ull;
   Steps st{opts, stream};
   const uint16_t* x = static_cast<const uint16_t*>(x_bf16);
-  if (T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING))) {
+  const bool small_route =
+      T <= kSmallRouteTokens && !(opts && (opts->debug_flags & MOE_DEBUG_SPLIT_ROUTING));
+  if (small_route) {
     if ((rc = enqueue_route_act_small_layers(logits, n, act, x, T, H, E, k, chunk_for(act, T),
                                              carve_chain(ws, C, 0), (int64_t)C.route_block, d,
                                              stream, st)))
@@ -1288,8 +1301,13 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
       nx.half = I;
       nx.stages = std::min(kChainPrefetchStages, H / 128);
     }
+    // every layer was routed before the chain's first GEMMs; the kernel in
+    // front of layer l's GEMMs is the previous layer's combine, or for layer 0
+    // the activation step (or the small-block routing, which writes the lists)
+    const bool chunks_before = l > 0 || !small_route;
     if ((rc = enqueue_gemms(act, path, w13[l], w13s[l], w2[l], w2s[l], T, H, I, E, k, w, d,
-                            stream, timeout_ns, opts, st, l + 1 < n ? &nx : nullptr)))
+                            stream, timeout_ns, opts, st, l + 1 < n ? &nx : nullptr,
+                            chunks_before)))
       return rc;
     const bool last = l == n - 1;
     const uint16_t* x_res = residual ? (l == 0 ? x : xb[l & 1]) : nullptr;

@@ -142,8 +142,10 @@ typedef struct {
    * MOE_DEBUG_SPLIT_ROUTING); persistent path — for T <= 32 one kernel, the
    * whole layer (with the router too for moe_mxfp4_forward_routed), else
    * route_topk, route_permute, act_quant, gemm1+gemm2+combine.
-   * moe_mxfp4_forward_routed otherwise puts router_gemm, router_reduce
-   * first. */
+   * moe_mxfp4_forward_routed otherwise puts router_gemm, router_sum first;
+   * router_sum adds the split partials into the logits and, where route_topk
+   * would follow (the split routing kernels), already takes the top-k, so
+   * route_topk is left out there. */
   cudaEvent_t* step_events;
   int n_step_events;
 } moe_opts;

@@ -323,13 +323,20 @@ __global__ void __launch_bounds__(kDenseThreads, 1)
       const uint32_t acc = tbase + lane_off + b * kNMax;
       const int row = it.mt * 128 + q * 32 + lane;
       float* dst = p.part + ((int64_t)it.ks * p.T + it.tok0) * p.M + row;
-      for (int n0 = 0; n0 < it.nvalid; n0 += 8) {
-        uint32_t v[8];
-        ptx::tmem_ld_x8(acc + n0, v);
+      // 32 tokens (accumulator columns) per wait: four loads in flight (the
+      // columns past the block exist and are not stored)
+      for (int n0 = 0; n0 < it.nvalid; n0 += 32) {
+        uint32_t v[4][8];
+#pragma unroll
+        for (int g = 0; g < 4; ++g)
+          if (n0 + 8 * g < kNMax) ptx::tmem_ld_x8(acc + n0 + 8 * g, v[g]);
         ptx::tmem_ld_wait();
 #pragma unroll
-        for (int t = 0; t < 8; ++t)
-          if (n0 + t < it.nvalid && row < p.M) dst[(int64_t)(n0 + t) * p.M] = __uint_as_float(v[t]);
+        for (int g = 0; g < 4; ++g)
+#pragma unroll
+          for (int t = 0; t < 8; ++t)
+            if (n0 + 8 * g + t < it.nvalid && row < p.M)
+              dst[(int64_t)(n0 + 8 * g + t) * p.M] = __uint_as_float(v[g][t]);
       }
       ptx::tc_fence_before();
       __syncwarp();

@@ -540,11 +540,12 @@ int grid_for(int64_t work, int per_block, int cap) {
 }
 
 // Router logits [T, E] = x [T, H] (bf16) times W_r^T (W_r [E, H] bf16): a
-// split-K GEMM into part[ks][t][e], then the partials summed in split order
-// into `logits`.  The first kernels of a call.
+// split-K GEMM into part[ks][t][e], then one kernel that sums the partials in
+// a fixed order into `logits` and, for k > 0, runs step (1) on them into
+// topk_idx / topk_w.  The first kernels of a call.
 int enqueue_router(const void* x_bf16, const void* w_router, int T, int H, int E, float* part,
                    float* logits, DeviceState* d, cudaStream_t s, unsigned long long timeout_ns,
-                   Steps& st) {
+                   Steps& st, int k = 0, int32_t* topk_idx = nullptr, float* topk_w = nullptr) {
   const DensePlan P =
       plan_dense(E, T, H / 64, kRouterNMax, d->sms, router_part_bytes(T, E));
   DenseParams dp{};
@@ -572,11 +573,23 @@ int enqueue_router(const void* x_bf16, const void* w_router, int T, int H, int E
           dp);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
+  if (P.k_splits > kTopkMaxSplits) return MOE_ERR_UNSUPPORTED_SHAPE;  // (kDenseMaxSplits)
   st.mark();
-  if (launch_pdl(splitk_reduce_f32_kernel, dim3(grid_for((int64_t)T * E, 32, d->sms * 8)),
-                 dim3(256), 0, s,
-                 (const float*)part, P.k_splits, T, E, logits) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  const int vec = E % 4 == 0 ? 4 : 1;
+  const dim3 grid(std::min(T, d->sms * 8));
+  const dim3 block(std::min(kTopkThreads, (kTopkGroups * (E / vec) + 31) / 32 * 32));
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, grid, block, 0, s, (const float*)part, P.k_splits, T, E, k, logits,
+                      topk_idx, topk_w, d->status);
+  };
+  const cudaError_t e =
+      vec == 4 ? (E <= 128   ? go(splitk_topk_kernel<4, 4>)
+                  : E <= 384 ? go(splitk_topk_kernel<12, 4>)
+                             : go(splitk_topk_kernel<32, 4>))
+               : (E <= 128   ? go(splitk_topk_kernel<4, 1>)
+                  : E <= 384 ? go(splitk_topk_kernel<12, 1>)
+                             : go(splitk_topk_kernel<32, 1>));
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
   return MOE_OK;
 }
@@ -603,10 +616,12 @@ int enqueue_topk(const float* logits, bool first, int T, int E, int k, int32_t* 
   return MOE_OK;
 }
 
-// Routing steps (1)-(4) into w; `first`: the top-k is the call's first kernel
+// Routing steps (1)-(4) into w; `first`: the top-k is the call's first kernel;
+// `topk_done`: step (1) already ran (the router's last kernel), only (2)-(4)
 int enqueue_route(const float* logits, bool first, int T, int E, int k, int chunk_max,
-                  const Work& w, DeviceState* d, cudaStream_t s, Steps& st) {
-  int rc = enqueue_topk(logits, first, T, E, k, w.topk_idx, w.topk_w, d, s, st);
+                  const Work& w, DeviceState* d, cudaStream_t s, Steps& st,
+                  bool topk_done = false) {
+  int rc = topk_done ? MOE_OK : enqueue_topk(logits, first, T, E, k, w.topk_idx, w.topk_w, d, s, st);
   if (rc) return rc;
   st.mark();
   const size_t smem = (size_t)(35 * E + 35) * sizeof(int);
@@ -1066,13 +1081,17 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
       return launch_status();
     }
   }
+  // the router's last kernel also runs step (1) when the split routing
+  // kernels follow (the small-block kernel routes from the logits itself)
+  const bool small_route = T <= kSmallRouteTokens && !split;
   if (routed && (rc = enqueue_router(x_bf16, w_router, T, H, E, w.part, w.rlogits, d, stream,
-                                     timeout_ns, st)))
+                                     timeout_ns, st, small_route ? 0 : k, w.topk_idx,
+                                     w.topk_w)))
     return rc;
-  if (T <= kSmallRouteTokens && !split) {
+  if (small_route) {
     if ((rc = enqueue_route_act_small(lg, !routed, act, x, T, H, E, k, chunk, w, d, stream, st)))
       return rc;
-  } else if ((rc = enqueue_route(lg, !routed, T, E, k, chunk, w, d, stream, st)) ||
+  } else if ((rc = enqueue_route(lg, !routed, T, E, k, chunk, w, d, stream, st, routed)) ||
              (rc = enqueue_act(act, x, w, T, H, k, d, stream, st))) {
     return rc;
   }
@@ -1087,7 +1106,7 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
   }
   // (the small-block routing kernel writes the chunk list right before the
   // GEMMs; the split path's activation step runs after it is final)
-  const bool chunks_before = !(T <= kSmallRouteTokens && !split);
+  const bool chunks_before = !small_route;
   if ((rc = enqueue_gemms(act, gemm_path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream,
                           timeout_ns, opts, st, nullptr, chunks_before)))
     return rc;
@@ -1487,10 +1506,8 @@ int moe_router_topk(const void* x_bf16, const void* w_router_bf16, int T, int H,
   float* lg = logits_out ? logits_out : reinterpret_cast<float*>(static_cast<uint8_t*>(ws) +
                                                                    part_bytes);
   Steps st{nullptr, stream};
-  if ((rc = enqueue_router(x_bf16, w_router_bf16, T, H, E, part, lg, d, stream, 2000000000ull,
-                           st)))
-    return rc;
-  return enqueue_topk(lg, false, T, E, k, topk_idx, topk_w, d, stream, st);
+  return enqueue_router(x_bf16, w_router_bf16, T, H, E, part, lg, d, stream, 2000000000ull, st, k,
+                        topk_idx, topk_w);
 }
 
 int mxfp8_quantize(const float* w, int64_t rows, int64_t K, uint8_t* out_e4m3, uint8_t* out_e8m0,

@@ -43,12 +43,12 @@ __device__ __forceinline__ uint32_t warp_redux_min(uint32_t v) {
 // equal ones: the warp's largest key (one reduction), then the lowest index
 // among the lanes whose own best has that key (a second one).
 // kL2: load the logits from L2 only (written by other CTAs of the same launch)
+// `l`: token t's E logits (global or shared memory)
 template <int MAXPL, bool kL2 = false>
-__device__ __forceinline__ void route_topk_token(const float* __restrict__ logits, int t, int E,
-                                                 int k, int32_t* __restrict__ idx,
-                                                 float* __restrict__ w, int* status) {
+__device__ __forceinline__ void route_topk_row(const float* __restrict__ l, int t, int E, int k,
+                                               int32_t* __restrict__ idx, float* __restrict__ w,
+                                               int* status) {
   const int lane = threadIdx.x & 31;
-  const float* l = logits + (size_t)t * E;
   uint32_t key[MAXPL];
 #pragma unroll
   for (int i = 0; i < MAXPL; ++i) {
@@ -90,6 +90,83 @@ __device__ __forceinline__ void route_topk_token(const float* __restrict__ logit
   if (lane < k) {
     idx[(size_t)t * k + lane] = my_e;
     w[(size_t)t * k + lane] = ex / s;
+  }
+}
+
+template <int MAXPL, bool kL2 = false>
+__device__ __forceinline__ void route_topk_token(const float* __restrict__ logits, int t, int E,
+                                                 int k, int32_t* __restrict__ idx,
+                                                 float* __restrict__ w, int* status) {
+  route_topk_row<MAXPL, kL2>(logits + (size_t)t * E, t, E, k, idx, w, status);
+}
+
+// The router's split-K partials part[ks][t][e] summed into logits, and step
+// (1) on them, in one kernel: a CTA per token.  Each thread takes kVec
+// consecutive experts (4 when E % 4 == 0, else 1) of one of kTopkGroups split
+// groups (splits g, g + 8, ...): its loads (one per split) are all issued
+// before they are added, then the groups' sums are added in group order
+// through shared memory — a fixed order, so the logits are deterministic;
+// `logits` (may be null) receives them.  Then one warp takes the top-k from
+// shared memory.  k == 0: the logits alone.  k_splits <= kTopkMaxSplits.
+constexpr int kTopkGroups = 8, kTopkLoads = 8;
+constexpr int kTopkMaxSplits = kTopkGroups * kTopkLoads;
+constexpr int kTopkThreads = 1024;
+template <int MAXPL, int kVec>
+__global__ void __launch_bounds__(kTopkThreads) splitk_topk_kernel(
+    const float* __restrict__ part, int k_splits, int T, int E, int k, float* __restrict__ logits,
+    int32_t* __restrict__ idx, float* __restrict__ w, int* status) {
+  static_assert(kVec == 1 || kVec == 4, "experts per thread");
+  __shared__ __align__(16) float s_grp[kTopkGroups][32 * MAXPL];
+  __shared__ __align__(16) float s_l[32 * MAXPL];
+  grid_dependency_wait();
+  grid_launch_dependents();
+  const int64_t n = (int64_t)T * E;  // floats per split
+  const int EV = E / kVec;
+  auto load = [&](const float* p, float (&r)[kVec]) {
+    if (kVec == 4) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(p));
+      r[0] = q.x;
+      r[kVec > 1 ? 1 : 0] = q.y;
+      r[kVec > 2 ? 2 : 0] = q.z;
+      r[kVec > 3 ? 3 : 0] = q.w;
+    } else {
+      r[0] = __ldcg(p);
+    }
+  };
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int u = threadIdx.x; u < kTopkGroups * EV; u += blockDim.x) {
+      const int g = u / EV, e0 = (u - g * EV) * kVec;
+      const float* src = part + (int64_t)t * E + e0;
+      float v[kTopkLoads][kVec];
+#pragma unroll
+      for (int i = 0; i < kTopkLoads; ++i) {
+        const int ks = g + kTopkGroups * i;
+        if (ks < k_splits) {
+          load(src + ks * n, v[i]);
+        } else {
+#pragma unroll
+          for (int c = 0; c < kVec; ++c) v[i][c] = 0.0f;
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < kVec; ++c) {
+        float a = v[0][c];
+#pragma unroll
+        for (int i = 1; i < kTopkLoads; ++i) a += v[i][c];
+        s_grp[g][e0 + c] = a;
+      }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float a = s_grp[0][e];
+#pragma unroll
+      for (int g = 1; g < kTopkGroups; ++g) a += s_grp[g][e];
+      s_l[e] = a;
+      if (logits) logits[(int64_t)t * E + e] = a;
+    }
+    __syncthreads();
+    if (k > 0 && threadIdx.x < 32) route_topk_row<MAXPL>(s_l, t, E, k, idx, w, status);
+    __syncthreads();
   }
 }
 

@@ -101,10 +101,13 @@ def test_routed_layer_matches_oracle(O, name):
     assert f <= 1e-2 and m <= 4e-2
 
 
-def test_routed_layer_equals_layer_on_its_logits():
+@pytest.mark.parametrize("L", [LY.LAYERS["full_t8"], LY.Layer("routed_t64", 2048, 1024, 64, 8, 64, 7),
+                               LY.Layer("routed_t256", 6144, 2048, 384, 8, 256, 3)],
+                         ids=["full_t8", "mid_t64", "full_t256"])
+def test_routed_layer_equals_layer_on_its_logits(L):
     """The fused router changes nothing but where the logits come from: the layer fed the
-    router's own fp32 logits gives the same bits."""
-    L = LY.LAYERS["full_t8"]
+    router's own fp32 logits gives the same bits (above 32 tokens the router's last kernel
+    also takes the top-k the layer would)."""
     inp = device_layer(L)
     w_r = dev(S.router_bf16(L.seed, L.E, L.H))
     idx = torch.empty((L.T, L.k), dtype=torch.int32, device="cuda")

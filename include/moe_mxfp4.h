@@ -235,7 +235,7 @@ size_t moe_mxfp4_workspace_size_chain(int n_layers, int T, int H, int I, int E, 
 /*
  * moe_mxfp4_select_path — the path MOE_PATH_AUTO takes for this shape on the
  * current device: MOE_PATH_GEMMS when a bound on the GEMM work items
- * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is at most 90 per SM,
+ * (min(T*k, E) + T*k / chunk) * (I/128 + ceil(H/256)) is at most 110 per SM,
  * else MOE_PATH_MULTI (always MOE_PATH_MULTI in the bf16 mode).  One launch
  * for both GEMMs saves the gap between them and fills GEMM1's last wave with
  * GEMM2 items; with many items per SM two launches stream weights faster.  The automatic choice never takes

@@ -27,19 +27,6 @@ constexpr int kChunkWide = MOE_CHUNK_WIDE;
 #define MOE_WIDE_MIN_TOKENS 512
 #endif
 constexpr int kWideMinTokens = MOE_WIDE_MIN_TOKENS;
-// automatic path choice: one persistent launch for both GEMMs when the bound
-// on GEMM work items per SM lies in [kPersistentMinItemsPerSm,
-// kPersistentItemsPerSm] (measured: one launch is faster up to ~70 items per
-// SM, two launches from ~110 on, where GEMM1's last wave is a small share and
-// the single launch interleaves two weight streams)
-#ifndef MOE_PERSISTENT_ITEMS_PER_SM
-#define MOE_PERSISTENT_ITEMS_PER_SM 90
-#endif
-#ifndef MOE_PERSISTENT_MIN_ITEMS_PER_SM
-#define MOE_PERSISTENT_MIN_ITEMS_PER_SM 0
-#endif
-constexpr int kPersistentItemsPerSm = MOE_PERSISTENT_ITEMS_PER_SM;
-constexpr int kPersistentMinItemsPerSm = MOE_PERSISTENT_MIN_ITEMS_PER_SM;
 constexpr int kStatusTimeout = MOE_ERR_DEVICE_TIMEOUT;
 constexpr int kStatusFault = MOE_ERR_DEVICE_FAULT;
 

@@ -397,16 +397,17 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
   const uint32_t tbase = *tmem_slot;
   // Programmatic launch: the preceding kernel may still run.  Its outputs (the
   // activation tiles and scales, h for GEMM2) are read only after the wait
-  // below; but in a single-GEMM launch whose routing finished before that
-  // kernel started (early_chunks: the preceding kernel is the activation step
-  // or a chain's combine, or GEMM1 for GEMM2), the chunk list is final, and
-  // the weights are inputs, so the producer already issues the weight tiles
-  // of its first fills (each
+  // below; but in a single-GEMM launch with narrow chunks whose routing
+  // finished before that kernel started (early_chunks: the preceding kernel is
+  // the activation step or a chain's combine, or GEMM1 for GEMM2), the chunk
+  // list is final, and the weights are inputs, so the producer already issues
+  // the weight tiles of its first fills (each
   // stage's barrier expects both operands' bytes; the activation tiles follow
   // after the wait) — the weight stream starts while the preceding kernel
   // finishes, on the SMs it has left.
   uint32_t prefilled = 0;  // (producer) fills whose weight tiles are in flight
-  if ((kMode == kModeGemm1 || kMode == kModeGemm2) && p.early_chunks && warp == 0) {
+  if ((kMode == kModeGemm1 || kMode == kModeGemm2) && kNMax == kChunkNarrow && p.early_chunks &&
+      warp == 0) {
     const int nch = p.meta[0];
     const int items0 = nch * p.ph[0].m_tiles;
     const int items_all = items0 + (kPhases > 1 ? nch * p.ph[kPhases - 1].m_tiles : 0);

@@ -739,21 +739,25 @@ int enqueue_route_act_small_layers(const float* const* logits, int n, int act, c
   return MOE_OK;
 }
 
-// The path MOE_PATH_AUTO takes.  One launch removes the gap and the tail
-// between the two GEMMs, which pays when each SM gets a handful of work items;
-// with many items per SM the two specialised launches stream weights faster,
-// and with very few the cooperative launch's fixed cost outweighs the gain.
-// The bound on work items uses at most min(T*k, E) touched experts.
+// The path MOE_PATH_AUTO takes: one launch for both GEMMs when the bound on
+// GEMM work items per SM is at most kPersistentItemsPerSm, else two.  One
+// launch removes the gap and the tail between the GEMMs and fills GEMM1's last
+// wave with GEMM2 items; with many items per SM the two specialised launches
+// stream weights faster (measured, µs, L2 emptied: full per-expert shape at
+// T = 64, 108 items per SM: one launch 913.5, two 919.8; at T = 256, 121 per
+// SM: 1265.6 against 1258.7).  The bound uses at most min(T*k, E) touched
+// experts.
+#ifndef MOE_PERSISTENT_ITEMS_PER_SM
+#define MOE_PERSISTENT_ITEMS_PER_SM 110
+#endif
+constexpr int kPersistentItemsPerSm = MOE_PERSISTENT_ITEMS_PER_SM;
 int auto_path(int T, int H, int I, int E, int k, int act, int sms) {
   if (act != MOE_ACT_MXFP8) return MOE_PATH_MULTI;  // the bf16 GEMMs are two launches
   const int64_t TK = (int64_t)T * k;
   const bool wide = T >= kWideMinTokens;
   const int64_t chunk_bound = std::min<int64_t>(TK, E) + TK / (wide ? kChunkWide : kChunkNarrow);
   const int64_t item_bound = chunk_bound * (I / 128 + (H + 255) / 256);
-  return item_bound >= (int64_t)kPersistentMinItemsPerSm * sms &&
-                 item_bound <= (int64_t)kPersistentItemsPerSm * sms
-             ? MOE_PATH_GEMMS
-             : MOE_PATH_MULTI;
+  return item_bound <= (int64_t)kPersistentItemsPerSm * sms ? MOE_PATH_GEMMS : MOE_PATH_MULTI;
 }
 
 // step a4: x rows into slot order, MXFP8-quantised or copied as bf16; each
@@ -1105,8 +1109,9 @@ int forward_impl(const void* x_bf16, const float* logits, const uint8_t* w13, co
     }
   }
   // (the small-block routing kernel writes the chunk list right before the
-  // GEMMs; the split path's activation step runs after it is final)
-  const bool chunks_before = !small_route;
+  // GEMMs; the split path's activation step runs after it is final; the GEMM
+  // kernels of wide chunks, T >= kWideMinTokens, have no early copies)
+  const bool chunks_before = !small_route && T < kWideMinTokens;
   if ((rc = enqueue_gemms(act, gemm_path, w13, w13s, w2, w2s, T, H, I, E, k, w, d, stream,
                           timeout_ns, opts, st, nullptr, chunks_before)))
     return rc;
@@ -1323,7 +1328,7 @@ int chain_impl(int n, const void* x_bf16, const float* const* logits,
     // every layer was routed before the chain's first GEMMs; the kernel in
     // front of layer l's GEMMs is the previous layer's combine, or for layer 0
     // the activation step (or the small-block routing, which writes the lists)
-    const bool chunks_before = l > 0 || !small_route;
+    const bool chunks_before = (l > 0 || !small_route) && T < kWideMinTokens;
     if ((rc = enqueue_gemms(act, path, w13[l], w13s[l], w2[l], w2s[l], T, H, I, E, k, w, d,
                             stream, timeout_ns, opts, st, l + 1 < n ? &nx : nullptr,
                             chunks_before)))

@@ -254,7 +254,7 @@ def test_persistent_equals_multi_kernel_bitwise(name):
 
 
 def test_auto_path_choice():
-    """One launch for both GEMMs up to 90 GEMM work items per SM, two launches above."""
+    """One launch for both GEMMs up to 110 GEMM work items per SM, two launches above."""
     sel = moe.moe_mxfp4_select_path
     assert sel(8, 2048, 1024, 64, 8) == moe.MOE_PATH_GEMMS           # 8 tokens, mid shape
     assert sel(32, 2048, 1024, 64, 8) == moe.MOE_PATH_GEMMS          # 32 tokens, mid shape
@@ -262,7 +262,8 @@ def test_auto_path_choice():
     assert sel(16, 256, 128, 8, 2) == moe.MOE_PATH_GEMMS
     assert sel(8, 6144, 2048, 384, 8) == moe.MOE_PATH_GEMMS          # full shape, 8 tokens
     assert sel(32, 6144, 2048, 384, 8) == moe.MOE_PATH_GEMMS         # 71 items per SM
-    assert sel(64, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI         # 108 items per SM
+    assert sel(64, 6144, 2048, 384, 8) == moe.MOE_PATH_GEMMS         # 108 items per SM
+    assert sel(128, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # 112 items per SM
     assert sel(256, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI        # full shape, 256 tokens
     assert sel(1024, 6144, 2048, 384, 8) == moe.MOE_PATH_MULTI
     assert sel(8, 2048, 1024, 64, 8, moe.MOE_ACT_BF16) == moe.MOE_PATH_MULTI

@@ -380,36 +380,4 @@ __global__ void __launch_bounds__(256) splitk_reduce_bf16_kernel(const float* __
   }
 }
 
-// out[t, m] = sum over ks of part[ks][t][m] (fp32), over the flat T*M
-// elements.  A block of 8 warps takes 32 elements (a lane each): warp w adds
-// the splits w, w+8, w+16, ... in that order, then warp 0 adds the 8 warp
-// sums in warp order — a fixed order (deterministic run to run) whose loads
-// are all in flight at once instead of one long chain per thread.
-__global__ void __launch_bounds__(256) splitk_reduce_f32_kernel(const float* __restrict__ part,
-                                                                int k_splits, int T, int M,
-                                                                float* __restrict__ out) {
-  __shared__ float red[8][32];
-  grid_dependency_wait();
-  grid_launch_dependents();
-  const int64_t n = (int64_t)T * M;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int64_t base = (int64_t)blockIdx.x * 32; base < n; base += (int64_t)gridDim.x * 32) {
-    const int64_t i = base + lane;
-    float a = 0.0f;
-    if (i < n) {
-#pragma unroll 4
-      for (int ks = warp; ks < k_splits; ks += 8) a += part[ks * n + i];
-    }
-    red[warp][lane] = a;
-    __syncthreads();
-    if (warp == 0) {
-      float sum = red[0][lane];
-#pragma unroll
-      for (int w = 1; w < 8; ++w) sum += red[w][lane];
-      if (i < n) out[i] = sum;
-    }
-    __syncthreads();
-  }
-}
-
 }  // namespace moe

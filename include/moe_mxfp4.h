@@ -286,7 +286,10 @@ size_t moe_mxfp4_workspace_size_padded(int T, int H, int I, int E, int k, int ac
  *                                                 SIZE_MAX otherwise)
  *  x_stream[2] [T, H] bf16                        SIZE_MAX here (chain only)
  *  total                                          moe_mxfp4_workspace_size
- * The layout depends only on the arguments.  Returns MOE_OK or an error for
+ * The layout depends only on the arguments.  A layer that runs on zero-padded
+ * copies (H or I not a multiple of 128; see moe_mxfp4_forward) has the
+ * padded shape's arrays at these offsets: rows of Hp = H rounded up to 128
+ * (xq, xs, yp) and Ip (hq, hs) elements.  Returns MOE_OK or an error for
  * invalid arguments.  No counterpart in the papers: a support call for
  * checking the layer's steps one by one.
  */

@@ -716,13 +716,15 @@ int enqueue_route_act_small_layers(const float* const* logits, int n, int act, c
                                    int64_t stride, DeviceState* d, cudaStream_t s, Steps& st) {
   LayerLogits lg{};
   for (int l = 0; l < n; ++l) lg.p[l] = logits[l];
-  const dim3 grid(small_route_grid(T, H, d->sms), n);
+  // layer 0's CTAs, then one CTA per later layer
+  const int g0 = small_route_grid(T, H, d->sms);
+  const dim3 grid(g0 + n - 1);
   const size_t smem = small_route_smem(T, E, k, w0.max_chunks).total;
   st.mark();
   auto go = [&](auto kernel) {
     kernel<<<grid, 1024, smem, s>>>(lg, x, T, H, E, k, w0.max_chunks, chunk_max, w0.topk_idx,
                                     w0.topk_w, w0.cnt, w0.off, w0.perm, w0.pos, w0.chunks,
-                                    w0.meta, w0.done, w0.xq, w0.xs, stride, d->status);
+                                    w0.meta, w0.done, w0.xq, w0.xs, stride, g0, d->status);
     return cudaGetLastError();
   };
   cudaError_t e;

@@ -113,9 +113,10 @@ struct SmallActUnit {
   }
 };
 
-// The routing of one block of T <= 32 tokens by one CTA (every CTA of the
-// grid's x dimension that calls it computes the same arrays); `publish`: this
-// CTA writes them out.  x == nullptr: no step a4.
+// The routing of one block of T <= 32 tokens by one CTA (every CTA that calls
+// it for the block computes the same arrays); `publish`: this CTA writes them
+// out.  x == nullptr: no step a4; else CTA `cta` of the `ncta` that share the
+// block's a4 units.
 template <int MAXPL, bool kMxfp8>
 __device__ __forceinline__ void route_small_block(
     const float* __restrict__ logits, const uint16_t* __restrict__ x, int T, int H, int E, int k,
@@ -123,7 +124,7 @@ __device__ __forceinline__ void route_small_block(
     float* __restrict__ topk_w, int32_t* __restrict__ cnt, int32_t* __restrict__ off,
     int32_t* __restrict__ perm, int32_t* __restrict__ pos, int4* __restrict__ chunks,
     int32_t* __restrict__ meta, int32_t* __restrict__ done, uint8_t* __restrict__ q,
-    uint8_t* __restrict__ s, int* status) {
+    uint8_t* __restrict__ s, int* status, int cta, int ncta) {
   extern __shared__ __align__(16) uint8_t sm[];
   const SmallRouteSmem L = small_route_smem(T, E, k, max_chunks);
   int* s_warp = reinterpret_cast<int*>(sm);  // 32 + 2 ints of block-scan scratch
@@ -141,7 +142,7 @@ __device__ __forceinline__ void route_small_block(
   const int64_t segs = (H / 32 + 31) / 32, units = (int64_t)T * segs;
   // warps T..31 of every CTA take the first token-major units of a4 while
   // warps 0..T-1 route; the rest of the units follow the routing
-  const int64_t early = (int64_t)gridDim.x * (32 - T);
+  const int64_t early = (int64_t)ncta * (32 - T);
 
   SmallActUnit<kMxfp8> held;
   held.live = false;
@@ -149,7 +150,7 @@ __device__ __forceinline__ void route_small_block(
     // (1) top-k + softmax: warp t takes token t
     route_topk_token<MAXPL>(logits, warp, E, k, s_idx, s_gate, status);
   } else if (x) {
-    const int64_t u = blockIdx.x + (int64_t)gridDim.x * (warp - T);
+    const int64_t u = cta + (int64_t)ncta * (warp - T);
     if (u < units) held.load(x, u, segs, H);
   }
   for (int e = tid; e < E; e += 1024) s_cnt[e] = 0;
@@ -209,8 +210,7 @@ __device__ __forceinline__ void route_small_block(
   if (!x) return;
   // a4: the held unit, then the units past the early ones (a warp each)
   held.store(s_pos, k, TK, H, q, s, status);
-  for (int64_t u = early + (int64_t)blockIdx.x * 32 + warp; u < units;
-       u += (int64_t)gridDim.x * 32) {
+  for (int64_t u = early + (int64_t)cta * 32 + warp; u < units; u += (int64_t)ncta * 32) {
     SmallActUnit<kMxfp8> a;
     a.load(x, u, segs, H);
     a.store(s_pos, k, TK, H, q, s, status);
@@ -229,22 +229,23 @@ __global__ void __launch_bounds__(1024) route_act_small_kernel(
   grid_launch_dependents();
   route_small_block<MAXPL, kMxfp8>(logits, x, T, H, E, k, max_chunks, chunk_max,
                                    blockIdx.x == 0, topk_idx, topk_w, cnt, off, perm, pos,
-                                   chunks, meta, done, q, s, status);
+                                   chunks, meta, done, q, s, status, blockIdx.x, gridDim.x);
 }
 
-// A chain of layers over one small block: blockIdx.y = layer, whose routing
-// arrays start `stride` bytes after the previous layer's.  Layer 0 as in
-// route_act_small_kernel (every CTA routes it, CTA 0 publishes, all CTAs run
-// its step a4 into q / s); every later layer is routed and published by its
-// CTA x = 0 alone (its activation rows come from the previous layer's combine).
+// A chain of layers over one small block, on a 1-D grid of g0 + n - 1 CTAs:
+// CTAs 0..g0-1 route layer 0 as route_act_small_kernel does (every one routes
+// it, CTA 0 publishes, all run its step a4 into q / s); CTA g0 + l - 1 routes
+// and publishes layer l >= 1 alone (its activation rows come from the
+// previous layer's combine).  Layer l's routing arrays start l * stride bytes
+// after layer 0's.
 template <int MAXPL, bool kMxfp8>
 __global__ void __launch_bounds__(1024) route_act_small_layers_kernel(
     const __grid_constant__ LayerLogits lg, const uint16_t* __restrict__ x, int T, int H, int E,
     int k, int max_chunks, int chunk_max, int32_t* topk_idx0, float* topk_w0, int32_t* cnt0,
     int32_t* off0, int32_t* perm0, int32_t* pos0, int4* chunks0, int32_t* meta0, int32_t* done0,
-    uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t stride, int* status) {
-  const int l = blockIdx.y;
-  if (l > 0 && blockIdx.x > 0) return;
+    uint8_t* __restrict__ q, uint8_t* __restrict__ s, int64_t stride, int g0, int* status) {
+  const int b = (int)blockIdx.x;
+  const int l = b < g0 ? 0 : b - g0 + 1;
   grid_dependency_wait();
   grid_launch_dependents();
   const int64_t o = (int64_t)l * stride;
@@ -253,9 +254,10 @@ __global__ void __launch_bounds__(1024) route_act_small_layers_kernel(
     return reinterpret_cast<P>(reinterpret_cast<char*>(p) + o);
   };
   route_small_block<MAXPL, kMxfp8>(lg.p[l], l == 0 ? x : nullptr, T, H, E, k, max_chunks,
-                                   chunk_max, blockIdx.x == 0, at(topk_idx0), at(topk_w0),
+                                   chunk_max, b == 0 || l > 0, at(topk_idx0), at(topk_w0),
                                    at(cnt0), at(off0), at(perm0), at(pos0), at(chunks0), at(meta0),
-                                   done0 ? at(done0) : nullptr, q, s, status);
+                                   done0 ? at(done0) : nullptr, q, s, status, l == 0 ? b : 0,
+                                   l == 0 ? g0 : 1);
 }
 
 }  // namespace moe

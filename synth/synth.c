@@ -17,26 +17,24 @@
 
 #include "synth_core.h"
 
-static float z_as_float(int32_t num) {
-  /* num is an integer of magnitude <= 393210 < 2^24: exact in fp32, and the
-   * power-of-two scaling keeps it exact */
-  return (float)num * 0x1p-16f;
-}
-
 uint64_t synth_splitmix_out(uint64_t s, uint64_t n) { return synth_splitmix(s, n); }
 
-int32_t synth_z_numerator(uint64_t seed, uint32_t tensor_id, uint64_t i) {
-  return synth_z_num(synth_key(seed, tensor_id), i);
+/* normal(key(seed, id), i): one draw, for tests */
+float synth_std_normal(uint64_t seed, uint32_t tensor_id, uint64_t i) {
+  return synth_normal(synth_key(seed, tensor_id), i);
 }
 
-/* out[j] = sigma * z(key(seed, id), start + j), fp32, j in [0, n) */
+/* the generator's logarithm, for tests */
+float synth_ln_f32(float s) { return synth_ln(s); }
+
+/* out[j] = sigma * normal(key(seed, id), start + j), fp32, j in [0, n) */
 void synth_fill_normal_f32(uint64_t seed, uint32_t tensor_id, uint64_t start,
                            uint64_t n, float sigma, float* out) {
   const uint64_t key = synth_key(seed, tensor_id);
   int64_t nn = (int64_t)n;
 #pragma omp parallel for schedule(static)
   for (int64_t j = 0; j < nn; ++j) {
-    float z = z_as_float(synth_z_num(key, start + (uint64_t)j));
+    float z = synth_normal(key, start + (uint64_t)j);
     volatile float p = sigma * z; /* one RN multiply, never fused */
     out[j] = p;
   }
@@ -50,36 +48,36 @@ static uint16_t f32_to_bf16_rne(float f) {
   return (uint16_t)(u >> 16);
 }
 
-/* out[j] = bf16_RNE(sigma * z(key(seed, id), start + j)), j in [0, n) */
+/* out[j] = bf16_RNE(sigma * normal(key(seed, id), start + j)), j in [0, n) */
 void synth_fill_bf16(uint64_t seed, uint32_t tensor_id, uint64_t start, uint64_t n,
                      float sigma, uint16_t* out) {
   const uint64_t key = synth_key(seed, tensor_id);
   int64_t nn = (int64_t)n;
 #pragma omp parallel for schedule(static)
   for (int64_t j = 0; j < nn; ++j) {
-    volatile float p = sigma * z_as_float(synth_z_num(key, start + (uint64_t)j));
+    volatile float p = sigma * synth_normal(key, start + (uint64_t)j);
     out[j] = f32_to_bf16_rne(p);
   }
 }
 
-/* x[t, h] = bf16_RNE(z(key(seed, X), t*H + h)), unit variance */
+/* x[t, h] = bf16_RNE(normal(key(seed, X), t*H + h)) */
 void synth_fill_x_bf16(uint64_t seed, int64_t T, int64_t H, uint16_t* out) {
   const uint64_t key = synth_key(seed, SYNTH_ID_X);
   int64_t n = T * H;
 #pragma omp parallel for schedule(static)
   for (int64_t j = 0; j < n; ++j) {
-    out[j] = f32_to_bf16_rne(z_as_float(synth_z_num(key, (uint64_t)j)));
+    out[j] = f32_to_bf16_rne(synth_normal(key, (uint64_t)j));
   }
 }
 
-/* logits[t, e] = z(key(seed, LOGITS), t*E + e); with zipf_bias != 0 a per-expert
+/* logits[t, e] = normal(key(seed, LOGITS), t*E + e); with zipf_bias != 0 a per-expert
  * bias 3*ln(1/rank), rank = e + 1, is added in double and the sum rounded to
  * fp32 (expert 0 is the most popular). */
 void synth_fill_logits(uint64_t seed, int64_t T, int64_t E, int zipf_bias, float* out) {
   const uint64_t key = synth_key(seed, SYNTH_ID_LOGITS);
   for (int64_t t = 0; t < T; ++t) {
     for (int64_t e = 0; e < E; ++e) {
-      float z = z_as_float(synth_z_num(key, (uint64_t)(t * E + e)));
+      float z = synth_normal(key, (uint64_t)(t * E + e));
       if (zipf_bias) {
         double b = 3.0 * log(1.0 / (double)(e + 1));
         out[t * E + e] = (float)((double)z + b);
@@ -119,12 +117,12 @@ void synth_fill_verify(uint64_t seed, int64_t S, int g, int64_t V, float sigma_t
     const int64_t s = row / (g + 1), i = row % (g + 1);
     double* z = (double*)malloc(sizeof(double) * (size_t)V);
     for (int64_t v = 0; v < V; ++v)
-      z[v] = (double)sigma_t * (double)z_as_float(synth_z_num(kz, (uint64_t)(row * V + v)));
+      z[v] = (double)sigma_t * (double)synth_normal(kz, (uint64_t)(row * V + v));
     softmax_row_f32(z, V, p + row * V);
     if (i < g) {
       const int64_t qrow = s * g + i;
       for (int64_t v = 0; v < V; ++v)
-        z[v] += (double)sigma_n * (double)z_as_float(synth_z_num(kn, (uint64_t)(qrow * V + v)));
+        z[v] += (double)sigma_n * (double)synth_normal(kn, (uint64_t)(qrow * V + v));
       float* qr = q + qrow * V;
       softmax_row_f32(z, V, qr);
       const double r = (double)(synth_splitmix(kd, (uint64_t)qrow) >> 11) * 0x1p-53;

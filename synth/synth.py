@@ -1,15 +1,16 @@
 """Seeded synthetic inputs for the MXFP4 MoE layer (test and benchmark infrastructure).
 
-The generator is counter-based and integer-only (definitions in ``synth_core.h``), so the
-host library (``libsynth.so``) and the device library (``libsynth_dev.so``) produce the same
-bits.  It holds none of the layer's arithmetic; packing the fp32 weights to MXFP4 is done by
+The generator is counter-based (definitions in ``synth_core.h``): SplitMix64 streams, and
+standard normal draws by Marsaglia's polar method in a fixed sequence of correctly rounded
+fp32 operations, so the host library (``libsynth.so``) and the device library
+(``libsynth_dev.so``) produce the same bits.  It holds none of the layer's arithmetic; packing the fp32 weights to MXFP4 is done by
 whichever side (the oracle or the CUDA library) is under test.
 
 Workload recipe (shapes and value distributions of the layers this repository measures):
-  x       [T, H]  bf16 RNE of a unit-variance draw           (tensor id 0)
-  logits  [T, E]  fp32 unit-variance draw, optional Zipf bias (tensor id 1)
-  w13     [E, 2I, H] fp32 draw with sigma 0.02 before packing (tensor id 2)
-  w2      [E, H, I]  fp32 draw with sigma 0.02 before packing (tensor id 3)
+  x       [T, H]  bf16 RNE of an N(0, 1) draw                (tensor id 0)
+  logits  [T, E]  fp32 N(0, 1) draw, optional Zipf bias      (tensor id 1)
+  w13     [E, 2I, H] fp32 N(0, 0.02^2) draw before packing   (tensor id 2)
+  w2      [E, H, I]  fp32 N(0, 0.02^2) draw before packing   (tensor id 3)
 """
 from __future__ import annotations
 
@@ -53,8 +54,10 @@ def _host_lib():
         u64, u32, i64 = ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int64
         lib.synth_splitmix_out.restype = u64
         lib.synth_splitmix_out.argtypes = [u64, u64]
-        lib.synth_z_numerator.restype = ctypes.c_int32
-        lib.synth_z_numerator.argtypes = [u64, u32, u64]
+        lib.synth_std_normal.restype = ctypes.c_float
+        lib.synth_std_normal.argtypes = [u64, u32, u64]
+        lib.synth_ln_f32.restype = ctypes.c_float
+        lib.synth_ln_f32.argtypes = [ctypes.c_float]
         lib.synth_fill_normal_f32.restype = None
         lib.synth_fill_normal_f32.argtypes = [u64, u32, u64, u64, ctypes.c_float, ctypes.c_void_p]
         lib.synth_fill_x_bf16.restype = None
@@ -91,8 +94,14 @@ def splitmix_out(seed: int, n: int) -> int:
     return int(_host_lib().synth_splitmix_out(seed, n))
 
 
-def z_numerator(seed: int, tensor_id: int, i: int) -> int:
-    return int(_host_lib().synth_z_numerator(seed, tensor_id, i))
+def std_normal(seed: int, tensor_id: int, i: int) -> np.float32:
+    """Draw i of the (seed, tensor id) stream: a standard normal value in fp32."""
+    return np.float32(_host_lib().synth_std_normal(seed, tensor_id, i))
+
+
+def ln_f32(s: float) -> np.float32:
+    """The generator's own fp32 natural logarithm (positive normal arguments)."""
+    return np.float32(_host_lib().synth_ln_f32(s))
 
 
 def normal_f32(seed: int, tensor_id: int, start: int, n: int, sigma: float) -> np.ndarray:
@@ -113,7 +122,7 @@ def x_bf16(seed: int, T: int, H: int) -> np.ndarray:
 
 def router_sigma(H: int) -> float:
     """Router weight scale: the power of two nearest below 1/sqrt(H), so that logits of
-    unit-variance x have a standard deviation in [0.5, 1)."""
+    N(0, 1) x have a standard deviation in [0.5, 1)."""
     s = 1.0
     while s * s * H > 1.0:
         s *= 0.5

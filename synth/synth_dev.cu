@@ -2,8 +2,9 @@
 // synth_core.h).  Test and benchmark infrastructure: it fills full-size fp32
 // expert weights on the GPU, chunk by chunk, so that multi-gigabyte layers need
 // no host generation or upload.  Bit-identical to synth_fill_normal_f32 in
-// synth.c: integer hashing, an exact int->fp32 conversion, an exact
-// power-of-two scaling and one fp32 multiply rounded to nearest (__fmul_rn).
+// synth.c: integer hashing, exact conversions and the same sequence of fp32
+// operations, each rounded to nearest (the _rn intrinsics), then one
+// multiply by sigma (__fmul_rn).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -13,8 +14,7 @@ __global__ void synth_normal_f32_kernel(uint64_t key, uint64_t start, uint64_t n
                                         float sigma, float* __restrict__ out) {
   uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
   for (uint64_t j = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; j < n; j += stride) {
-    float z = __fmul_rn((float)synth_z_num(key, start + j), 0x1p-16f);
-    out[j] = __fmul_rn(sigma, z);
+    out[j] = __fmul_rn(sigma, synth_normal(key, start + j));
   }
 }
 

@@ -2,9 +2,13 @@
 
 Without the residual the chain must equal successive single-layer calls bit for bit (the fused
 combine + next-layer activation step keeps the unfused arithmetic and order).  With the residual
-it is compared with the oracle's chain under the layer's own bars: MXFP8 mode against the
-MXFP8-emulation oracle (rel-Frobenius <= 1e-2, max|err| <= 4e-2 * rms), bf16 mode against the
-exact oracle (rel-Frobenius <= 5e-3).  Those cases raise every E8M0 scale by 2 (weights x 4,
+it is compared with the oracle's chain under the layer's own bars, each against the oracle mode
+that applies the path's roundings: MXFP8 mode against the MXFP8-emulation oracle (rel-Frobenius
+<= 1e-2, max|err| <= 4e-2 * rms), bf16 mode against the bf16-emulation oracle, which rounds h
+to bf16 before GEMM2 as the mode does (rel-Frobenius <= 5e-3).  Against the exact chain those
+h roundings compound over the layers and their bf16 hand-offs: the oracle's own bf16-emulation
+chain already lies 4.7e-3 to 5.1e-3 from its exact chain on these cases, against 1.7e-3 for
+one layer.  Those cases raise every E8M0 scale by 2 (weights x 4,
 exactly) so that each layer's output is comparable to the residual stream it is added to (the
 stream's rms grows from 1 to between 1.2 and 4.6 over the layers).
 """
@@ -94,7 +98,7 @@ def test_chain_with_residual_matches_oracle(T, H, I, E, k, n, act, path):
     y = _chain(dev(xh), [dev(a) for a in lgh], [tuple(dev(a) for a in w) for w in wh], Ls[0],
                True, act, path)
     yg = bf16_to_f64(host_bf16(y))
-    mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_EXACT
+    mode = O.ACT_MXFP8 if act == moe.MOE_ACT_MXFP8 else O.ACT_BF16
     yref = bf16_to_f64(O.moe_chain(xh, lgh, wh, k, mode, residual=True))
     delta = yref - bf16_to_f64(xh)
     print(f"rms(x) {np.sqrt(np.mean(bf16_to_f64(xh) ** 2)):.3f} "

@@ -205,7 +205,7 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
   return launch_cooperative(gemm_tc_kernel<kN, kModeBoth>, grid, smem, stream, prm, first);
 }
 
-constexpr int kRouterNMax = 256;                        // router tokens per work item
+constexpr int kRouterNMax = 128;                        // router tokens per work item
 constexpr int kDenseNMax = 128;                         // projection tokens per work item
 constexpr int64_t kRouterPartBytes = 24ll << 20;       // cap on router split partials
 constexpr int64_t kDensePartBytes = 64ll << 20;        // cap on projection split partials
@@ -577,18 +577,25 @@ int enqueue_router(const void* x_bf16, const void* w_router, int T, int H, int E
   st.mark();
   const int vec = E % 4 == 0 ? 4 : 1;
   const dim3 grid(std::min(T, d->sms * 8));
-  const dim3 block(std::min(kTopkThreads, (kTopkGroups * (E / vec) + 31) / 32 * 32));
+  // above one token per SM (and up to 384 experts), two CTAs per SM
+  const bool two = T > d->sms && E <= 384;
+  const dim3 block(std::min(two ? kTopkThreads2 : kTopkThreads,
+                            (kTopkGroups * (E / vec) + 31) / 32 * 32));
   auto go = [&](auto kernel) {
     return launch_pdl(kernel, grid, block, 0, s, (const float*)part, P.k_splits, T, E, k, logits,
                       topk_idx, topk_w, d->status);
   };
   const cudaError_t e =
-      vec == 4 ? (E <= 128   ? go(splitk_topk_kernel<4, 4>)
-                  : E <= 384 ? go(splitk_topk_kernel<12, 4>)
-                             : go(splitk_topk_kernel<32, 4>))
-               : (E <= 128   ? go(splitk_topk_kernel<4, 1>)
-                  : E <= 384 ? go(splitk_topk_kernel<12, 1>)
-                             : go(splitk_topk_kernel<32, 1>));
+      two ? (vec == 4 ? (E <= 128 ? go(splitk_topk_kernel<4, 4, 2>)
+                                  : go(splitk_topk_kernel<12, 4, 2>))
+                      : (E <= 128 ? go(splitk_topk_kernel<4, 1, 2>)
+                                  : go(splitk_topk_kernel<12, 1, 2>)))
+      : vec == 4 ? (E <= 128   ? go(splitk_topk_kernel<4, 4, 1>)
+                    : E <= 384 ? go(splitk_topk_kernel<12, 4, 1>)
+                               : go(splitk_topk_kernel<32, 4, 1>))
+                 : (E <= 128   ? go(splitk_topk_kernel<4, 1, 1>)
+                    : E <= 384 ? go(splitk_topk_kernel<12, 1, 1>)
+                               : go(splitk_topk_kernel<32, 1, 1>));
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   st.launched();
   return MOE_OK;

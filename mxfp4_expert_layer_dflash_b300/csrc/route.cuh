@@ -111,10 +111,15 @@ __device__ __forceinline__ void route_topk_token(const float* __restrict__ logit
 constexpr int kTopkGroups = 8, kTopkLoads = 8;
 constexpr int kTopkMaxSplits = kTopkGroups * kTopkLoads;
 constexpr int kTopkThreads = 1024;
-template <int MAXPL, int kVec>
-__global__ void __launch_bounds__(kTopkThreads) splitk_topk_kernel(
-    const float* __restrict__ part, int k_splits, int T, int E, int k, float* __restrict__ logits,
-    int32_t* __restrict__ idx, float* __restrict__ w, int* status) {
+// kCtas = 2: two CTAs of at most kTopkThreads2 threads share an SM (fewer
+// registers each), so one wave covers twice the tokens — for token counts
+// above one CTA per SM; kCtas = 1 keeps every load of a thread in registers
+constexpr int kTopkThreads2 = 768;
+template <int MAXPL, int kVec, int kCtas>
+__global__ void __launch_bounds__(kCtas == 2 ? kTopkThreads2 : kTopkThreads, kCtas)
+    splitk_topk_kernel(const float* __restrict__ part, int k_splits, int T, int E, int k,
+                       float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ w,
+                       int* status) {
   static_assert(kVec == 1 || kVec == 4, "experts per thread");
   __shared__ __align__(16) float s_grp[kTopkGroups][32 * MAXPL];
   __shared__ __align__(16) float s_l[32 * MAXPL];

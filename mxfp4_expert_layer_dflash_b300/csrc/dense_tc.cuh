@@ -63,7 +63,9 @@ struct DenseCfg {
   static constexpr int kElemsPerBlock = kKind == kDenseBf16 ? 64 : 128;  // K elements / stage
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
   static_assert(kStageBytes % 1024 == 0, "stage alignment");
-  static_assert(kNMax % kDenseBoxRowsB == 0 && kNMax <= 256, "token block");
+  static_assert(kNMax % 16 == 0 && kNMax <= 256, "token block");
+  // (activation boxes of 16, 32 or 64 rows: a launch with kNMax < 64 only
+  // takes token counts whose box fits, T <= kNMax)
   static_assert(kKind == kDenseBf16 || kSfbCol + kNMax / 32 <= kSfStride, "B scale columns");
   static_assert(kSfBase + kStages * kSfStride <= kTmemCols, "TMEM budget");
   static_assert(kSmem <= 232448, "shared memory budget");

@@ -206,7 +206,11 @@ cudaError_t launch_gemm(int mode, int grid, cudaStream_t stream, const TcParams&
 }
 
 constexpr int kRouterNMax = 128;                        // router tokens per work item
-constexpr int kDenseNMax = 128;                         // projection tokens per work item
+// projection tokens per work item: up to 32 tokens a small B tile, so that
+// more stages of weights are in flight (11 against 7: T = 8 20.8 -> 18 us);
+// above, 128 (256-token items, one wave at T = 256, were slower: 35 -> 37 us)
+constexpr int kDenseNSmall = 32, kDenseNMax = 128;
+int dense_n_for(int T) { return T <= kDenseNSmall ? kDenseNSmall : kDenseNMax; }
 constexpr int64_t kRouterPartBytes = 24ll << 20;       // cap on router split partials
 constexpr int64_t kDensePartBytes = 64ll << 20;        // cap on projection split partials
 
@@ -285,6 +289,9 @@ int device_state(DeviceState** out) {
         cudaFuncSetAttribute(dense_tc_kernel<kDenseBf16, kRouterNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DenseCfg<kDenseBf16, kRouterNMax>::kSmem) != cudaSuccess ||
+        cudaFuncSetAttribute(dense_tc_kernel<kDenseMxf8, kDenseNSmall>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)DenseCfg<kDenseMxf8, kDenseNSmall>::kSmem) != cudaSuccess ||
         cudaFuncSetAttribute(dense_tc_kernel<kDenseMxf8, kDenseNMax>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)DenseCfg<kDenseMxf8, kDenseNMax>::kSmem) != cudaSuccess ||
@@ -1550,7 +1557,8 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
   DeviceState* d = nullptr;
   int rc = device_state(&d);
   if (rc) return rc;
-  const DensePlan P = plan_dense(N, T, K / 128, kDenseNMax, d->sms, kDensePartBytes);
+  const int n_max = dense_n_for(T);
+  const DensePlan P = plan_dense(N, T, K / 128, n_max, d->sms, kDensePartBytes);
   const size_t xq_bytes = align256((size_t)T * K), xs_bytes = align256((size_t)T * (K / 32));
   const size_t part_bytes = (size_t)P.k_splits * T * N * 4;
   void* ws = nullptr;
@@ -1584,10 +1592,15 @@ int moe_fp8_dense_forward(const void* x_bf16, const uint8_t* w_e4m3, const uint8
   dp.status = d->status;
   dp.timeout_ns = 2000000000ull;
   const int items = P.m_tiles * P.n_blocks * P.k_splits;
-  if (launch_pdl(dense_tc_kernel<kDenseMxf8, kDenseNMax>, dim3(std::min(items, d->sms)),
-                 dim3(kDenseThreads), DenseCfg<kDenseMxf8, kDenseNMax>::kSmem, stream, dp) !=
-      cudaSuccess)
-    return MOE_ERR_CUDA;
+  auto go = [&](auto kernel, size_t smem) {
+    return launch_pdl(kernel, dim3(std::min(items, d->sms)), dim3(kDenseThreads), smem, stream,
+                      dp);
+  };
+  const cudaError_t e =
+      n_max == kDenseNSmall
+          ? go(dense_tc_kernel<kDenseMxf8, kDenseNSmall>, DenseCfg<kDenseMxf8, kDenseNSmall>::kSmem)
+          : go(dense_tc_kernel<kDenseMxf8, kDenseNMax>, DenseCfg<kDenseMxf8, kDenseNMax>::kSmem);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (launch_pdl(splitk_reduce_bf16_kernel, dim3(grid_for((int64_t)T * N / 4, 256, d->sms * 8)),
                  dim3(256), 0, stream, (const float*)part, P.k_splits, T, N,

@@ -186,19 +186,24 @@ def test_forward_full_size_sampled(O, name):
 def test_forward_extreme_sizes_sampled(O, T, E, seed):
     """The full per-expert shape at the edges of the supported range: 4096 tokens (32768
     assignments: the permutation's many passes, wide chunks at scale) and the largest expert
-    count (E = 1024, 20 GB of packed weights).  Sampled tokens against the oracle."""
+    count (E = 1024, 20 GB of packed weights).  Sampled tokens against the oracle, in both
+    activation modes."""
     L = LY.Layer(f"edge_t{T}_e{E}", 6144, 2048, E, 8, T, seed)
     inp = device_layer(L)
     y = host_bf16(gpu_forward(L, inp))
+    yb = host_bf16(gpu_forward(L, inp, act_mode=moe.MOE_ACT_BF16))
     x, lg = LY.host_x(L), LY.host_logits(L)
     toks = _sample_tokens(T)
     ridx, _ = O.route(lg[toks], L.k)
     w = _oracle_layer(O, L, np.unique(ridx))
     _, yref, _ = O.moe_forward(x, lg, *w, L.k, O.ACT_MXFP8, tokens=toks)
+    _, yex, _ = O.moe_forward(x, lg, *w, L.k, O.ACT_EXACT, tokens=toks)
     yt = bf16_to_f64(y[toks])
     f, m = rel_fro(yt, yref), max_err_over_rms(yt, yref)
-    print(f"T={T} E={E}: mxfp8 fro={f:.3e} max/rms={m:.3e}")
+    fb = rel_fro(bf16_to_f64(yb[toks]), yex)
+    print(f"T={T} E={E}: mxfp8 fro={f:.3e} max/rms={m:.3e}; bf16 vs exact fro={fb:.3e}")
     assert f <= MXFP8_FRO and m <= MXFP8_MAX
+    assert fb <= BF16_FRO
     del inp
     torch.cuda.empty_cache()
 

@@ -113,7 +113,7 @@ def test_route_bit_exact(O, name):
 
 
 @pytest.mark.parametrize("T,E,k", [(1, 8, 2), (13, 8, 8), (300, 2, 1), (1024, 1024, 16),
-                                   (37, 64, 8), (5000, 384, 8)])
+                                   (37, 64, 8), (5000, 384, 8), (511, 64, 8), (513, 64, 8)])
 def test_route_ties_and_shapes(O, T, E, k):
     rng = np.random.default_rng(T + E)
     lg = (np.round(rng.standard_normal((T, E)) * 2) / 2).astype(np.float32)

@@ -323,7 +323,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // between rows, box of box_inner x box_rows, 128-byte swizzle
 int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
              uint64_t rows, uint64_t stride, uint32_t box_inner, uint32_t box_rows,
-             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+             CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+             CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
   auto enc = tensor_map_encoder();
   if (!enc) return MOE_ERR_CUDA;
   const cuuint64_t dims[2] = {inner, rows};
@@ -331,8 +332,8 @@ int make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t 
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, promo,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -797,18 +798,25 @@ int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, 
 // The MXFP8 GEMMs' parameters: phase 0 = GEMM1 (gate/up rows paired, SwiGLU
 // epilogue into hq/hs), phase 1 = GEMM2 (output rows r and r + 128 paired,
 // fp32 rows into yp)
+// `two_launch`: the GEMMs run as two launches (the large layers); their
+// weight copies promote L2 fills to 128 bytes instead of 256 (full_t256 1259
+// -> 1255 us; the one-launch GEMMs of the small layers are faster with 256:
+// full_t8 231.5 against 233.7 us)
 int mxfp8_gemm_params(const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                       const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
-                      DeviceState* d, unsigned long long timeout_ns, TcParams& p) {
+                      DeviceState* d, unsigned long long timeout_ns, TcParams& p,
+                      bool two_launch = false) {
   const int TK = T * k;
   TcPhase& g1 = p.ph[0];
   TcPhase& g2 = p.ph[1];
+  const CUtensorMapL2promotion wp =
+      two_launch ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   int rc;
   if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
-                     H / 2, 128, 128)) ||
+                     H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, wp)) ||
       (rc = make_map(&g1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)) ||
       (rc = make_map(&g2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
-                     I / 2, 128, 128)) ||
+                     I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, wp)) ||
       (rc = make_map(&g2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
     return rc;
   g1.w_sf = w13s;
@@ -929,8 +937,15 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
   const bool bf_wide = chunk_for(act, T) == kChunkBf16Wide;
   int rc = MOE_OK;
   if (act == MOE_ACT_MXFP8) {
+    // both GEMMs in one launch: the chain's MOE_PATH_PERSISTENT asks for it
+    // too (the chain has no whole-layer launch)
+    bool persistent = path == MOE_PATH_GEMMS || path == MOE_PATH_PERSISTENT ||
+                      (path == MOE_PATH_AUTO &&
+                       auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_GEMMS);
     TcParams p{};
-    if ((rc = mxfp8_gemm_params(w13, w13s, w2, w2s, T, H, I, E, k, w, d, timeout_ns, p))) return rc;
+    if ((rc = mxfp8_gemm_params(w13, w13s, w2, w2s, T, H, I, E, k, w, d, timeout_ns, p,
+                                !persistent)))
+      return rc;
     TcPhase g1 = p.ph[0], g2 = p.ph[1];
     auto launch = [&](int mode, const TcParams& prm) {
       const cudaError_t e = wide ? launch_gemm<kChunkWide>(mode, d->sms, stream, prm)
@@ -938,11 +953,6 @@ int enqueue_gemms(int act, int path, const uint8_t* w13, const uint8_t* w13s, co
       if (e == cudaSuccess) st.launched();
       return e;
     };
-    // both GEMMs in one launch: the chain's MOE_PATH_PERSISTENT asks for it
-    // too (the chain has no whole-layer launch)
-    bool persistent = path == MOE_PATH_GEMMS || path == MOE_PATH_PERSISTENT ||
-                      (path == MOE_PATH_AUTO &&
-                       auto_path(T, H, I, E, k, act, d->sms) == MOE_PATH_GEMMS);
     p.early_chunks = chunks_before ? 1 : 0;
     if (persistent) {  // both GEMMs in one launch
       g2.dep_target = 4 * g1.m_tiles;  // four epilogue warps publish per tile pair

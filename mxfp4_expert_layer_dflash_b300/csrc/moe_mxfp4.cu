@@ -798,10 +798,11 @@ int enqueue_act(int act, const uint16_t* x, const Work& w, int T, int H, int k, 
 // The MXFP8 GEMMs' parameters: phase 0 = GEMM1 (gate/up rows paired, SwiGLU
 // epilogue into hq/hs), phase 1 = GEMM2 (output rows r and r + 128 paired,
 // fp32 rows into yp)
-// `two_launch`: the GEMMs run as two launches (the large layers); their
-// weight copies promote L2 fills to 128 bytes instead of 256 (full_t256 1259
-// -> 1255 us; the one-launch GEMMs of the small layers are faster with 256:
-// full_t8 231.5 against 233.7 us)
+// `two_launch`: the GEMMs run as two launches (the large layers); GEMM2's
+// weight copies then promote L2 fills to 128 bytes instead of 256 (one box,
+// back to back: full_t256 1275 -> 1267.5 us, GEMM2 417 -> 408 us; GEMM1 is
+// faster with 256, 842 against 853 us, and so are the one-launch GEMMs of the
+// small layers)
 int mxfp8_gemm_params(const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                       const uint8_t* w2s, int T, int H, int I, int E, int k, const Work& w,
                       DeviceState* d, unsigned long long timeout_ns, TcParams& p,
@@ -809,14 +810,14 @@ int mxfp8_gemm_params(const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2
   const int TK = T * k;
   TcPhase& g1 = p.ph[0];
   TcPhase& g2 = p.ph[1];
-  const CUtensorMapL2promotion wp =
+  const CUtensorMapL2promotion wp2 =
       two_launch ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B : CU_TENSOR_MAP_L2_PROMOTION_L2_256B;
   int rc;
   if ((rc = make_map(&g1.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w13, H, (uint64_t)E * 2 * I,
-                     H / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, wp)) ||
+                     H / 2, 128, 128)) ||
       (rc = make_map(&g1.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.xq, H, TK, H, 128, kBoxRowsB)) ||
       (rc = make_map(&g2.map_w, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, w2, I, (uint64_t)E * H,
-                     I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, wp)) ||
+                     I / 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B, wp2)) ||
       (rc = make_map(&g2.map_x, CU_TENSOR_MAP_DATA_TYPE_UINT8, w.hq, I, TK, I, 128, kBoxRowsB)))
     return rc;
   g1.w_sf = w13s;

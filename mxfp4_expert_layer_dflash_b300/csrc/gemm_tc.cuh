@@ -320,6 +320,15 @@ __device__ __forceinline__ bool wait_chunk_ready(const TcParams& p, int chunk, i
   return true;
 }
 
+// L2 priority of a weight tile copy.  GEMM1's tiles take the normal class: when
+// an expert's tokens fill several chunks, its tiles are read once per chunk, and
+// evict-first lines tend to be gone by the second read (measured: the 256- and
+// 1024-token layers ran about 1% faster).  GEMM2's tiles, each read while its
+// chunk's intermediate rows are live in L2, keep evict-first.
+__device__ __forceinline__ uint64_t weight_policy(int phase) {
+  return phase == 0 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
+}
+
 // The kernel body of every mode.  `lay`/`n_layers`: the layers of a chained
 // whole-layer launch (lay null: one layer, described by p itself).
 template <int kNMax, int kMode>
@@ -411,7 +420,6 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
     const int nch = p.meta[0];
     const int items0 = nch * p.ph[0].m_tiles;
     const int items_all = items0 + (kPhases > 1 ? nch * p.ph[kPhases - 1].m_tiles : 0);
-    const uint64_t pol_w0 = ptx::policy_evict_first();
     int it = blockIdx.x, ks = 0;
     while (prefilled < (uint32_t)C::kStages && it < items_all) {
       const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
@@ -423,6 +431,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
       const uint32_t tx = C::kA * C::kTxA + (uint32_t)((ch.z + 15) & ~15) * 128;
       uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
       ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
+      const uint64_t pol_w0 = weight_policy(phase);
       ptx::tma_load_2d_warp(st, map_w(phase, 0), &full[prefilled], ks * kBlockK, row0, pol_w0);
       ptx::tma_load_2d_warp(st + C::kATile, map_w(phase, 0), &full[prefilled], ks * kBlockK,
                             row0 + ph.half, pol_w0);
@@ -497,7 +506,6 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
   if (route_in) {
     const int items0 = s_nchunks * m1, items_all = items0 + s_nchunks * m2;
     if (warp == 0) {
-      const uint64_t pol_w0 = ptx::policy_evict_first();
       int it = blockIdx.x, ks = 0;
       while (prefilled < (uint32_t)C::kStages && it < items_all) {
         const int phase = (kPhases > 1 && it >= items0) ? 1 : 0;
@@ -509,6 +517,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
         const uint32_t tx = C::kA * C::kTxA + (uint32_t)((ch.z + 15) & ~15) * 128;
         uint8_t* st = smem + prefilled * C::kStageBytes;  // first use of every stage: free
         ptx::mbar_arrive_expect_tx_warp(&full[prefilled], tx);
+        const uint64_t pol_w0 = weight_policy(phase);
         ptx::tma_load_2d_warp(st, map_w(phase, 0), &full[prefilled], ks * kBlockK, row0, pol_w0);
         ptx::tma_load_2d_warp(st + C::kATile, map_w(phase, 0), &full[prefilled], ks * kBlockK,
                               row0 + ph.half, pol_w0);
@@ -628,7 +637,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
     // ------------------------------------------------------------ TMA producer
     // Like the MMA issuer: a convergent warp walks the fills and one elected
     // lane issues each copy.
-    const uint64_t pol_w = ptx::policy_evict_first(), pol_x = ptx::policy_evict_last();
+    const uint64_t pol_x = ptx::policy_evict_last();
     uint32_t fill = 0;
     uint32_t a_until = prefilled;  // fills below this have their weight tiles issued
     bool ok = true;
@@ -657,6 +666,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
           }
           uint8_t* st = smem + s * C::kStageBytes;
           ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
+          const uint64_t pol_w = weight_policy(phase);
           ptx::tma_load_2d_warp(st, map_w(phase, l), &full[s], ks * kBlockK, row0, pol_w);
           ptx::tma_load_2d_warp(st + C::kATile, map_w(phase, l), &full[s], ks * kBlockK,
                                 row0 + ph.half, pol_w);
@@ -748,6 +758,7 @@ __device__ __forceinline__ void gemm_tc_body(const TcParams& p, const ChainLayer
               break;
             }
             ptx::mbar_arrive_expect_tx_warp(&full[s], tx);
+            const uint64_t pol_w = weight_policy(phase);
             ptx::tma_load_2d_warp(st, map_w(phase, l), &full[s], ks * kBlockK, row0, pol_w);
             ptx::tma_load_2d_warp(st + C::kATile, map_w(phase, l), &full[s], ks * kBlockK,
                                   row0 + ph.half, pol_w);

@@ -157,7 +157,8 @@ def _dense_gpu(x, T, K, N, seed):
 
 
 @pytest.mark.parametrize("T,K,N", [(16, 256, 384), (8, 6144, 6144), (300, 128, 96),
-                                   (1, 1024, 2048), (129, 512, 260)])
+                                   (1, 1024, 2048), (129, 512, 260), (33, 384, 200),
+                                   (32, 256, 260)])
 def test_dense_projection_within_one_ulp(O, T, K, N):
     seed = T + K + N
     x = S.x_bf16(seed, T, K)

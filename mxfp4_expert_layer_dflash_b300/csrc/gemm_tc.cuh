@@ -320,11 +320,13 @@ __device__ __forceinline__ bool wait_chunk_ready(const TcParams& p, int chunk, i
   return true;
 }
 
-// L2 priority of a weight tile copy.  GEMM1's tiles take the normal class: when
-// an expert's tokens fill several chunks, its tiles are read once per chunk, and
-// evict-first lines tend to be gone by the second read (measured: the 256- and
-// 1024-token layers ran about 1% faster).  GEMM2's tiles, each read while its
-// chunk's intermediate rows are live in L2, keep evict-first.
+// L2 priority of a weight tile copy.  Phase 0 of a launch (GEMM1 of the
+// both-GEMMs launch; the one GEMM of either launch of the two-launch path)
+// takes the normal class: when an expert's tokens fill several chunks, its
+// tiles are read once per chunk, and evict-first lines tend to be gone by the
+// second read (measured: the 256- and 1024-token layers ran about 1% faster,
+// the 1024-token one 1% slower again with GEMM2's launch back at evict-first).
+// GEMM2 of the both-GEMMs launch keeps evict-first.
 __device__ __forceinline__ uint64_t weight_policy(int phase) {
   return phase == 0 ? ptx::policy_evict_normal() : ptx::policy_evict_first();
 }
